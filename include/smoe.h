@@ -1,0 +1,144 @@
+/* smoe.h -- C ABI of libsmoe: the prompt-chunk (prefill) routed-expert block of a mixture-of-experts layer on one
+ * GB300 (sm_103a).
+ *
+ * The block, for a chunk of T tokens of hidden size H, E experts, top-K routing and expert FFN width F, runs as seven
+ * calls in this order (each the step of the same name in the Strata engine's prompt path -- page
+ * "src/prefill/prefill.cpp", Prefill::run, MoE half -- and its fused int8 expert contract -- page "Strata compare
+ * v0.1.35...v0.1.37", include/strata/prefill/moe_fused.hpp):
+ *
+ *   smoe_route_topk      router softmax, top-K of the E logits, weights renormalised over the K
+ *   smoe_group           stable counting sort of the T*K (token, k) pairs by expert: counts, offsets, src, slot, tiles
+ *   smoe_quantize_q8     activations to int8 once per token, one fp16 scale per 32 values
+ *   smoe_experts_gateup  grouped gate/up product of each routed row against its expert's 2-bit weights
+ *   smoe_swiglu_requant  h = silu(gate) * up, requantised to int8 per 32 values
+ *   smoe_experts_down    grouped down product into one fp32 row per routed pair
+ *   smoe_combine         Y[t] = sum_k w[t][k] * Dm[slot[t*K+k]] (gather form, no atomics)
+ *
+ * FORMATS (all row-major, little-endian):
+ *   q8 activations   codes int8 [rows][cols] and scales fp16 (as uint16 bits) [rows][cols/32].  A block of 32 values
+ *                    x has amax = max|x|, d = fp16_rne(amax / 127.0f) (IEEE fp32 division) and codes
+ *                    q = clamp(roundf(x / float(d)), -127, 127) (IEEE fp32 division, roundf = half away from zero);
+ *                    d == 0 gives all-zero codes.  The value of a code is d * q.
+ *   Q2 weights       per matrix, all E experts contiguous: codes uint8 [E][rows][cols/4], weight 4j+i of a row in
+ *                    bits 2i..2i+1 of byte j; scales fp16 [E][rows][cols/32].  The value of a weight is d * (q - 2),
+ *                    q in {0,1,2,3}.  Gate/up matrix: rows [0, F) gate, [F, 2F) up, cols H.  Down matrix: rows H,
+ *                    cols F.
+ *   tiles            int32 [4 + 4 * smoe_max_tiles(n, E)]: header {n_tiles, group_status, n, kernel_status}, then
+ *                    per tile {expert, first row, rows, 0}; each expert's c rows split into ceil(c/256) near-equal
+ *                    tiles [floor(i*c/nt), floor((i+1)*c/nt)), experts in id order.
+ *
+ * CONVENTIONS
+ *   - Every pointer argument is a DEVICE pointer owned by the caller; the library allocates nothing and keeps no
+ *     state between calls.  Every buffer must be 16-byte aligned.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream) and never
+ *     synchronises with the host.
+ *   - A call returns SMOE_OK or an error found on the host before anything is launched (a bad argument, an
+ *     unsupported shape, a device that is not sm_103) or a launch error (SMOE_ERR_LAUNCH, with the CUDA error
+ *     cleared).  Errors found on the device (a routed id outside [0, E), a kernel's internal wait that ran out) are
+ *     written to the tiles header, which the caller reads after the stream has run:
+ *     header[1] = SMOE_ERR_RANGE, header[3] = SMOE_ERR_TIMEOUT.  No call traps, asserts or exits.
+ *   - Calls on different streams that share an output buffer race; the library does no locking.
+ */
+#ifndef SMOE_H
+#define SMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int smoe_status;
+#define SMOE_OK 0
+#define SMOE_ERR_ARG 1          /* null or misaligned pointer, or a size out of range */
+#define SMOE_ERR_LAUNCH 2       /* a kernel launch failed (cudaGetLastError was not cudaSuccess) */
+#define SMOE_ERR_UNSUPPORTED 3  /* a shape the kernels do not cover, or a device other than sm_103 */
+#define SMOE_ERR_RANGE 4        /* (device, tiles header[1]) a routed id outside [0, E) */
+#define SMOE_ERR_TIMEOUT 5      /* (device, tiles header[3]) a kernel's internal wait gave up; outputs undefined */
+
+/* Largest supported sizes. */
+#define SMOE_MAX_EXPERTS 1024
+#define SMOE_MAX_TOPK 32
+#define SMOE_TILE_ROWS 256
+
+/* Human-readable name of a status code (static storage). */
+const char* smoe_status_string(smoe_status s);
+
+/* SMOE_OK when the current CUDA device is an sm_103 part the kernels were built for. */
+smoe_status smoe_device_check(void);
+
+/* Most tiles smoe_group can emit for n pairs over E experts: ceil(n / 256) + min(E, n). */
+int64_t smoe_max_tiles(int64_t n, int E);
+/* Bytes of the tiles buffer: 16 * (1 + smoe_max_tiles(n, E)). */
+size_t smoe_tiles_bytes(int64_t n, int E);
+/* Bytes of smoe_group's scratch space for n pairs over E experts. */
+size_t smoe_group_work_bytes(int64_t n, int E);
+
+/* Step 1 -- route.  Page "src/prefill/prefill.cpp", Prefill::run, MoE half: route(logits, ids, w, T, n_expert) after
+ * the router projection; the engine's "fused 512-expert top-10 router".
+ *   logits  fp32 [T][E] router logits (finite).
+ *   ids     int32 [T][K] out: the K largest logits of each token, largest first; ties go to the lower expert id
+ *           (the engine's top-k tie rule, page "Strata compare v0.1.35...v0.1.37", qsa_select.hpp).
+ *   w       fp32 [T][K] out: softmax restricted to the K and renormalised,
+ *           w_k = exp(l_k - l_1) / sum_j exp(l_j - l_1) (the full softmax denominator cancels).
+ *   1 <= K <= min(E, 32), 1 <= E <= 1024, T >= 0 (T == 0 launches nothing). */
+smoe_status smoe_route_topk(const float* logits, int64_t T, int E, int K, int32_t* ids, float* w, void* stream);
+
+/* Step 2 -- group.  Page "src/prefill/prefill.cpp", Prefill::run: the host loop that groups the (token, k) pairs by
+ * expert (counts, exclusive offsets, then in pair order slot[i] = the next row of expert ids[i] and
+ * src[row] = i / K); page "Strata compare v0.1.35...v0.1.37", moe_fused.hpp group(): the same tables built on the
+ * GPU, plus a tile list, so that the host never waits for the routing.  The order is stable (by pair index).
+ *   ids      int32 [T][K] (n = T*K pairs, pair i = t*K + k).
+ *   counts   int32 [E] out;  offsets int32 [E+1] out (offsets[E] = n);  src int32 [n] out;  slot int32 [n] out.
+ *   tiles    int32 out, tiles_bytes >= smoe_tiles_bytes(n, E).
+ *   work     scratch, work_bytes >= smoe_group_work_bytes(n, E); its contents are undefined afterwards.
+ * An id outside [0, E) sets tiles header[1] = SMOE_ERR_RANGE; the pair is then left out of every table and the
+ * expert calls do no work for that chunk. */
+smoe_status smoe_group(const int32_t* ids, int64_t T, int K, int E, int32_t* counts, int32_t* offsets, int32_t* src,
+                       int32_t* slot, int32_t* tiles, size_t tiles_bytes, void* work, size_t work_bytes,
+                       void* stream);
+
+/* Step 3 -- q8 activations.  Page "Strata compare v0.1.35...v0.1.37", moe_fused.hpp quantize_act: the layer input is
+ * rounded to int8 once per TOKEN (not per routed slot) with one scale per 32 values.
+ *   x fp32 [rows][cols] (|x| < 65504) -> codes int8 [rows][cols], scales fp16 [rows][cols/32].  cols % 32 == 0. */
+smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales, void* stream);
+
+/* Step 4 -- grouped gate/up.  moe_fused.hpp experts(): gate/up from the per-token int8 activations through the rows
+ * `src` of group; per routed row r of expert e and output j in [0, 2F):
+ *   GU[r][j] = sum_b dW[e][j][b] * dX[src r][b] * sum_{i in block b} (qW - 2) * qX     (fp32 result)
+ *   xc, xs   q8 activations of the chunk, [T][H] and [T][H/32].
+ *   src, tiles  from smoe_group (tiles header[3] receives SMOE_ERR_TIMEOUT).   n = T*K (sizes the launch).
+ *   wc, ws   gate/up weights, codes [E][2F][H/4], scales [E][2F][H/32].
+ *   gu       fp32 [n][2F] out, row r = routed row r.
+ *   H % 128 == 0, F % 64 == 0. */
+smoe_status smoe_experts_gateup(const int8_t* xc, const uint16_t* xs, const int32_t* src, int32_t* tiles,
+                                int64_t n, int E, const uint8_t* wc, const uint16_t* ws, int H, int F, float* gu,
+                                void* stream);
+
+/* Step 5 -- SwiGLU and requantisation.  Page "src/prefill/prefill.cpp": mmq::swiglu(GU, H, rows, ...) then the
+ * int8 rounding of H; moe_fused.hpp: "SwiGLU, H as int8".
+ *   gu fp32 [n][2F] -> h_j = silu(gu[r][j]) * gu[r][F + j] (fp32; silu(g) = g / (1 + exp(-g))), then the q8 rule:
+ *   hc int8 [n][F], hs fp16 [n][F/32].  F % 32 == 0. */
+smoe_status smoe_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, void* stream);
+
+/* Step 6 -- grouped down.  moe_fused.hpp experts(): "down into dm [n][2560] FP32 at the rows of group":
+ *   Dm[r][o] = sum_b dW[e][o][b] * dH[r][b] * sum_{i in block b} (qW - 2) * qH,   o in [0, H)
+ *   hc, hs   q8 H rows [n][F], [n][F/32] (routed-row order).   tiles from smoe_group.
+ *   wc, ws   down weights, codes [E][H][F/4], scales [E][H][F/32].
+ *   dm       fp32 [n][H] out.   H % 128 == 0, F % 64 == 0. */
+smoe_status smoe_experts_down(const int8_t* hc, const uint16_t* hs, int32_t* tiles, int64_t n, int E,
+                              const uint8_t* wc, const uint16_t* ws, int H, int F, float* dm, void* stream);
+
+/* Step 7 -- combine.  The combine that reads the per-slot rows (page "src/prefill/prefill.cpp", the engine's
+ * "fused CUDA weighted reduction"): Y[t][o] = sum_{k=0}^{K-1} w[t][k] * dm[slot[t*K+k]][o], summed in k order in
+ * fp32; each token gathers its own K rows, so no output is written twice and no atomics are used.
+ *   dm fp32 [n][H], slot int32 [T*K], w fp32 [T][K] -> y fp32 [T][H].   H % 4 == 0. */
+smoe_status smoe_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
+                         void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMOE_H */

@@ -1,0 +1,234 @@
+"""Thin Python binding of libsmoe's C ABI (include/smoe.h): the same seven calls, argument marshalling only.
+
+Every step runs in the CUDA kernels of libsmoe.so; this module checks tensor types and shapes, passes raw device
+pointers and the current CUDA stream, and raises SmoeError on a non-OK status.  There is no fallback: when the
+library is missing or the device is not an sm_103 part, the calls raise.
+
+``SmoeBlock`` holds the intermediate buffers of one chunk size (allocated once with PyTorch) and runs the seven
+calls in order; it is what the tests and the benchmark drive.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libsmoe.so")
+
+SMOE_OK, SMOE_ERR_ARG, SMOE_ERR_LAUNCH, SMOE_ERR_UNSUPPORTED, SMOE_ERR_RANGE, SMOE_ERR_TIMEOUT = range(6)
+TILE_ROWS = 256
+
+
+class SmoeError(RuntimeError):
+    def __init__(self, call: str, status: int, text: str):
+        super().__init__(f"{call}: status {status} ({text})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+_SIGS = {
+    "smoe_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "smoe_device_check": ([], ctypes.c_int),
+    "smoe_max_tiles": ([ctypes.c_int64, ctypes.c_int], ctypes.c_int64),
+    "smoe_tiles_bytes": ([ctypes.c_int64, ctypes.c_int], ctypes.c_size_t),
+    "smoe_group_work_bytes": ([ctypes.c_int64, ctypes.c_int], ctypes.c_size_t),
+    "smoe_route_topk": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                         ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_group": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                    ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    "smoe_quantize_q8": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                          ctypes.c_void_p], ctypes.c_int),
+    "smoe_experts_gateup": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                             ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_swiglu_requant": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                             ctypes.c_void_p], ctypes.c_int),
+    "smoe_experts_down": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                           ctypes.c_void_p], ctypes.c_int),
+    "smoe_combine": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                      ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+}
+
+# every symbol include/smoe.h declares
+EXPORTS = tuple(_SIGS)
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libsmoe.so and set the C signatures (no GPU needed to load it)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"libsmoe.so is missing at {path}: build it first (__graft_entry__.build() or "
+                                   "python quantized_routed_expert_smoe_gb300/build.py); there is no fallback path")
+            L = ctypes.CDLL(path)
+            for name, (args, res) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().smoe_status_string(status).decode()
+
+
+def _check(call: str, status: int):
+    if status != SMOE_OK:
+        raise SmoeError(call, status, status_string(status))
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _dev(t: torch.Tensor, dtype, name: str):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def device_check():
+    _check("smoe_device_check", load_library().smoe_device_check())
+
+
+def max_tiles(n: int, E: int) -> int:
+    return int(load_library().smoe_max_tiles(n, E))
+
+
+def tiles_bytes(n: int, E: int) -> int:
+    return int(load_library().smoe_tiles_bytes(n, E))
+
+
+def group_work_bytes(n: int, E: int) -> int:
+    return int(load_library().smoe_group_work_bytes(n, E))
+
+
+# ------------------------------------------------------------------------------------------------ the seven calls
+def smoe_route_topk(logits, ids, w, stream=None):
+    T, E = logits.shape
+    K = ids.shape[1]
+    _check("smoe_route_topk", load_library().smoe_route_topk(
+        _dev(logits, torch.float32, "logits"), T, E, K, _dev(ids, torch.int32, "ids"), _dev(w, torch.float32, "w"),
+        _stream(stream)))
+
+
+def smoe_group(ids, E, counts, offsets, src, slot, tiles, work, stream=None):
+    T, K = ids.shape
+    _check("smoe_group", load_library().smoe_group(
+        _dev(ids, torch.int32, "ids"), T, K, E, _dev(counts, torch.int32, "counts"),
+        _dev(offsets, torch.int32, "offsets"), _dev(src, torch.int32, "src"), _dev(slot, torch.int32, "slot"),
+        _dev(tiles, torch.int32, "tiles"), tiles.numel() * 4, _dev(work, torch.uint8, "work"), work.numel(),
+        _stream(stream)))
+
+
+def smoe_quantize_q8(x, codes, scales, stream=None):
+    rows, cols = x.shape
+    _check("smoe_quantize_q8", load_library().smoe_quantize_q8(
+        _dev(x, torch.float32, "x"), rows, cols, _dev(codes, torch.int8, "codes"),
+        _dev(scales, torch.int16, "scales"), _stream(stream)))
+
+
+def smoe_experts_gateup(xc, xs, src, tiles, n, wc, ws, gu, stream=None):
+    E, twoF, H4 = wc.shape
+    _check("smoe_experts_gateup", load_library().smoe_experts_gateup(
+        _dev(xc, torch.int8, "xc"), _dev(xs, torch.int16, "xs"), _dev(src, torch.int32, "src"),
+        _dev(tiles, torch.int32, "tiles"), n, E, _dev(wc, torch.uint8, "wc"), _dev(ws, torch.int16, "ws"),
+        H4 * 4, twoF // 2, _dev(gu, torch.float32, "gu"), _stream(stream)))
+
+
+def smoe_swiglu_requant(gu, hc, hs, stream=None):
+    n, twoF = gu.shape
+    _check("smoe_swiglu_requant", load_library().smoe_swiglu_requant(
+        _dev(gu, torch.float32, "gu"), n, twoF // 2, _dev(hc, torch.int8, "hc"), _dev(hs, torch.int16, "hs"),
+        _stream(stream)))
+
+
+def smoe_experts_down(hc, hs, tiles, n, wc, ws, dm, stream=None):
+    E, H, F4 = wc.shape
+    _check("smoe_experts_down", load_library().smoe_experts_down(
+        _dev(hc, torch.int8, "hc"), _dev(hs, torch.int16, "hs"), _dev(tiles, torch.int32, "tiles"), n, E,
+        _dev(wc, torch.uint8, "wc"), _dev(ws, torch.int16, "ws"), H, F4 * 4, _dev(dm, torch.float32, "dm"),
+        _stream(stream)))
+
+
+def smoe_combine(dm, slot, w, y, stream=None):
+    T, K = w.shape
+    H = y.shape[1]
+    _check("smoe_combine", load_library().smoe_combine(
+        _dev(dm, torch.float32, "dm"), _dev(slot, torch.int32, "slot"), _dev(w, torch.float32, "w"), T, K, H,
+        _dev(y, torch.float32, "y"), _stream(stream)))
+
+
+# ------------------------------------------------------------------------------------------------ one block
+class SmoeBlock:
+    """The routed-expert block for chunks of up to T tokens: weights resident on the device, every intermediate
+    buffer allocated once.  run(logits, x) issues the seven calls on the current stream and returns y [T][H]."""
+
+    def __init__(self, T: int, H: int, E: int, K: int, F: int, wgu_c, wgu_s, wd_c, wd_s, device="cuda"):
+        load_library()
+        device_check()
+        self.T, self.H, self.E, self.K, self.F = T, H, E, K, F
+        dev = torch.device(device)
+        as_t = lambda a, dt: torch.as_tensor(a).to(device=dev, dtype=dt).contiguous()
+        self.wgu_c = as_t(wgu_c, torch.uint8) if not isinstance(wgu_c, torch.Tensor) else wgu_c.to(dev).contiguous()
+        self.wgu_s = _as_i16(wgu_s, dev)
+        self.wd_c = as_t(wd_c, torch.uint8) if not isinstance(wd_c, torch.Tensor) else wd_c.to(dev).contiguous()
+        self.wd_s = _as_i16(wd_s, dev)
+        n = T * K
+        self.n = n
+        e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)
+        self.ids = e(T, K, dt=torch.int32)
+        self.w = e(T, K, dt=torch.float32)
+        self.counts = e(E, dt=torch.int32)
+        self.offsets = e(E + 1 + 3, dt=torch.int32)  # padded to 16 bytes
+        self.src = e(max(n, 4), dt=torch.int32)
+        self.slot = e(max(n, 4), dt=torch.int32)
+        self.tiles = e(tiles_bytes(n, E) // 4, dt=torch.int32)
+        self.work = e(max(group_work_bytes(n, E), 16), dt=torch.uint8)
+        self.xc = e(T, H, dt=torch.int8)
+        self.xs = e(T, H // 32, dt=torch.int16)
+        self.gu = e(n, 2 * F, dt=torch.float32)
+        self.hc = e(n, F, dt=torch.int8)
+        self.hs = e(n, F // 32, dt=torch.int16)
+        self.dm = e(n, H, dt=torch.float32)
+        self.y = e(T, H, dt=torch.float32)
+
+    def run(self, logits, x, stream=None):
+        smoe_route_topk(logits, self.ids, self.w, stream)
+        smoe_group(self.ids, self.E, self.counts, self.offsets, self.src[:self.n], self.slot[:self.n], self.tiles,
+                   self.work, stream)
+        smoe_quantize_q8(x, self.xc, self.xs, stream)
+        smoe_experts_gateup(self.xc, self.xs, self.src, self.tiles, self.n, self.wgu_c, self.wgu_s, self.gu, stream)
+        smoe_swiglu_requant(self.gu, self.hc, self.hs, stream)
+        smoe_experts_down(self.hc, self.hs, self.tiles, self.n, self.wd_c, self.wd_s, self.dm, stream)
+        smoe_combine(self.dm, self.slot, self.w, self.y, stream)
+        return self.y
+
+    def device_status(self):
+        """(group status, kernel status) from the tiles header; reads the device (synchronises)."""
+        h = self.tiles[:4].cpu().tolist()
+        return h[1], h[3]
+
+
+def _as_i16(a, dev):
+    if isinstance(a, torch.Tensor):
+        return a.to(dev).view(torch.int16).contiguous()
+    import numpy as np
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)

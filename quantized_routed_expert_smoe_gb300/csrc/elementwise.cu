@@ -1,0 +1,154 @@
+// elementwise.cu -- the HBM-bound steps of the routed-expert block: q8 quantisation of the activations (step 3),
+// SwiGLU + requantisation of the gate/up rows (step 5) and the weighted combine (step 7).
+//
+// Page "Strata compare v0.1.35...v0.1.37", include/strata/prefill/moe_fused.hpp: the layer input is rounded to int8
+// once per token with one scale per 32 values (quantize_act); gate/up is followed by SwiGLU and the int8 rounding of
+// H; down writes one row per routed pair that the combine reads.  Page "src/prefill/prefill.cpp": mmq::swiglu, and
+// the engine's fused weighted reduction of the K rows of each token.
+//
+// The q8 rule (the library's activation format): for 32 fp32 values, amax = max |x|, d = fp16_rne(amax / 127) with
+// an IEEE fp32 division, and q = clamp(roundf(x / float(d)), -127, 127), again an IEEE fp32 division, roundf
+// rounding half away from zero; d == 0 gives zero codes.  Four threads share a block, eight values each.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "smoe_device.cuh"
+#include "smoe_internal.h"
+
+namespace smoe {
+namespace {
+
+// q8 of the 8 values v held by this thread, its block being spread over 4 consecutive lanes; returns the 8 codes
+// packed little-endian and the block's fp16 scale bits.
+__device__ __forceinline__ uint2 q8_encode8(const float (&v)[8], uint16_t* scale_bits) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+    const float d = __half2float(dh);
+    *scale_bits = __half_as_ushort(dh);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int q = 0;
+        if (d != 0.0f) {
+            float r = roundf(__fdiv_rn(v[i], d));
+            r = fminf(fmaxf(r, -127.0f), 127.0f);
+            q = (int)r;
+        }
+        const uint32_t b = (uint32_t)(q & 0xff);
+        if (i < 4) lo |= b << (8 * i);
+        else hi |= b << (8 * (i - 4));
+    }
+    return make_uint2(lo, hi);
+}
+
+// step 3: x [rows][cols] -> codes, scales; thread i covers elements [8i, 8i + 8) of the flattened rows
+__global__ void __launch_bounds__(256) quantize_q8_kernel(const float4* __restrict__ x, int64_t n8,
+                                                          uint2* __restrict__ codes, uint16_t* __restrict__ scales) {
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < n8; base += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = base + threadIdx.x;
+        // n8 is a multiple of 4 (cols % 32 == 0), so every group of 4 lanes is either all in range or all out;
+        // lanes past the end still take part in the block's shuffles
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const bool in = i < n8;
+        if (in) {
+            const float4 a = __ldcs(x + 2 * i), b = __ldcs(x + 2 * i + 1);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        }
+        uint16_t sb;
+        const uint2 q = q8_encode8(v, &sb);
+        if (in) {
+            codes[i] = q;
+            if ((i & 3) == 0) scales[i >> 2] = sb;
+        }
+    }
+}
+
+// step 5: per routed row, h_j = silu(g_j) * u_j with g = gu[r][j], u = gu[r][F + j], then the q8 rule per 32 of h.
+// thread i covers h values [8c, 8c + 8) of row r = i / (F/8), c = i % (F/8).
+__global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __restrict__ gu, int64_t n, int F,
+                                                             uint2* __restrict__ hc, uint16_t* __restrict__ hs) {
+    const int64_t per_row = F / 8;
+    const int64_t total = n * per_row;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = base + threadIdx.x;
+        const bool in = i < total;
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (in) {
+            const int64_t r = i / per_row, c = i - r * per_row;
+            const float4* g4 = reinterpret_cast<const float4*>(gu + r * 2 * F + 8 * c);
+            const float4* u4 = reinterpret_cast<const float4*>(gu + r * 2 * F + F + 8 * c);
+            const float4 g0 = __ldcs(g4), g1 = __ldcs(g4 + 1), u0 = __ldcs(u4), u1 = __ldcs(u4 + 1);
+            const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const float u[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = __fdiv_rn(g[k], 1.0f + expf(-g[k])) * u[k];
+        }
+        uint16_t sb;
+        const uint2 q = q8_encode8(v, &sb);
+        if (in) {
+            hc[i] = q;  // row r's codes start at r * F = 8 * (r * per_row): element offset 8i
+            if ((i & 3) == 0) hs[i >> 2] = sb;
+        }
+    }
+}
+
+// step 7: Y[t][o] = sum_k w[t][k] * dm[slot[t*K+k]][o], in k order, fp32.  Block (t, y): 128 threads, a float4 each.
+// A slot outside [0, n) (a pair dropped for an out-of-range id) contributes nothing.
+__global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ dm, const int32_t* __restrict__ slot,
+                                                      const float* __restrict__ w, int K, int H, int64_t n,
+                                                      float* __restrict__ y) {
+    const int64_t t = blockIdx.x;
+    const int o4 = blockIdx.y * blockDim.x + threadIdx.x;
+    if (4 * o4 >= H) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < K; ++k) {
+        const int32_t r = __ldg(slot + t * K + k);
+        const float wk = __ldg(w + t * K + k);
+        if (r < 0 || r >= n) continue;
+        const float4 d = __ldcs(reinterpret_cast<const float4*>(dm + (int64_t)r * H) + o4);
+        acc.x = fmaf(wk, d.x, acc.x);
+        acc.y = fmaf(wk, d.y, acc.y);
+        acc.z = fmaf(wk, d.z, acc.z);
+        acc.w = fmaf(wk, d.w, acc.w);
+    }
+    reinterpret_cast<float4*>(y + t * H)[o4] = acc;
+}
+
+int grid_for(int64_t threads, int block) {
+    const int64_t blocks = (threads + block - 1) / block;
+    const int64_t cap = 152 * 16;  // a few waves of resident blocks; the kernels stride beyond this
+    return (int)(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales,
+                               cudaStream_t s) {
+    const int64_t n8 = rows * (int64_t)cols / 8;
+    if (n8 == 0) return cudaSuccess;
+    quantize_q8_kernel<<<grid_for(n8, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(x), n8,
+                                                        reinterpret_cast<uint2*>(codes), scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, cudaStream_t s) {
+    const int64_t total = n * (int64_t)(F / 8);
+    if (total == 0) return cudaSuccess;
+    swiglu_requant_kernel<<<grid_for(total, 256), 256, 0, s>>>(gu, n, F, reinterpret_cast<uint2*>(hc), hs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
+                           cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const dim3 grid((unsigned)T, (unsigned)((H / 4 + 127) / 128));
+    combine_kernel<<<grid, 128, 0, s>>>(dm, slot, w, K, H, T * (int64_t)K, y);
+    return cudaGetLastError();
+}
+
+}  // namespace smoe

@@ -1,0 +1,150 @@
+// smoe_api.cu -- the extern "C" entry points of libsmoe (declared and documented in include/smoe.h): host-side
+// argument checks, then the launches of each step on the caller's stream.  Nothing here allocates memory.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "smoe.h"
+#include "smoe_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }
+
+smoe_status launch_status(cudaError_t err) {
+    if (err == cudaSuccess) return SMOE_OK;
+    cudaGetLastError();  // clear a sticky launch error so that the caller's next call starts clean
+    return SMOE_ERR_LAUNCH;
+}
+
+// 1: sm_103 device, 0: not, cached per device
+int device_is_sm103() {
+    static int cache[64] = {0};  // 0 unknown, 1 yes, 2 no
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (dev >= 0 && dev < 64 && cache[dev] != 0) return cache[dev] == 1;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    const bool ok = major == 10 && minor == 3;
+    if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+    return ok;
+}
+
+constexpr int64_t kMaxGridY = 65535;
+
+}  // namespace
+
+extern "C" {
+
+const char* smoe_status_string(smoe_status s) {
+    switch (s) {
+        case SMOE_OK: return "ok";
+        case SMOE_ERR_ARG: return "bad argument (null or misaligned pointer, or a size out of range)";
+        case SMOE_ERR_LAUNCH: return "kernel launch failed";
+        case SMOE_ERR_UNSUPPORTED: return "unsupported shape or device (libsmoe runs on sm_103 only)";
+        case SMOE_ERR_RANGE: return "a routed expert id is outside [0, E)";
+        case SMOE_ERR_TIMEOUT: return "a kernel's internal wait ran out";
+        default: return "unknown status";
+    }
+}
+
+smoe_status smoe_device_check(void) { return device_is_sm103() ? SMOE_OK : SMOE_ERR_UNSUPPORTED; }
+
+int64_t smoe_max_tiles(int64_t n, int E) {
+    if (n <= 0 || E <= 0) return 0;
+    return (n + SMOE_TILE_ROWS - 1) / SMOE_TILE_ROWS + (n < E ? n : E);
+}
+
+size_t smoe_tiles_bytes(int64_t n, int E) { return (size_t)16 * (size_t)(1 + smoe_max_tiles(n, E)); }
+
+size_t smoe_group_work_bytes(int64_t n, int E) { return smoe::group_work_bytes(n, E); }
+
+smoe_status smoe_route_topk(const float* logits, int64_t T, int E, int K, int32_t* ids, float* w, void* stream) {
+    if (T < 0 || E < 1 || E > SMOE_MAX_EXPERTS || K < 1 || K > SMOE_MAX_TOPK || K > E) return SMOE_ERR_ARG;
+    if (T == 0) return SMOE_OK;
+    if (!aligned16(logits) || !aligned16(ids) || !aligned16(w)) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_route_topk(logits, T, E, K, ids, w, (cudaStream_t)stream));
+}
+
+smoe_status smoe_group(const int32_t* ids, int64_t T, int K, int E, int32_t* counts, int32_t* offsets, int32_t* src,
+                       int32_t* slot, int32_t* tiles, size_t tiles_bytes, void* work, size_t work_bytes,
+                       void* stream) {
+    if (T < 0 || E < 1 || E > SMOE_MAX_EXPERTS || K < 1 || K > SMOE_MAX_TOPK) return SMOE_ERR_ARG;
+    const int64_t n = T * K;
+    if (n > INT32_MAX / 2) return SMOE_ERR_ARG;
+    if (!aligned16(counts) || !aligned16(offsets) || !aligned16(tiles)) return SMOE_ERR_ARG;
+    if (n > 0 && (!aligned16(ids) || !aligned16(src) || !aligned16(slot))) return SMOE_ERR_ARG;
+    if (tiles_bytes < smoe_tiles_bytes(n, E)) return SMOE_ERR_ARG;
+    const size_t need = smoe_group_work_bytes(n, E);
+    if (n > 0 && (work_bytes < need || !aligned16(work))) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_group(ids, n, K, E, counts, offsets, src, slot, tiles,
+                                            reinterpret_cast<int32_t*>(work), (cudaStream_t)stream));
+}
+
+smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales, void* stream) {
+    if (rows < 0 || cols < 32 || cols % 32 != 0) return SMOE_ERR_ARG;
+    if (rows == 0) return SMOE_OK;
+    if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_quantize_q8(x, rows, cols, codes, scales, (cudaStream_t)stream));
+}
+
+static smoe_status check_gemm_shape(int64_t n, int E, int H, int F) {
+    if (n < 0 || E < 1 || E > SMOE_MAX_EXPERTS) return SMOE_ERR_ARG;
+    if (H < 128 || F < 64) return SMOE_ERR_UNSUPPORTED;
+    if (H % 128 != 0 || F % 64 != 0) return SMOE_ERR_UNSUPPORTED;
+    if (smoe_max_tiles(n, E) > kMaxGridY) return SMOE_ERR_UNSUPPORTED;
+    return SMOE_OK;
+}
+
+smoe_status smoe_experts_gateup(const int8_t* xc, const uint16_t* xs, const int32_t* src, int32_t* tiles,
+                                int64_t n, int E, const uint8_t* wc, const uint16_t* ws, int H, int F, float* gu,
+                                void* stream) {
+    const smoe_status st = check_gemm_shape(n, E, H, F);
+    if (st != SMOE_OK) return st;
+    if (n == 0) return SMOE_OK;
+    if (!aligned16(xc) || !aligned16(xs) || !aligned16(src) || !aligned16(tiles) || !aligned16(wc) ||
+        !aligned16(ws) || !aligned16(gu))
+        return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    smoe::ExpertsGemmArgs a{xc, xs, src, tiles, wc, ws, 2 * F, H, gu};
+    return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
+}
+
+smoe_status smoe_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, void* stream) {
+    if (n < 0 || F < 32 || F % 32 != 0) return SMOE_ERR_ARG;
+    if (n == 0) return SMOE_OK;
+    if (!aligned16(gu) || !aligned16(hc) || !aligned16(hs)) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_swiglu_requant(gu, n, F, hc, hs, (cudaStream_t)stream));
+}
+
+smoe_status smoe_experts_down(const int8_t* hc, const uint16_t* hs, int32_t* tiles, int64_t n, int E,
+                              const uint8_t* wc, const uint16_t* ws, int H, int F, float* dm, void* stream) {
+    const smoe_status st = check_gemm_shape(n, E, H, F);
+    if (st != SMOE_OK) return st;
+    if (n == 0) return SMOE_OK;
+    if (!aligned16(hc) || !aligned16(hs) || !aligned16(tiles) || !aligned16(wc) || !aligned16(ws) || !aligned16(dm))
+        return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    smoe::ExpertsGemmArgs a{hc, hs, nullptr, tiles, wc, ws, H, F, dm};
+    return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
+}
+
+smoe_status smoe_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
+                         void* stream) {
+    if (T < 0 || K < 1 || K > SMOE_MAX_TOPK || H < 4 || H % 4 != 0) return SMOE_ERR_ARG;
+    if (T == 0) return SMOE_OK;
+    if (!aligned16(dm) || !aligned16(slot) || !aligned16(w) || !aligned16(y)) return SMOE_ERR_ARG;
+    if ((H / 4 + 127) / 128 > kMaxGridY) return SMOE_ERR_UNSUPPORTED;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_combine(dm, slot, w, T, K, H, y, (cudaStream_t)stream));
+}
+
+}  // extern "C"

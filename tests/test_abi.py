@@ -1,0 +1,97 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU, exports every symbol include/smoe.h declares, and
+rejects bad arguments on the host before it touches a device (CPU only: no compute call runs here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantized_routed_expert_smoe_gb300 import build as smoe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "smoe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    smoe_build.build()
+    from quantized_routed_expert_smoe_gb300 import binding
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(smoe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_seven_steps():
+    names = declared_functions()
+    for step in ["smoe_route_topk", "smoe_group", "smoe_quantize_q8", "smoe_experts_gateup", "smoe_swiglu_requant",
+                 "smoe_experts_down", "smoe_combine"]:
+        assert step in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from quantized_routed_expert_smoe_gb300 import binding
+    names = declared_functions()
+    assert set(names) == set(binding.EXPORTS)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_sizing_helpers(lib):
+    from quantized_routed_expert_smoe_gb300 import binding
+    assert binding.max_tiles(81920, 512) == 320 + 512
+    assert binding.max_tiles(128, 16) == 1 + 16
+    assert binding.max_tiles(0, 16) == 0
+    assert binding.tiles_bytes(128, 16) == 16 * 18
+    assert binding.group_work_bytes(81920, 512) >= 512 * 4
+
+
+def test_host_side_rejections_need_no_gpu(lib):
+    fake = ctypes.c_void_p(1 << 20)          # 16-byte aligned, never dereferenced on these paths
+    odd = ctypes.c_void_p((1 << 20) + 4)     # misaligned
+    null = ctypes.c_void_p(0)
+    ARG, UNSUP = 1, 3
+    # route: K > E, E too large, null / misaligned pointers
+    assert lib.smoe_route_topk(fake, 4, 8, 9, fake, fake, null) == ARG
+    assert lib.smoe_route_topk(fake, 4, 2048, 2, fake, fake, null) == ARG
+    assert lib.smoe_route_topk(null, 4, 16, 2, fake, fake, null) == ARG
+    assert lib.smoe_route_topk(odd, 4, 16, 2, fake, fake, null) == ARG
+    assert lib.smoe_route_topk(fake, 0, 16, 2, fake, fake, null) == 0  # empty chunk: nothing to do
+    # q8: cols not a multiple of 32
+    assert lib.smoe_quantize_q8(fake, 4, 48, fake, fake, null) == ARG
+    # gemm shapes the kernels do not cover
+    assert lib.smoe_experts_gateup(fake, fake, fake, fake, 10, 4, fake, fake, 96, 64, fake, null) == UNSUP
+    assert lib.smoe_experts_down(fake, fake, fake, 10, 4, fake, fake, 256, 48, fake, null) == UNSUP
+    # group: tiles buffer too small
+    assert lib.smoe_group(fake, 8, 2, 4, fake, fake, fake, fake, fake, 16, fake, 1 << 20, null) == ARG
+    # well-formed arguments on a machine without an sm_103 device: a clean error, never a fallback
+    st = lib.smoe_route_topk(fake, 4, 16, 2, fake, fake, null)
+    if not _has_gpu():
+        assert st == UNSUP
+    assert lib.smoe_status_string(UNSUP).decode().startswith("unsupported")
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from quantized_routed_expert_smoe_gb300 import binding
+    saved = binding._lib
+    try:
+        binding._lib = None
+        with pytest.raises(RuntimeError, match="no fallback"):
+            binding.load_library(str(tmp_path / "libsmoe.so"))
+    finally:
+        binding._lib = saved
+
+
+def test_build_targets_sm103a_only():
+    assert smoe_build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]

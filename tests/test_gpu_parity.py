@@ -1,0 +1,424 @@
+"""Parity of libsmoe's CUDA path with the CPU oracle, through the C ABI (GPU: sm_103a).
+
+Bars (the library's contract):
+  * bit-exact: routing ids, counts / offsets / src / slot / tile list, q8 codes and scales of the activations;
+  * routing weights: |w_gpu - w_oracle| <= 2e-6 * w_oracle (fp32 exp and division against double);
+  * expert products (gate/up, down), per element: |gpu - oracle| <= 2e-6 * sum_i |w_i a_i| -- the fp32 accumulation
+    of exact products, with ~25x margin over its expected error and tight enough that a dropped hi/lo part or a lost
+    block fails;
+  * SwiGLU + requant on the same fp32 input: scales and codes equal except where the fp32 SwiGLU and the double one
+    straddle a rounding boundary (at most 1e-4 of the codes; each such code differs by 1 and sits within 1e-3 of a
+    .5 tie, each such scale sits within 1e-5 of an fp16 rounding midpoint);
+  * the block's output, per token row: max |y_gpu - y_oracle| <= 2e-3 * RMS(y_oracle row).
+Full-size chunks are compared on every routing / grouping / q8 value and on sampled rows for the products.
+"""
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from quantized_routed_expert_smoe_gb300 import synth
+
+from helpers import deq_a, deq_w, i16
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+FULL = ["t1024", "t8192", "t32768", "skew8192"]
+ALL = ["tiny"] + FULL
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_routed_expert_smoe_gb300 import build, binding
+    build.build()
+    binding.load_library()
+    binding.device_check()
+    return binding
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.cpu().numpy()
+
+
+_cache = {}
+
+
+def layer_inputs(name):
+    if name not in _cache:
+        _cache.clear()
+        _cache[name] = synth.make_layer(synth.CONFIGS[name])
+    return _cache[name]
+
+
+# ------------------------------------------------------------------------------------------------ route
+def gpu_route(B, logits, K):
+    T = logits.shape[0]
+    ids = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    B.smoe_route_topk(dev(logits), ids, w)
+    return host(ids), host(w)
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_route_bit_exact(B, name):
+    cfg = synth.CONFIGS[name]
+    inp = synth.make_layer(cfg, with_weights=False)
+    ids, w = gpu_route(B, inp["logits"], cfg.K)
+    ids_o, w_o = oracle.route(inp["logits"], cfg.K)
+    assert np.array_equal(ids, ids_o)
+    assert np.all(np.abs(w - w_o) <= 2e-6 * w_o)
+
+
+def test_route_edge_cases(B):
+    lg = np.zeros((5, 16), np.float32)
+    lg[0] = 1.0                                   # all tied: lowest ids first
+    lg[1, [3, 7, 9]] = 2.0                        # tie at the top
+    lg[2] = np.arange(16, dtype=np.float32)[::-1]  # descending already
+    lg[3] = -np.arange(16, dtype=np.float32)
+    lg[4, 15] = 5.0
+    for K in (1, 4, 16):
+        ids, w = gpu_route(B, lg, K)
+        ids_o, w_o = oracle.route(lg, K)
+        assert np.array_equal(ids, ids_o)
+        assert np.all(np.abs(w - w_o) <= 2e-6 * w_o)
+    rng = np.random.default_rng(7)
+    for E, K in ((1000, 10), (33, 32), (512, 1), (2, 2), (1024, 8)):
+        lg = (rng.standard_normal((67, E)) * 0.3).astype(np.float32)
+        lg[5, :] = np.round(lg[5, :] * 4) / 4     # many exact ties
+        ids, w = gpu_route(B, lg, K)
+        ids_o, w_o = oracle.route(lg, K)
+        assert np.array_equal(ids, ids_o), (E, K)
+        assert np.all(np.abs(w - w_o) <= 2e-6 * w_o), (E, K)
+
+
+# ------------------------------------------------------------------------------------------------ group
+def gpu_group(B, ids, E):
+    T, K = ids.shape
+    n = T * K
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 4, dtype=torch.int32, device="cuda")
+    src = torch.full((max(n, 4),), -7, dtype=torch.int32, device="cuda")
+    slot = torch.full((max(n, 4),), -7, dtype=torch.int32, device="cuda")
+    tiles = torch.full((B.tiles_bytes(n, E) // 4,), -7, dtype=torch.int32, device="cuda")
+    work = torch.empty(max(B.group_work_bytes(n, E), 16), dtype=torch.uint8, device="cuda")
+    B.smoe_group(dev(ids) if n else torch.empty(0, K, dtype=torch.int32, device="cuda").reshape(T, K), E, counts,
+                 offsets, src[:n] if n else src, slot[:n] if n else slot, tiles, work)
+    t = host(tiles)
+    nt = int(t[0])
+    return dict(counts=host(counts), offsets=host(offsets)[:E + 1], src=host(src)[:n], slot=host(slot)[:n],
+                tiles=t[4:4 + 4 * nt].reshape(nt, 4), header=t[:4], tiles_raw=t, src_full=host(src))
+
+
+def assert_group_equal(g, go):
+    for k in ("counts", "offsets", "src", "slot", "tiles"):
+        assert np.array_equal(g[k], go[k]), k
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_group_bit_exact(B, name):
+    cfg = synth.CONFIGS[name]
+    inp = synth.make_layer(cfg, with_weights=False)
+    ids, _ = oracle.route(inp["logits"], cfg.K)
+    g = gpu_group(B, ids, cfg.E)
+    assert g["header"][1] == 0 and g["header"][2] == ids.size
+    assert_group_equal(g, oracle.group(ids, cfg.E))
+
+
+def test_group_edge_cases(B):
+    # one expert takes every pair: several tiles, one ragged
+    ids = np.zeros((1000, 1), np.int32)
+    ids[::7] = 3
+    assert_group_equal(gpu_group(B, ids, 4), oracle.group(ids, 4))
+    # a long chunk over few experts (several scatter rounds per chunk, many chunks)
+    rng = np.random.default_rng(3)
+    ids = rng.integers(0, 5, size=(70001, 3)).astype(np.int32)
+    assert_group_equal(gpu_group(B, ids, 5), oracle.group(ids, 5))
+    ids = rng.integers(0, 1024, size=(3001, 7)).astype(np.int32)
+    assert_group_equal(gpu_group(B, ids, 1024), oracle.group(ids, 1024))
+    # a single pair
+    ids = np.array([[2]], np.int32)
+    assert_group_equal(gpu_group(B, ids, 4), oracle.group(ids, 4))
+    # an id out of range is reported in the header, never faults
+    ids = np.array([[0, 1], [9, 2]], np.int32)
+    g = gpu_group(B, ids, 4)
+    assert g["header"][1] == 4
+    ids = np.array([[0, -3]], np.int32)
+    assert gpu_group(B, ids, 4)["header"][1] == 4
+
+
+# ------------------------------------------------------------------------------------------------ q8
+def gpu_q8(B, x):
+    rows, cols = x.shape
+    codes = torch.empty(rows, cols, dtype=torch.int8, device="cuda")
+    scales = torch.empty(rows, cols // 32, dtype=torch.int16, device="cuda")
+    B.smoe_quantize_q8(dev(x), codes, scales)
+    return host(codes), host(scales).view(np.uint16)
+
+
+def test_quantize_bit_exact_full_and_edges(B):
+    x = layer_inputs("t8192")["x"]
+    c, s = gpu_q8(B, x)
+    co, so = oracle.quantize_q8(x)
+    assert np.array_equal(c, co) and np.array_equal(s, so)
+    # edge blocks: zeros, exact .5 ties at d = 1, subnormal and zero-rounding scales, clamping, huge values
+    rng = np.random.default_rng(1)
+    e = rng.standard_normal((9, 64)).astype(np.float32)
+    e[0] = 0
+    e[1, :32] = np.arange(32) - 15.5
+    e[1, 0] = 127.0
+    e[2, :32] = 1e-9
+    e[3, :32] = 1e-5 * rng.standard_normal(32)
+    e[4, :32] = 60000.0 * rng.standard_normal(32).clip(-1, 1)
+    e[5] = np.float32(2.5 * 129 / 16384)
+    e[5, 0] = 1.0
+    e[6] = -e[6]
+    e[7, :32] = np.float32(3.0e-8)
+    e[8] = rng.standard_normal(64).astype(np.float32) * 1e3
+    c, s = gpu_q8(B, e)
+    co, so = oracle.quantize_q8(e)
+    assert np.array_equal(c, co) and np.array_equal(s, so)
+    # an odd number of rows of the tiny width
+    x = synth.make_rows(3, 256, seed=5)
+    c, s = gpu_q8(B, x)
+    co, so = oracle.quantize_q8(x)
+    assert np.array_equal(c, co) and np.array_equal(s, so)
+
+
+# ------------------------------------------------------------------------------------------------ expert products
+def gpu_gateup(B, xc, xs, g, wgu_c, wgu_s, n, E):
+    tiles = dev(g["tiles_raw"]) if "tiles_raw" in g else None
+    if tiles is None:
+        raw = np.zeros(B.tiles_bytes(n, E) // 4, np.int32)
+        nt = g["tiles"].shape[0]
+        raw[0], raw[2] = nt, n
+        raw[4:4 + 4 * nt] = g["tiles"].ravel()
+        tiles = dev(raw)
+    F = wgu_c.shape[1] // 2
+    gu = torch.full((n, 2 * F), float("nan"), dtype=torch.float32, device="cuda")
+    B.smoe_experts_gateup(dev(xc), dev(i16(xs)), dev(g["src"]), tiles, n, dev(wgu_c), dev(i16(wgu_s)), gu)
+    t = host(tiles)
+    assert t[3] == 0, "kernel reported a timeout"
+    return gu
+
+
+def gpu_down(B, hc, hs, g, wd_c, wd_s, n, E):
+    raw = np.zeros(B.tiles_bytes(n, E) // 4, np.int32)
+    nt = g["tiles"].shape[0]
+    raw[0], raw[2] = nt, n
+    raw[4:4 + 4 * nt] = g["tiles"].ravel()
+    tiles = dev(raw)
+    H = wd_c.shape[1]
+    dm = torch.full((n, H), float("nan"), dtype=torch.float32, device="cuda")
+    B.smoe_experts_down(dev(hc), dev(i16(hs)), tiles, n, dev(wd_c), dev(i16(wd_s)), dm)
+    assert host(tiles)[3] == 0
+    return dm
+
+
+def rows_of(t, rows):
+    return host(t[torch.from_numpy(np.ascontiguousarray(rows, dtype=np.int64)).cuda()])
+
+
+def check_products(got, want, absmag, what):
+    err = np.abs(got.astype(np.float64) - want)
+    bound = 2e-6 * absmag + 1e-30
+    bad = err > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} outside 2e-6*sum|terms|; worst ratio " \
+                          f"{float((err / bound).max()):.3g}"
+
+
+def gateup_reference(xc, xs, g, wgu_c, wgu_s, H, F, experts):
+    """oracle gate/up on the rows of the listed experts only, plus sum |terms| per element (numpy)."""
+    rows, want, mag = [], [], []
+    A = deq_a(xc, xs)
+    for e in experts:
+        r0, r1 = int(g["offsets"][e]), int(g["offsets"][e + 1])
+        if r1 == r0:
+            continue
+        sub_off = np.array([0, r1 - r0], np.int32)
+        gu = oracle.gateup(xc, xs, g["src"][r0:r1], sub_off, wgu_c[e:e + 1], wgu_s[e:e + 1], H, F)
+        W = deq_w(wgu_c[e], wgu_s[e], H)
+        rows.append(np.arange(r0, r1))
+        want.append(gu)
+        mag.append(np.abs(A[g["src"][r0:r1]]) @ np.abs(W).T)
+    return np.concatenate(rows), np.concatenate(want), np.concatenate(mag)
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_gateup_parity(B, name):
+    cfg = synth.CONFIGS[name]
+    inp = layer_inputs(name)
+    ids, _ = oracle.route(inp["logits"], cfg.K)
+    g = oracle.group(ids, cfg.E)
+    xc, xs = oracle.quantize_q8(inp["x"])
+    gu = gpu_gateup(B, xc, xs, g, inp["wgu_c"], inp["wgu_s"], cfg.n, cfg.E)
+    if name == "tiny":
+        experts = range(cfg.E)
+    else:  # the busiest expert (several tiles when skewed), the quietest routed one, and two in between
+        order = np.argsort(g["counts"], kind="stable")
+        routed = order[g["counts"][order] > 0]
+        experts = sorted({int(routed[-1]), int(routed[0]), int(routed[len(routed) // 2]), 0})
+    rows, want, mag = gateup_reference(xc, xs, g, inp["wgu_c"], inp["wgu_s"], cfg.H, cfg.F, experts)
+    check_products(rows_of(gu, rows), want, mag, f"gate/up {name}")
+    assert bool(torch.isfinite(gu).all())
+
+
+@pytest.mark.parametrize("name", ["tiny", "t8192", "skew8192"])
+def test_down_parity(B, name):
+    cfg = synth.CONFIGS[name]
+    inp = layer_inputs(name)
+    ids, _ = oracle.route(inp["logits"], cfg.K)
+    g = oracle.group(ids, cfg.E)
+    # H rows: the q8 of synthetic gate/up values through the oracle's SwiGLU (oracle outputs are valid inputs)
+    hc, hs = oracle.swiglu_requant(synth.make_gu(cfg.n, cfg.F, seed=cfg.seed + 100, scale=1.5), cfg.F)
+    dm = gpu_down(B, hc, hs, g, inp["wd_c"], inp["wd_s"], cfg.n, cfg.E)
+    assert bool(torch.isfinite(dm).all())
+    experts = range(cfg.E) if name == "tiny" else [int(np.argmax(g["counts"])), int(np.argmin(g["counts"])), 7]
+    Hd = deq_a(hc, hs)
+    for e in experts:
+        r0, r1 = int(g["offsets"][e]), int(g["offsets"][e + 1])
+        if r1 == r0:
+            continue
+        want = oracle.down(hc[r0:r1], hs[r0:r1], np.array([0, r1 - r0], np.int32), inp["wd_c"][e:e + 1],
+                           inp["wd_s"][e:e + 1], cfg.H, cfg.F)
+        mag = np.abs(Hd[r0:r1]) @ np.abs(deq_w(inp["wd_c"][e], inp["wd_s"][e], cfg.F)).T
+        check_products(rows_of(dm, np.arange(r0, r1)), want, mag, f"down {name} expert {e}")
+
+
+def test_products_special_cases(B):
+    # all weight codes 2: every weight is 0 and every product exactly 0
+    T, H, E, K, F = 40, 256, 3, 2, 128
+    inp = synth.make_custom(T, H, E, K, F, seed=8)
+    ids, _ = oracle.route(inp["logits"], K)
+    g = oracle.group(ids, E)
+    xc, xs = oracle.quantize_q8(inp["x"])
+    zc = np.full_like(inp["wgu_c"], 0b10101010)
+    gu = host(gpu_gateup(B, xc, xs, g, zc, inp["wgu_s"], T * K, E))
+    assert np.all(gu == 0.0)
+    # a constant row through weights of code 3 and one scale: the closed form H * d_w * d_a * 127, exact in fp32
+    xq = np.full((1, H), 0.75, np.float32)
+    xc1, xs1 = oracle.quantize_q8(xq)
+    g1 = oracle.group(np.zeros((1, 1), np.int32), 1)
+    wc = np.full((1, 2 * F, H // 4), 0xFF, np.uint8)
+    ws = np.full((1, 2 * F, H // 32), np.float16(0.0125).view(np.uint16), np.uint16)
+    gu1 = host(gpu_gateup(B, xc1, xs1, g1, wc, ws, 1, 1))
+    want = H * float(np.float16(0.0125)) * float(xs1.view(np.float16)[0, 0]) * 127.0
+    assert np.all(gu1 == np.float32(want))
+
+
+@pytest.mark.parametrize("shape", [(37, 128, 5, 3, 64), (300, 256, 2, 1, 128), (513, 128, 1, 1, 64),
+                                   (64, 384, 9, 4, 192)])
+def test_products_ragged_shapes(B, shape):
+    T, H, E, K, F = shape
+    inp = synth.make_custom(T, H, E, K, F, seed=sum(shape))
+    ids, _ = oracle.route(inp["logits"], K)
+    g = oracle.group(ids, E)
+    xc, xs = oracle.quantize_q8(inp["x"])
+    gu = host(gpu_gateup(B, xc, xs, g, inp["wgu_c"], inp["wgu_s"], T * K, E))
+    rows, want, mag = gateup_reference(xc, xs, g, inp["wgu_c"], inp["wgu_s"], H, F, range(E))
+    check_products(gu[rows], want, mag, f"gate/up {shape}")
+    hc, hs = oracle.swiglu_requant(want[np.argsort(rows)], F)
+    dm = host(gpu_down(B, hc, hs, g, inp["wd_c"], inp["wd_s"], T * K, E))
+    want_d = oracle.down(hc, hs, g["offsets"], inp["wd_c"], inp["wd_s"], H, F)
+    Hd = deq_a(hc, hs)
+    for e in range(E):
+        r0, r1 = int(g["offsets"][e]), int(g["offsets"][e + 1])
+        if r1 > r0:
+            mag = np.abs(Hd[r0:r1]) @ np.abs(deq_w(inp["wd_c"][e], inp["wd_s"][e], F)).T
+            check_products(dm[r0:r1], want_d[r0:r1], mag, f"down {shape}")
+
+
+# ------------------------------------------------------------------------------------------------ SwiGLU + requant
+def test_swiglu_requant_parity(B):
+    n, F = 8192, 1024
+    gu = synth.make_gu(n, F, seed=11, scale=2.0)
+    hc = torch.empty(n, F, dtype=torch.int8, device="cuda")
+    hs = torch.empty(n, F // 32, dtype=torch.int16, device="cuda")
+    B.smoe_swiglu_requant(dev(gu), hc, hs)
+    c, s = host(hc), host(hs).view(np.uint16)
+    co, so = oracle.swiglu_requant(gu, F)
+    g = gu[:, :F].astype(np.float64)
+    u = gu[:, F:].astype(np.float64)
+    h = g * scipy.special.expit(g) * u
+    d = so.view(np.float16).astype(np.float64)
+    # scales: equal, or amax/127 within 1e-5 of an fp16 rounding midpoint
+    sbad = s != so
+    if sbad.any():
+        amax = np.abs(h.reshape(n, F // 32, 32)).max(axis=2)[sbad] / 127.0
+        lo = np.minimum(s[sbad], so[sbad]).view(np.float16).astype(np.float64)
+        hi = np.maximum(s[sbad], so[sbad]).view(np.float16).astype(np.float64)
+        assert np.all(np.abs(amax - 0.5 * (lo + hi)) <= 1e-5 * amax)
+    same_blocks = np.repeat(~sbad, 32, axis=1)
+    cbad = (c != co) & same_blocks
+    assert cbad.sum() <= 1e-4 * c.size
+    if cbad.any():
+        ratio = h / np.repeat(d, 32, axis=1)
+        assert np.all(np.abs(c[cbad].astype(int) - co[cbad].astype(int)) == 1)
+        assert np.all(np.abs(np.abs(ratio[cbad]) % 1.0 - 0.5) <= 1e-3)
+
+
+# ------------------------------------------------------------------------------------------------ combine
+def test_combine_parity(B):
+    rng = np.random.default_rng(4)
+    T, K, H = 777, 10, 2560
+    n = T * K
+    dm = synth.make_dm(n, H, seed=5)
+    slot = rng.permutation(n).astype(np.int32)
+    w = rng.random((T, K)).astype(np.float32)
+    y = torch.empty(T, H, dtype=torch.float32, device="cuda")
+    B.smoe_combine(dev(dm), dev(slot), dev(w), y)
+    got = host(y)
+    want = oracle.combine(dm.astype(np.float64), slot, w.astype(np.float64), T, K, H)
+    mag = np.einsum("tk,tkh->th", np.abs(w.astype(np.float64)), np.abs(dm[slot.reshape(T, K)].astype(np.float64)))
+    assert np.all(np.abs(got - want) <= 1e-6 * mag + 1e-30)
+
+
+# ------------------------------------------------------------------------------------------------ the whole block
+@pytest.mark.parametrize("name", ALL)
+def test_block_parity(B, name):
+    cfg = synth.CONFIGS[name]
+    inp = layer_inputs(name)
+    blk = B.SmoeBlock(cfg.T, cfg.H, cfg.E, cfg.K, cfg.F, inp["wgu_c"], inp["wgu_s"], inp["wd_c"], inp["wd_s"])
+    y = host(blk.run(dev(inp["logits"]), dev(inp["x"]))).astype(np.float64)
+    assert blk.device_status() == (0, 0)
+    # bit-exact integer stages over the whole chunk
+    ids_o, w_o = oracle.route(inp["logits"], cfg.K)
+    assert np.array_equal(host(blk.ids), ids_o)
+    go = oracle.group(ids_o, cfg.E)
+    assert np.array_equal(host(blk.offsets)[:cfg.E + 1], go["offsets"])
+    assert np.array_equal(host(blk.src)[:cfg.n], go["src"]) and np.array_equal(host(blk.slot)[:cfg.n], go["slot"])
+    xc_o, xs_o = oracle.quantize_q8(inp["x"])
+    assert np.array_equal(host(blk.xc), xc_o) and np.array_equal(host(blk.xs).view(np.uint16), xs_o)
+    # the output, row by row
+    if name == "tiny":
+        toks = np.arange(cfg.T)
+        y_o = oracle.layer(inp)
+    else:
+        rng = np.random.default_rng(cfg.seed)
+        toks = np.unique(np.concatenate([[0, cfg.T - 1], rng.choice(cfg.T, 30, replace=False)]))
+        y_o, ids_t, _ = oracle.layer_tokens(inp, toks)
+        assert np.array_equal(ids_t, ids_o[toks])
+    y_s = y[toks] if name != "tiny" else y
+    rms = np.sqrt((y_o ** 2).mean(axis=1))
+    err = np.abs(y_s - y_o).max(axis=1)
+    assert np.all(err <= 2e-3 * rms), f"worst err/rms {float((err / rms).max()):.3e}"
+    assert np.isfinite(y).all()
+    del blk
+    torch.cuda.empty_cache()
+
+
+def test_block_is_deterministic(B):
+    cfg = synth.CONFIGS["tiny"]
+    inp = layer_inputs("tiny")
+    blk = B.SmoeBlock(cfg.T, cfg.H, cfg.E, cfg.K, cfg.F, inp["wgu_c"], inp["wgu_s"], inp["wd_c"], inp["wd_s"])
+    lg, x = dev(inp["logits"]), dev(inp["x"])
+    y1 = host(blk.run(lg, x)).copy()
+    y2 = host(blk.run(lg, x))
+    assert np.array_equal(y1, y2)
