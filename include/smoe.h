@@ -65,6 +65,9 @@ typedef int smoe_status;
 /* Human-readable name of a status code (static storage). */
 const char* smoe_status_string(smoe_status s);
 
+/* Name of the CUDA error behind this thread's most recent SMOE_ERR_LAUNCH (static storage; "no error" before any). */
+const char* smoe_last_error_string(void);
+
 /* SMOE_OK when the current CUDA device is an sm_103 part the kernels were built for. */
 smoe_status smoe_device_check(void);
 

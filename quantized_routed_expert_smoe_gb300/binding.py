@@ -33,6 +33,7 @@ _lib = None
 
 _SIGS = {
     "smoe_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "smoe_last_error_string": ([], ctypes.c_char_p),
     "smoe_device_check": ([], ctypes.c_int),
     "smoe_max_tiles": ([ctypes.c_int64, ctypes.c_int], ctypes.c_int64),
     "smoe_tiles_bytes": ([ctypes.c_int64, ctypes.c_int], ctypes.c_size_t),
@@ -83,7 +84,10 @@ def status_string(status: int) -> str:
 
 def _check(call: str, status: int):
     if status != SMOE_OK:
-        raise SmoeError(call, status, status_string(status))
+        text = status_string(status)
+        if status == SMOE_ERR_LAUNCH:
+            text += ": " + load_library().smoe_last_error_string().decode()
+        raise SmoeError(call, status, text)
 
 
 def _stream(stream):

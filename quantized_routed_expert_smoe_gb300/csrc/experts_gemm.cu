@@ -12,16 +12,20 @@
 //     hi = fp16_rn(d * q) and lo = d * q - hi, which is exact in fp16 (at most 8 significant bits), so
 //     hi + lo = d * q exactly.
 // Every product of an fp16 weight and an fp16 hi/lo part is exact in the fp32 accumulator, so each output is the
-// sum of the exact products d_w (q_w - 2) d_a q_a, accumulated in fp32 -- the same numbers the per-block integer dot
-// scaled by d_w d_a computes, with one fp32 rounding per addition.  The K loop runs two MMAs per 16-wide K step
-// (A x B_hi, A x B_lo) into one accumulator.
+// sum of the exact products d_w (q_w - 2) d_a q_a.  The K loop runs two MMAs per 16-wide K step (A x B_hi,
+// A x B_lo).  The tensor core's fp32 accumulation aligns its addends with truncation, which over the 2 * K / 16 steps
+// of a whole row costs about 3e-6 of the result -- enough to flip requantised H codes -- so the accumulation is
+// two-level: each 64-wide K slice accumulates from zero into one of two tensor-memory buffers (the slice's partial is
+// small, so its truncation error is too), and the converter warps add each finished slice into fp32 registers with
+// round-to-nearest while the tensor core fills the other buffer.
 //
 // Tile: one CTA = one tile of the tile list (an expert and up to 256 of its routed rows, the MMA's N, a multiple of
 // 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB: weights are the M operand so that a
-// small expert wastes little).  Warp 0 allocates tensor memory and one lane issues the MMAs; eight converter warps
-// read the 2-bit weight codes and the int8 rows from global memory, decode them into the fp16 operand tiles in shared
-// memory (K-major, 128-byte swizzle, 64 K values per stage, two stages) and then run the epilogue, reading the
-// accumulator from tensor memory and writing fp32 rows.
+// small expert wastes little).  Eight warps read the 2-bit weight codes and the int8 rows from global memory, decode
+// them into the fp16 operand tiles in shared memory (K-major, 128-byte swizzle, 64 K values per stage, two stages),
+// promote each slice's partial from tensor memory into their registers, and finally write the fp32 rows; lane 0 of
+// warp 0 also issues the MMAs of each stage once all eight warps have filled it.  (Eight warps, two per SM
+// sub-partition, leave each thread up to 255 registers; the 128 fp32 sums a thread keeps need that room.)
 //
 // K order inside the operand tiles: within each group of 16 K values, shared-memory position 2m holds value m and
 // position 2m+1 holds value m+8 (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so
@@ -41,12 +45,12 @@ constexpr int kMaxBN = SMOE_TILE_ROWS;         // routed rows per tile (MMA N <=
 constexpr int kStages = 2;
 constexpr int kConvWarps = 8;
 constexpr int kConvThreads = 32 * kConvWarps;  // 256
-constexpr int kThreads = 32 + kConvThreads;    // warp 0: MMA; warps 1..8: converters + epilogue
+constexpr int kThreads = kConvThreads;         // every warp converts and promotes; lane 0 of warp 0 issues MMAs
 constexpr int kATile = kBM * 128;              // 16 KB of fp16 weights
 constexpr int kBTile = kMaxBN * 128;           // 32 KB of fp16 activations (one of hi / lo)
 constexpr int kStage = kATile + 2 * kBTile;
 constexpr int kSmemBytes = 1024 + kStages * kStage + 256;
-constexpr uint32_t kTmemCols = 256;            // fp32 accumulator 128 lanes x N <= 256 columns
+constexpr uint32_t kTmemCols = 512;            // two fp32 partial buffers, 128 lanes x N <= 256 columns each
 
 struct AReg {
     uint2 codes;      // 32 2-bit codes
@@ -118,6 +122,7 @@ __device__ __forceinline__ void zero_activations(uint32_t hi_addr, uint32_t lo_a
     }
 }
 
+// 256 threads, two warps per sub-partition: up to 255 registers a thread; one CTA per SM (shared and tensor memory).
 __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const ExpertsGemmArgs p) {
     int32_t* tiles = p.tiles;
     const int ti = blockIdx.y;
@@ -133,7 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     uint8_t* smem = smem_raw + pad;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStage);
     uint64_t* empty = full + kStages;
-    uint64_t* accf = empty + kStages;
+    uint64_t* pfull = empty + kStages;   // a slice's partial is complete in tensor-memory buffer b
+    uint64_t* pempty = pfull + 2;        // the converters have added buffer b into their registers
+    uint64_t* accf = pempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -142,6 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], kConvThreads);
             mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&pfull[b], 1);
+            mbar_init(&pempty[b], kConvThreads);
         }
         mbar_init(accf, 1);
         *abort_flag = 0;
@@ -158,37 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const int nk = p.K / kBK;
     const uint32_t sbase = smem_u32(smem);
 
-    if (warp == 0) {
-        // ------------------------------------------------------------------ MMA issue (one thread)
-        if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(kBM, N);
-            bool ok = true;
-            for (int kt = 0; kt < nk; ++kt) {
-                const int s = kt % kStages;
-                if (!mbar_wait(&full[s], (uint32_t)(kt / kStages) & 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t a = sbase + s * kStage, bh = a + kATile, bl = bh + kBTile;
-#pragma unroll
-                for (int j = 0; j < kBK / 16; ++j) {
-                    const uint64_t ad = sdesc_k_sw128(a + 32 * j);
-                    mma_f16(tmem, ad, sdesc_k_sw128(bh + 32 * j), idesc, (kt > 0 || j > 0) ? 1u : 0u);
-                    mma_f16(tmem, ad, sdesc_k_sw128(bl + 32 * j), idesc, 1u);
-                }
-                mma_commit(&empty[s]);
-            }
-            if (!ok) {
-                *abort_flag = 1;
-                tiles[3] = SMOE_ERR_TIMEOUT;
-            }
-            mma_commit(accf);  // completes once every MMA issued above has completed (abort path included)
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------------------ converters
-        const int ct = threadIdx.x - 32;
+    {
+        const int ct = threadIdx.x;
         const int ar = ct >> 1, half = ct & 1;  // weight row of this thread, and which 32 of the stage's 64 K
         const int64_t arow = (int64_t)e * p.a_rows + m0 + ar;
         const uint2* acodes = reinterpret_cast<const uint2*>(p.wc + arow * (p.K / 4)) + half;
@@ -219,49 +201,97 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 bn1.scale = __ldg(b1s + 2 * kt);
             }
         };
+        // promotion: this thread owns TMEM lane 32*q + lane (weight row mrow) and columns [chalf*128, +128)
+        const int q = warp & 3;             // the TMEM lane quarter this warp may access
+        const int chalf = warp >> 2;        // warps 0-3: columns [0, 128); 4-7: [128, 256)
+        const int mrow = 32 * q + lane;
+        float acc[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+        auto promote = [&](int k) -> bool {
+            const int b = k & 1;
+            if (!mbar_wait(&pfull[b], (uint32_t)(k / 2) & 1u, abort_flag)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int c0 = chalf * 128 + 32 * c;
+                if (c0 < N) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)b + (uint32_t)c0, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[32 * c + i] += __uint_as_float(v[i]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&pempty[b]);
+            return true;
+        };
+        // the MMAs of slice kt (lane 0 of warp 0): after every warp has filled stage kt and buffer kt & 1 has been
+        // promoted (slice kt - 2)
+        const uint32_t idesc = idesc_f16_f32(kBM, N);
+        auto issue = [&](int kt) -> bool {
+            const int s = kt % kStages, b = kt & 1;
+            if (!mbar_wait(&full[s], (uint32_t)(kt / kStages) & 1u, abort_flag)) return false;
+            if (kt >= 2 && !mbar_wait(&pempty[b], (uint32_t)(kt / 2 - 1) & 1u, abort_flag)) return false;
+            tc_fence_after();
+            const uint32_t a = sbase + s * kStage, bh = a + kATile, bl = bh + kBTile;
+            const uint32_t d = tmem + 256u * (uint32_t)b;
+#pragma unroll
+            for (int j = 0; j < kBK / 16; ++j) {
+                const uint64_t ad = sdesc_k_sw128(a + 32 * j);
+                mma_f16(d, ad, sdesc_k_sw128(bh + 32 * j), idesc, j > 0 ? 1u : 0u);
+                mma_f16(d, ad, sdesc_k_sw128(bl + 32 * j), idesc, 1u);
+            }
+            mma_commit(&empty[s]);
+            mma_commit(&pfull[b]);
+            return true;
+        };
+
         load(0);
         bool ok = true;
-        for (int kt = 0; kt < nk; ++kt) {
-            const AReg a = an;
-            const BReg b0 = bn0, b1 = bn1;
-            if (kt + 1 < nk) load(kt + 1);
+        for (int kt = 0; kt < nk && ok; ++kt) {
             const int s = kt % kStages;
             if (kt >= kStages && !mbar_wait(&empty[s], (uint32_t)(kt / kStages - 1) & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
             const uint32_t sa = sbase + s * kStage, sh = sa + kATile, sl = sh + kBTile;
-            decode_weights(a, sa + ar * 128, ar, half);
+            decode_weights(an, sa + ar * 128, ar, half);
             if (br0 < N) {
-                if (b0p) split_activations(b0, sh + br0 * 128, sl + br0 * 128, br0, half);
+                if (b0p) split_activations(bn0, sh + br0 * 128, sl + br0 * 128, br0, half);
                 else zero_activations(sh + br0 * 128, sl + br0 * 128, br0, half);
             }
             if (br1 < N) {
-                if (b1p) split_activations(b1, sh + br1 * 128, sl + br1 * 128, br1, half);
+                if (b1p) split_activations(bn1, sh + br1 * 128, sl + br1 * 128, br1, half);
                 else zero_activations(sh + br1 * 128, sl + br1 * 128, br1, half);
             }
             fence_async_smem();
             mbar_arrive(&full[s]);
+            if (warp == 0) {
+                bool issued = true;
+                if (lane == 0) issued = issue(kt);
+                ok = __shfl_sync(0xffffffffu, issued ? 1 : 0, 0) != 0;
+                if (!ok) break;
+            }
+            if (kt + 1 < nk) load(kt + 1);          // in flight while the previous slice is promoted
+            if (kt >= 1 && !promote(kt - 1)) ok = false;
         }
+        if (ok && !promote(nk - 1)) ok = false;
+        if (warp == 0 && lane == 0) mma_commit(accf);  // completes once every MMA issued above has completed
         if (!ok) {
             *abort_flag = 1;
             tiles[3] = SMOE_ERR_TIMEOUT;
-        }
-        // ------------------------------------------------------------------ epilogue
-        if (ok && mbar_wait(accf, 0, abort_flag)) {
-            tc_fence_after();
-            const int q = warp & 3;             // the TMEM lane quarter this warp may read
-            const int chalf = (warp - 1) >> 2;  // warps 1-4: columns [0, 128); 5-8: [128, 256)
-            const int mrow = 32 * q + lane;
+        } else {
+            // ------------------------------------------------------------------ epilogue: fp32 rows out
             float* outcol = p.out + (m0 + mrow);
-            const int cend = min(N, chalf * 128 + 128);
-            for (int c0 = chalf * 128; c0 < cend; c0 += 32) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
-                tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (c0 + i < rows) outcol[(int64_t)(row0 + c0 + i) * p.a_rows] = __uint_as_float(v[i]);
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int col = chalf * 128 + 32 * c + i;
+                    if (col < rows) outcol[(int64_t)(row0 + col) * p.a_rows] = acc[32 * c + i];
+                }
             }
         }
     }

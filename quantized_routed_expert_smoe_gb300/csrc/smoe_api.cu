@@ -11,8 +11,11 @@ namespace {
 
 bool aligned16(const void* p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }
 
+thread_local const char* g_last_cuda_error = "no error";
+
 smoe_status launch_status(cudaError_t err) {
     if (err == cudaSuccess) return SMOE_OK;
+    g_last_cuda_error = cudaGetErrorName(err);
     cudaGetLastError();  // clear a sticky launch error so that the caller's next call starts clean
     return SMOE_ERR_LAUNCH;
 }
@@ -51,6 +54,8 @@ const char* smoe_status_string(smoe_status s) {
         default: return "unknown status";
     }
 }
+
+const char* smoe_last_error_string(void) { return g_last_cuda_error; }
 
 smoe_status smoe_device_check(void) { return device_is_sm103() ? SMOE_OK : SMOE_ERR_UNSUPPORTED; }
 
