@@ -21,11 +21,13 @@
 //
 // Tile: one CTA = one tile of the tile list (an expert and up to 256 of its routed rows, the MMA's N, a multiple of
 // 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB: weights are the M operand so that a
-// small expert wastes little).  Eight warps read the 2-bit weight codes and the int8 rows from global memory, decode
-// them into the fp16 operand tiles in shared memory (K-major, 128-byte swizzle, 64 K values per stage, two stages),
-// promote each slice's partial from tensor memory into their registers, and finally write the fp32 rows; lane 0 of
-// warp 0 also issues the MMAs of each stage once all eight warps have filled it.  (Eight warps, two per SM
-// sub-partition, leave each thread up to 255 registers; the 128 fp32 sums a thread keeps need that room.)
+// small expert wastes little).  Warp roles (three warpgroups, registers rebalanced with setmaxnreg):
+//   warpgroup 0   warp 0: tensor-memory allocation and, on one lane, the MMAs of each slice;
+//                 warps 1-3: producers -- cp.async copies of each slice's 2-bit weight codes, int8 rows (gathered
+//                 through src) and scales into a ring of up to 16 slices in shared memory;
+//   warpgroups 1-2  converters: decode a ring slice into the fp16 operand tiles of one of two stages (K-major,
+//                 128-byte swizzle), then add the previous slice's partial from tensor memory into their registers;
+//                 at the end they write the fp32 rows.
 //
 // K order inside the operand tiles: within each group of 16 K values, shared-memory position 2m holds value m and
 // position 2m+1 holds value m+8 (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so
@@ -40,35 +42,59 @@ namespace smoe {
 namespace {
 
 constexpr int kBM = 128;                       // weight rows per CTA (MMA M)
-constexpr int kBK = 64;                        // K values per stage: one 128-byte swizzle row of fp16
+constexpr int kBK = 64;                        // K values per slice: one 128-byte swizzle row of fp16
 constexpr int kMaxBN = SMOE_TILE_ROWS;         // routed rows per tile (MMA N <= 256)
-constexpr int kStages = 2;
-constexpr int kConvWarps = 8;
-constexpr int kConvThreads = 32 * kConvWarps;  // 256
-constexpr int kThreads = kConvThreads;         // every warp converts and promotes; lane 0 of warp 0 issues MMAs
+constexpr int kStages = 2;                     // fp16 operand stages
+constexpr int kThreads = 384;                  // three warpgroups
+constexpr int kProducers = 96;                 // warps 1-3
+constexpr int kConverters = 256;               // warpgroups 1-2
 constexpr int kATile = kBM * 128;              // 16 KB of fp16 weights
 constexpr int kBTile = kMaxBN * 128;           // 32 KB of fp16 activations (one of hi / lo)
 constexpr int kStage = kATile + 2 * kBTile;
-constexpr int kSmemBytes = 1024 + kStages * kStage + 256;
+constexpr int kRingBytes = 64 * 1024;          // raw-data ring
+constexpr int kMaxRing = 16;                   // slices in flight at most
 constexpr uint32_t kTmemCols = 512;            // two fp32 partial buffers, 128 lanes x N <= 256 columns each
+// shared memory: [1 KB alignment slack][stages][ring][src rows 1 KB][barriers]
+constexpr int kSmemBytes = 1024 + kStages * kStage + kRingBytes + 1024 + 512;
+// registers: launched at 168 a thread (384 x 168 = 64,512 of 65,536); warpgroup 0 gives back to 56 and the two
+// converter warpgroups take 224: 128 x 56 + 256 x 224 = 64,512.
+constexpr int kRegsWg0 = 56;
+constexpr int kRegsConv = 224;
 
-struct AReg {
-    uint2 codes;      // 32 2-bit codes
-    uint16_t scale;   // their fp16 scale
-};
-struct BReg {
-    uint4 c0, c1;     // 32 int8 codes
-    uint16_t scale;
-};
+// Raw slice layout in the ring (one 64-wide K slice of the tile): weight codes [128][16 B], weight scales [128][4 B],
+// activation codes [N][64 B], activation scales [N][4 B].
+__host__ __device__ constexpr int raw_slice_bytes(int N) { return (2048 + 512 + N * 68 + 127) & ~127; }
 
-// 32 weights of one row (codes r) into 4 16-byte chunks of the row's swizzled shared-memory line: d * (q - 2).
-__device__ __forceinline__ void decode_weights(const AReg& r, uint32_t row_addr, int row, int half) {
-    const __half2 d2 = __half2half2(__ushort_as_half(r.scale));
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// arrive on `bar` once every cp.async this thread issued so far has landed (the arrival counts toward the phase)
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// This thread's 32 weights of one row into 4 16-byte chunks of the row's swizzled line: d * (q - 2).
+// `codes` holds 32 2-bit codes, value i at bits 2i..2i+1 of the 64-bit word.
+__device__ __forceinline__ void decode_weights(uint2 codes, uint16_t scale, uint4* row_line, int row, int half) {
+    const __half2 d2 = __half2half2(__ushort_as_half(scale));
     const __half2 k1026 = __float2half2_rn(1026.0f);
     uint32_t h[16];
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
-        const uint32_t w = g ? r.codes.y : r.codes.x;  // 16 codes: value i at bits 2i..2i+1
+        const uint32_t w = g ? codes.y : codes.x;
 #pragma unroll
         for (int m = 0; m < 8; ++m) {
             // values m and m+8 as fp16 1024 + q in the two halves, then (1024 + q - 1026) * d = d * (q - 2)
@@ -77,18 +103,16 @@ __device__ __forceinline__ void decode_weights(const AReg& r, uint32_t row_addr,
         }
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int lc = half * 4 + c;
-        st_shared_v4(row_addr + ((uint32_t)(lc ^ (row & 7)) << 4), h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
-    }
+    for (int c = 0; c < 4; ++c)
+        row_line[(half * 4 + c) ^ (row & 7)] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
 }
 
 // 32 int8 activations of one row into the hi and lo tiles: hi = fp16_rn(d q), lo = d q - hi (exact).
-__device__ __forceinline__ void split_activations(const BReg& r, uint32_t hi_addr, uint32_t lo_addr, int row,
-                                                  int half) {
-    const __half2 d2 = __half2half2(__ushort_as_half(r.scale));
+__device__ __forceinline__ void split_activations(uint4 c0, uint4 c1, uint16_t scale, uint4* hi_line,
+                                                  uint4* lo_line, int row, int half) {
+    const __half2 d2 = __half2half2(__ushort_as_half(scale));
     const __half2 k1152 = __float2half2_rn(1152.0f);
-    const uint32_t w[8] = {r.c0.x, r.c0.y, r.c0.z, r.c0.w, r.c1.x, r.c1.y, r.c1.z, r.c1.w};
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
     uint32_t hi[16], lo[16];
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
@@ -107,22 +131,21 @@ __device__ __forceinline__ void split_activations(const BReg& r, uint32_t hi_add
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint32_t off = (uint32_t)((half * 4 + c) ^ (row & 7)) << 4;
-        st_shared_v4(hi_addr + off, hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-        st_shared_v4(lo_addr + off, lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+        const int pc = (half * 4 + c) ^ (row & 7);
+        hi_line[pc] = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+        lo_line[pc] = make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
     }
 }
 
-__device__ __forceinline__ void zero_activations(uint32_t hi_addr, uint32_t lo_addr, int row, int half) {
+__device__ __forceinline__ void zero_activations(uint4* hi_line, uint4* lo_line, int row, int half) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-        const uint32_t off = (uint32_t)((half * 4 + c) ^ (row & 7)) << 4;
-        st_shared_v4(hi_addr + off, 0u, 0u, 0u, 0u);
-        st_shared_v4(lo_addr + off, 0u, 0u, 0u, 0u);
+        const int pc = (half * 4 + c) ^ (row & 7);
+        hi_line[pc] = make_uint4(0u, 0u, 0u, 0u);
+        lo_line[pc] = make_uint4(0u, 0u, 0u, 0u);
     }
 }
 
-// 256 threads, two warps per sub-partition: up to 255 registers a thread; one CTA per SM (shared and tensor memory).
 __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const ExpertsGemmArgs p) {
     int32_t* tiles = p.tiles;
     const int ti = blockIdx.y;
@@ -132,32 +155,48 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     if (rows <= 0 || rows > kMaxBN) return;
     const int N = (rows + 15) & ~15;
     const int m0 = blockIdx.x * kBM;
+    const int nk = p.K / kBK;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t* smem = smem_raw + pad;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStage);
-    uint64_t* empty = full + kStages;
-    uint64_t* pfull = empty + kStages;   // a slice's partial is complete in tensor-memory buffer b
-    uint64_t* pempty = pfull + 2;        // the converters have added buffer b into their registers
-    uint64_t* accf = pempty + 2;
+    uint8_t* ring = smem + kStages * kStage;
+    int32_t* srcs = reinterpret_cast<int32_t*>(ring + kRingBytes);          // [256] B row of each tile row
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kRingBytes + 1024);  // operand stage s is filled
+    uint64_t* empty = full + kStages;                                         // ... and consumed by the MMAs
+    uint64_t* pfull = empty + kStages;     // a slice's partial is complete in tensor-memory buffer b
+    uint64_t* pempty = pfull + 2;          // the converters have added buffer b into their registers
+    uint64_t* rfull = pempty + 2;          // ring slot r holds its slice [kMaxRing]
+    uint64_t* rempty = rfull + kMaxRing;   // ring slot r has been read [kMaxRing]
+    uint64_t* accf = rempty + kMaxRing;    // every MMA has completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int sbytes = raw_slice_bytes(N);
+    const int depth = min(kMaxRing, kRingBytes / sbytes);
+    const int o_as = 2048, o_bc = 2560, o_bs = 2560 + N * 64;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], kConvThreads);
+            mbar_init(&full[s], kConverters);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&pfull[b], 1);
-            mbar_init(&pempty[b], kConvThreads);
+            mbar_init(&pempty[b], kConverters);
+        }
+        for (int r = 0; r < kMaxRing; ++r) {
+            mbar_init(&rfull[r], kProducers);
+            mbar_init(&rempty[r], kConverters);
         }
         mbar_init(accf, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
+    // the B row of every tile row (rows past the tile: -1)
+    for (int r = threadIdx.x; r < kMaxBN; r += kThreads)
+        srcs[r] = r < rows ? (p.src ? p.src[row0 + r] : row0 + r) : -1;
     if (warp == 0) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -166,44 +205,81 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int nk = p.K / kBK;
     const uint32_t sbase = smem_u32(smem);
+    bool ok = true;
 
-    {
-        const int ct = threadIdx.x;
-        const int ar = ct >> 1, half = ct & 1;  // weight row of this thread, and which 32 of the stage's 64 K
-        const int64_t arow = (int64_t)e * p.a_rows + m0 + ar;
-        const uint2* acodes = reinterpret_cast<const uint2*>(p.wc + arow * (p.K / 4)) + half;
-        const uint16_t* ascales = p.ws + arow * (p.K / 32) + half;
+    if (warp < 4) {
+        setmaxnreg_dec<kRegsWg0>();
+        if (warp == 0) {
+            // ------------------------------------------------------------------ MMA issue (one thread)
+            if (lane == 0) {
+                const uint32_t idesc = idesc_f16_f32(kBM, N);
+                for (int kt = 0; kt < nk; ++kt) {
+                    const int s = kt % kStages, b = kt & 1;
+                    if (!mbar_wait(&full[s], (uint32_t)(kt / kStages) & 1u, abort_flag) ||
+                        (kt >= 2 && !mbar_wait(&pempty[b], (uint32_t)(kt / 2 - 1) & 1u, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = sbase + s * kStage, bh = a + kATile, bl = bh + kBTile;
+                    const uint32_t d = tmem + 256u * (uint32_t)b;
+#pragma unroll
+                    for (int j = 0; j < kBK / 16; ++j) {
+                        const uint64_t ad = sdesc_k_sw128(a + 32 * j);
+                        mma_f16(d, ad, sdesc_k_sw128(bh + 32 * j), idesc, j > 0 ? 1u : 0u);
+                        mma_f16(d, ad, sdesc_k_sw128(bl + 32 * j), idesc, 1u);
+                    }
+                    mma_commit(&empty[s]);
+                    mma_commit(&pfull[b]);
+                }
+                mma_commit(accf);  // completes once every MMA issued above has completed (abort path included)
+            }
+            __syncwarp();
+        } else {
+            // ------------------------------------------------------------------ producers (96 threads)
+            const int pt = threadIdx.x - 32;
+            const int64_t wrow0 = (int64_t)e * p.a_rows + m0;
+            const uint8_t* wc = p.wc + wrow0 * (p.K / 4);
+            const uint16_t* ws = p.ws + wrow0 * (p.K / 32);
+            const int items = 128 + 128 + N * 4 + N;  // weight code rows, weight scale pairs, row chunks, row scales
+            for (int kt = 0; kt < nk; ++kt) {
+                const int r = kt % depth;
+                if (kt >= depth && !mbar_wait(&rempty[r], (uint32_t)(kt / depth - 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t slot = smem_u32(ring) + (uint32_t)(r * sbytes);
+                for (int i = pt; i < items; i += kProducers) {
+                    if (i < 128) {
+                        cp_async_16(slot + i * 16, wc + (int64_t)i * (p.K / 4) + kt * 16);
+                    } else if (i < 256) {
+                        const int row = i - 128;
+                        cp_async_4(slot + o_as + row * 4, ws + (int64_t)row * (p.K / 32) + kt * 2);
+                    } else if (i < 256 + N * 4) {
+                        const int row = (i - 256) >> 2, ch = (i - 256) & 3;
+                        const int32_t sr = srcs[row];
+                        if (sr >= 0) cp_async_16(slot + o_bc + row * 64 + ch * 16, p.bc + (int64_t)sr * p.K + kt * kBK + ch * 16);
+                    } else {
+                        const int row = i - 256 - N * 4;
+                        const int32_t sr = srcs[row];
+                        if (sr >= 0) cp_async_4(slot + o_bs + row * 4, p.bs + (int64_t)sr * (p.K / 32) + kt * 2);
+                    }
+                }
+                cp_async_arrive(&rfull[r]);
+            }
+            cp_async_wait_all();  // no copy may land after the CTA has moved on
+        }
+    } else {
+        setmaxnreg_inc<kRegsConv>();
+        // ------------------------------------------------------------------ converters (256 threads)
+        const int ct = threadIdx.x - 128;
+        const int ar = ct >> 1, half = ct & 1;  // weight row of this thread, and which 32 of the slice's 64 K
         const int br0 = ar, br1 = ar + 128;     // routed rows of this thread (two passes)
-        const int64_t bsrc0 = br0 < rows ? (p.src ? (int64_t)p.src[row0 + br0] : (int64_t)(row0 + br0)) : -1;
-        const int64_t bsrc1 = br1 < rows ? (p.src ? (int64_t)p.src[row0 + br1] : (int64_t)(row0 + br1)) : -1;
-        const int8_t* b0p = bsrc0 >= 0 ? p.bc + bsrc0 * p.K + half * 32 : nullptr;
-        const int8_t* b1p = bsrc1 >= 0 ? p.bc + bsrc1 * p.K + half * 32 : nullptr;
-        const uint16_t* b0s = bsrc0 >= 0 ? p.bs + bsrc0 * (p.K / 32) + half : nullptr;
-        const uint16_t* b1s = bsrc1 >= 0 ? p.bs + bsrc1 * (p.K / 32) + half : nullptr;
-
-        AReg an;
-        BReg bn0, bn1;
-        auto load = [&](int kt) {
-            an.codes = __ldg(acodes + 2 * kt);
-            an.scale = __ldg(ascales + 2 * kt);
-            if (b0p) {
-                const uint4* q = reinterpret_cast<const uint4*>(b0p + kt * kBK);
-                bn0.c0 = __ldg(q);
-                bn0.c1 = __ldg(q + 1);
-                bn0.scale = __ldg(b0s + 2 * kt);
-            }
-            if (b1p) {
-                const uint4* q = reinterpret_cast<const uint4*>(b1p + kt * kBK);
-                bn1.c0 = __ldg(q);
-                bn1.c1 = __ldg(q + 1);
-                bn1.scale = __ldg(b1s + 2 * kt);
-            }
-        };
+        const bool has0 = srcs[br0] >= 0, has1 = srcs[br1] >= 0;
         // promotion: this thread owns TMEM lane 32*q + lane (weight row mrow) and columns [chalf*128, +128)
-        const int q = warp & 3;             // the TMEM lane quarter this warp may access
-        const int chalf = warp >> 2;        // warps 0-3: columns [0, 128); 4-7: [128, 256)
+        const int q = warp & 3;                 // the TMEM lane quarter this warp may access
+        const int chalf = (warp - 4) >> 2;      // warpgroup 1: columns [0, 128); warpgroup 2: [128, 256)
         const int mrow = 32 * q + lane;
         float acc[128];
 #pragma unroll
@@ -227,62 +303,55 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             mbar_arrive(&pempty[b]);
             return true;
         };
-        // the MMAs of slice kt (lane 0 of warp 0): after every warp has filled stage kt and buffer kt & 1 has been
-        // promoted (slice kt - 2)
-        const uint32_t idesc = idesc_f16_f32(kBM, N);
-        auto issue = [&](int kt) -> bool {
-            const int s = kt % kStages, b = kt & 1;
-            if (!mbar_wait(&full[s], (uint32_t)(kt / kStages) & 1u, abort_flag)) return false;
-            if (kt >= 2 && !mbar_wait(&pempty[b], (uint32_t)(kt / 2 - 1) & 1u, abort_flag)) return false;
-            tc_fence_after();
-            const uint32_t a = sbase + s * kStage, bh = a + kATile, bl = bh + kBTile;
-            const uint32_t d = tmem + 256u * (uint32_t)b;
-#pragma unroll
-            for (int j = 0; j < kBK / 16; ++j) {
-                const uint64_t ad = sdesc_k_sw128(a + 32 * j);
-                mma_f16(d, ad, sdesc_k_sw128(bh + 32 * j), idesc, j > 0 ? 1u : 0u);
-                mma_f16(d, ad, sdesc_k_sw128(bl + 32 * j), idesc, 1u);
-            }
-            mma_commit(&empty[s]);
-            mma_commit(&pfull[b]);
-            return true;
-        };
 
-        load(0);
-        bool ok = true;
         for (int kt = 0; kt < nk && ok; ++kt) {
+            const int r = kt % depth;
+            if (!mbar_wait(&rfull[r], (uint32_t)(kt / depth) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            const uint8_t* slot = ring + r * sbytes;
+            const uint2 acodes = *reinterpret_cast<const uint2*>(slot + ar * 16 + half * 8);
+            const uint16_t ascale = *reinterpret_cast<const uint16_t*>(slot + o_as + ar * 4 + half * 2);
+            uint4 b0c0 = make_uint4(0, 0, 0, 0), b0c1 = b0c0, b1c0 = b0c0, b1c1 = b0c0;
+            uint16_t b0s = 0, b1s = 0;
+            if (has0) {
+                const uint4* c = reinterpret_cast<const uint4*>(slot + o_bc + br0 * 64 + half * 32);
+                b0c0 = c[0];
+                b0c1 = c[1];
+                b0s = *reinterpret_cast<const uint16_t*>(slot + o_bs + br0 * 4 + half * 2);
+            }
+            if (has1) {
+                const uint4* c = reinterpret_cast<const uint4*>(slot + o_bc + br1 * 64 + half * 32);
+                b1c0 = c[0];
+                b1c1 = c[1];
+                b1s = *reinterpret_cast<const uint16_t*>(slot + o_bs + br1 * 4 + half * 2);
+            }
+            mbar_arrive(&rempty[r]);
             const int s = kt % kStages;
             if (kt >= kStages && !mbar_wait(&empty[s], (uint32_t)(kt / kStages - 1) & 1u, abort_flag)) {
                 ok = false;
                 break;
             }
-            const uint32_t sa = sbase + s * kStage, sh = sa + kATile, sl = sh + kBTile;
-            decode_weights(an, sa + ar * 128, ar, half);
+            uint8_t* st = smem + s * kStage;
+            uint4* a_tile = reinterpret_cast<uint4*>(st);
+            uint4* hi_tile = reinterpret_cast<uint4*>(st + kATile);
+            uint4* lo_tile = reinterpret_cast<uint4*>(st + kATile + kBTile);
+            decode_weights(acodes, ascale, a_tile + ar * 8, ar, half);
             if (br0 < N) {
-                if (b0p) split_activations(bn0, sh + br0 * 128, sl + br0 * 128, br0, half);
-                else zero_activations(sh + br0 * 128, sl + br0 * 128, br0, half);
+                if (has0) split_activations(b0c0, b0c1, b0s, hi_tile + br0 * 8, lo_tile + br0 * 8, br0, half);
+                else zero_activations(hi_tile + br0 * 8, lo_tile + br0 * 8, br0, half);
             }
             if (br1 < N) {
-                if (b1p) split_activations(bn1, sh + br1 * 128, sl + br1 * 128, br1, half);
-                else zero_activations(sh + br1 * 128, sl + br1 * 128, br1, half);
+                if (has1) split_activations(b1c0, b1c1, b1s, hi_tile + br1 * 8, lo_tile + br1 * 8, br1, half);
+                else zero_activations(hi_tile + br1 * 8, lo_tile + br1 * 8, br1, half);
             }
             fence_async_smem();
             mbar_arrive(&full[s]);
-            if (warp == 0) {
-                bool issued = true;
-                if (lane == 0) issued = issue(kt);
-                ok = __shfl_sync(0xffffffffu, issued ? 1 : 0, 0) != 0;
-                if (!ok) break;
-            }
-            if (kt + 1 < nk) load(kt + 1);          // in flight while the previous slice is promoted
             if (kt >= 1 && !promote(kt - 1)) ok = false;
         }
         if (ok && !promote(nk - 1)) ok = false;
-        if (warp == 0 && lane == 0) mma_commit(accf);  // completes once every MMA issued above has completed
-        if (!ok) {
-            *abort_flag = 1;
-            tiles[3] = SMOE_ERR_TIMEOUT;
-        } else {
+        if (ok) {
             // ------------------------------------------------------------------ epilogue: fp32 rows out
             float* outcol = p.out + (m0 + mrow);
 #pragma unroll
@@ -294,6 +363,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 }
             }
         }
+    }
+    if (!ok) {
+        *abort_flag = 1;
+        tiles[3] = SMOE_ERR_TIMEOUT;
     }
     tc_fence_before();
     __syncthreads();
