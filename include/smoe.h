@@ -110,12 +110,12 @@ smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* cod
 /* Step 4 -- grouped gate/up.  moe_fused.hpp experts(): gate/up from the per-token int8 activations through the rows
  * `src` of group; per routed row r of expert e and output j in [0, 2F):
  *   GU[r][j] = sum_b dW[e][j][b] * dX[src r][b] * sum_{i in block b} (qW - 2) * qX     (fp32 result)
- *   xc, xs   q8 activations of the chunk, [T][H] and [T][H/32].
+ *   xc, xs   q8 activations of the chunk, [T][H] and [T][H/32]; T >= 1 (every src entry is < T).
  *   src, tiles  from smoe_group (tiles header[3] receives SMOE_ERR_TIMEOUT).   n = T*K (sizes the launch).
  *   wc, ws   gate/up weights, codes [E][2F][H/4], scales [E][2F][H/32].
  *   gu       fp32 [n][2F] out, row r = routed row r.
  *   H % 128 == 0, F % 64 == 0. */
-smoe_status smoe_experts_gateup(const int8_t* xc, const uint16_t* xs, const int32_t* src, int32_t* tiles,
+smoe_status smoe_experts_gateup(const int8_t* xc, const uint16_t* xs, int64_t T, const int32_t* src, int32_t* tiles,
                                 int64_t n, int E, const uint8_t* wc, const uint16_t* ws, int H, int F, float* gu,
                                 void* stream);
 

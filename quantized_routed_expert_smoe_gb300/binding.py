@@ -45,7 +45,8 @@ _SIGS = {
                     ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
     "smoe_quantize_q8": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                           ctypes.c_void_p], ctypes.c_int),
-    "smoe_experts_gateup": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+    "smoe_experts_gateup": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                             ctypes.c_int64,
                              ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                              ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_swiglu_requant": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
@@ -152,7 +153,7 @@ def smoe_quantize_q8(x, codes, scales, stream=None):
 def smoe_experts_gateup(xc, xs, src, tiles, n, wc, ws, gu, stream=None):
     E, twoF, H4 = wc.shape
     _check("smoe_experts_gateup", load_library().smoe_experts_gateup(
-        _dev(xc, torch.int8, "xc"), _dev(xs, torch.int16, "xs"), _dev(src, torch.int32, "src"),
+        _dev(xc, torch.int8, "xc"), _dev(xs, torch.int16, "xs"), xc.shape[0], _dev(src, torch.int32, "src"),
         _dev(tiles, torch.int32, "tiles"), n, E, _dev(wc, torch.uint8, "wc"), _dev(ws, torch.int16, "ws"),
         H4 * 4, twoF // 2, _dev(gu, torch.float32, "gu"), _stream(stream)))
 

@@ -15,23 +15,26 @@
 // sum of the exact products d_w (q_w - 2) d_a q_a.  The K loop runs two MMAs per 16-wide K step (A x B_hi,
 // A x B_lo).  The tensor core's fp32 accumulation aligns its addends with truncation, which over the 2 * K / 16 steps
 // of a whole row costs about 3e-6 of the result -- enough to flip requantised H codes -- so the accumulation is
-// two-level: each 64-wide K slice accumulates from zero into one of two tensor-memory buffers (the slice's partial is
-// small, so its truncation error is too), and the converter warps add each finished slice into fp32 registers with
-// round-to-nearest while the tensor core fills the other buffer.
+// two-level: each 64-wide K slice (kPromote slices) accumulates from zero into one of two tensor-memory buffers (the
+// partial is small, so its truncation error is too), and the converter warps add each finished partial into fp32
+// registers with round-to-nearest while the tensor core fills the other buffer.  One slice per partial keeps the
+// requantised H of the smallest test chunk identical to the oracle's; two slices flipped one H scale there.
 //
 // Tile: one CTA = one tile of the tile list (an expert and up to 256 of its routed rows, the MMA's N, a multiple of
 // 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB: weights are the M operand so that a
 // small expert wastes little).  Warp roles (three warpgroups, registers rebalanced with setmaxnreg):
 //   warpgroup 0   warp 0: tensor-memory allocation and, on one lane, the MMAs of each slice;
-//                 warps 1-3: producers -- cp.async copies of each slice's 2-bit weight codes, int8 rows (gathered
-//                 through src) and scales into a ring of up to 16 slices in shared memory;
+//                 warps 1-3: producers -- each slice's 2-bit weight codes (one TMA tile load), int8 rows (TMA
+//                 tile::gather4 loads through src, four rows each) and scales (cp.async) into a ring of up to 16
+//                 slices in shared memory;
 //   warpgroups 1-2  converters: decode a ring slice into the fp16 operand tiles of one of two stages (K-major,
-//                 128-byte swizzle), then add the previous slice's partial from tensor memory into their registers;
-//                 at the end they write the fp32 rows.
+//                 128-byte swizzle), 16 K values of one row per work item, then add the previous partial from tensor
+//                 memory into their registers; at the end they write the fp32 rows.
 //
 // K order inside the operand tiles: within each group of 16 K values, shared-memory position 2m holds value m and
 // position 2m+1 holds value m+8 (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so
 // the contraction is unchanged.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -54,6 +57,7 @@ constexpr int kStage = kATile + 2 * kBTile;
 constexpr int kRingBytes = 64 * 1024;          // raw-data ring
 constexpr int kMaxRing = 16;                   // slices in flight at most
 constexpr uint32_t kTmemCols = 512;            // two fp32 partial buffers, 128 lanes x N <= 256 columns each
+constexpr int kPromote = 1;                    // slices per tensor-memory partial
 // shared memory: [1 KB alignment slack][stages][ring][src rows 1 KB][barriers]
 constexpr int kSmemBytes = 1024 + kStages * kStage + kRingBytes + 1024 + 512;
 // registers: launched at 168 a thread (384 x 168 = 64,512 of 65,536); warpgroup 0 gives back to 56 and the two
@@ -62,20 +66,34 @@ constexpr int kRegsWg0 = 56;
 constexpr int kRegsConv = 224;
 
 // Raw slice layout in the ring (one 64-wide K slice of the tile): weight codes [128][16 B], weight scales [128][4 B],
-// activation codes [N][64 B], activation scales [N][4 B].
+// activation codes [N][64 B], activation scales [N][4 B].  TMA destinations are 128-byte aligned.
 __host__ __device__ constexpr int raw_slice_bytes(int N) { return (2048 + 512 + N * 68 + 127) & ~127; }
 
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 // arrive on `bar` once every cp.async this thread issued so far has landed (the arrival counts toward the phase)
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// TMA: a 2D tile (x bytes along the row, y rows) into shared memory, completing `bytes` on `bar`
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
+}
+// TMA: four rows (y0..y3) of a one-row-high box, placed one after another in shared memory
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)) : "memory");
+}
 
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {
@@ -86,67 +104,61 @@ __device__ __forceinline__ void setmaxnreg_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// This thread's 32 weights of one row into 4 16-byte chunks of the row's swizzled line: d * (q - 2).
-// `codes` holds 32 2-bit codes, value i at bits 2i..2i+1 of the 64-bit word.
-__device__ __forceinline__ void decode_weights(uint2 codes, uint16_t scale, uint4* row_line, int row, int half) {
+// 16 weights of one row (codes: value i at bits 2i..2i+1) into chunks 2*quarter and 2*quarter + 1 of the row's
+// swizzled 128-byte line: d * (q - 2).
+__device__ __forceinline__ void decode_weights16(uint32_t codes, uint16_t scale, uint4* row_line, int row,
+                                                 int quarter) {
     const __half2 d2 = __half2half2(__ushort_as_half(scale));
     const __half2 k1026 = __float2half2_rn(1026.0f);
-    uint32_t h[16];
+    uint32_t h[8];
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        const uint32_t w = g ? codes.y : codes.x;
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            // values m and m+8 as fp16 1024 + q in the two halves, then (1024 + q - 1026) * d = d * (q - 2)
-            const uint32_t v = ((w >> (2 * m)) & 0x00030003u) | 0x64006400u;
-            h[8 * g + m] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(v), k1026), d2));
-        }
+    for (int m = 0; m < 8; ++m) {
+        // values m and m+8 as fp16 1024 + q in the two halves, then (1024 + q - 1026) * d = d * (q - 2)
+        const uint32_t v = ((codes >> (2 * m)) & 0x00030003u) | 0x64006400u;
+        h[m] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(v), k1026), d2));
     }
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-        row_line[(half * 4 + c) ^ (row & 7)] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+    row_line[(2 * quarter) ^ (row & 7)] = make_uint4(h[0], h[1], h[2], h[3]);
+    row_line[(2 * quarter + 1) ^ (row & 7)] = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
-// 32 int8 activations of one row into the hi and lo tiles: hi = fp16_rn(d q), lo = d q - hi (exact).
-__device__ __forceinline__ void split_activations(uint4 c0, uint4 c1, uint16_t scale, uint4* hi_line,
-                                                  uint4* lo_line, int row, int half) {
+// 16 int8 activations of one row into the hi and lo tiles: hi = fp16_rn(d q), lo = d q - hi (exact).
+__device__ __forceinline__ void split_activations16(uint4 c, uint16_t scale, uint4* hi_line, uint4* lo_line, int row,
+                                                    int quarter) {
     const __half2 d2 = __half2half2(__ushort_as_half(scale));
     const __half2 k1152 = __float2half2_rn(1152.0f);
-    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    uint32_t hi[16], lo[16];
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    uint32_t hi[8], lo[8];
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            // bytes of values m and m+8 of the group into the low bytes of two halves; (b ^ 0x80) = b + 128 for a
-            // signed byte b, so the halves read 1024 + 128 + q
-            const uint32_t t = __byte_perm(w[4 * g + (m >> 2)], w[4 * g + 2 + (m >> 2)], (m & 3) | ((4 + (m & 3)) << 8));
-            const uint32_t v = (t & 0x00FF00FFu) ^ 0x64806480u;
-            const __half2 q = __hsub2(u32_as_h2(v), k1152);
-            const __half2 ph = __hmul2(q, d2);
-            const __half2 pl = __hfma2(q, d2, __hneg2(ph));
-            hi[8 * g + m] = h2_as_u32(ph);
-            lo[8 * g + m] = h2_as_u32(pl);
-        }
+    for (int m = 0; m < 8; ++m) {
+        // bytes of values m and m+8 into the low bytes of two halves; (b ^ 0x80) = b + 128 for a signed byte b, so
+        // the halves read 1024 + 128 + q
+        const uint32_t t = __byte_perm(w[m >> 2], w[2 + (m >> 2)], (m & 3) | ((4 + (m & 3)) << 8));
+        const uint32_t v = (t & 0x00FF00FFu) ^ 0x64806480u;
+        const __half2 q = __hsub2(u32_as_h2(v), k1152);
+        const __half2 ph = __hmul2(q, d2);
+        const __half2 pl = __hfma2(q, d2, __hneg2(ph));
+        hi[m] = h2_as_u32(ph);
+        lo[m] = h2_as_u32(pl);
     }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int pc = (half * 4 + c) ^ (row & 7);
-        hi_line[pc] = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-        lo_line[pc] = make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
-    }
+    const int c0 = (2 * quarter) ^ (row & 7), c1 = (2 * quarter + 1) ^ (row & 7);
+    hi_line[c0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    hi_line[c1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    lo_line[c0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    lo_line[c1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
 }
 
-__device__ __forceinline__ void zero_activations(uint4* hi_line, uint4* lo_line, int row, int half) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const int pc = (half * 4 + c) ^ (row & 7);
-        hi_line[pc] = make_uint4(0u, 0u, 0u, 0u);
-        lo_line[pc] = make_uint4(0u, 0u, 0u, 0u);
-    }
+__device__ __forceinline__ void zero_activations16(uint4* hi_line, uint4* lo_line, int row, int quarter) {
+    const int c0 = (2 * quarter) ^ (row & 7), c1 = (2 * quarter + 1) ^ (row & 7);
+    hi_line[c0] = hi_line[c1] = lo_line[c0] = lo_line[c1] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const ExpertsGemmArgs p) {
+struct GemmMaps {
+    CUtensorMap w;  // weight codes: [E * a_rows rows][K/4 bytes], box 16 bytes x 128 rows
+    CUtensorMap b;  // int8 rows:    [rows][K bytes], box 64 bytes x 1 row (gather4)
+};
+
+__global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const ExpertsGemmArgs p,
+                                                                   const __grid_constant__ GemmMaps maps) {
     int32_t* tiles = p.tiles;
     const int ti = blockIdx.y;
     if (ti >= tiles[0] || tiles[1] != 0) return;  // no such tile, or the grouping failed: nothing to do
@@ -187,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             mbar_init(&pempty[b], kConverters);
         }
         for (int r = 0; r < kMaxRing; ++r) {
-            mbar_init(&rfull[r], kProducers);
+            mbar_init(&rfull[r], kProducers + 1);  // cp.async arrivals + the TMA byte count's arrival
             mbar_init(&rempty[r], kConverters);
         }
         mbar_init(accf, 1);
@@ -215,9 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             if (lane == 0) {
                 const uint32_t idesc = idesc_f16_f32(kBM, N);
                 for (int kt = 0; kt < nk; ++kt) {
-                    const int s = kt % kStages, b = kt & 1;
+                    // slices kt of partial g = kt / kPromote go to buffer g & 1, which partial g - 2 has left
+                    const int s = kt % kStages, g = kt / kPromote, b = g & 1;
+                    const bool first = kt % kPromote == 0, last = kt % kPromote == kPromote - 1 || kt == nk - 1;
                     if (!mbar_wait(&full[s], (uint32_t)(kt / kStages) & 1u, abort_flag) ||
-                        (kt >= 2 && !mbar_wait(&pempty[b], (uint32_t)(kt / 2 - 1) & 1u, abort_flag))) {
+                        (first && g >= 2 && !mbar_wait(&pempty[b], (uint32_t)(g / 2 - 1) & 1u, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -227,11 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
 #pragma unroll
                     for (int j = 0; j < kBK / 16; ++j) {
                         const uint64_t ad = sdesc_k_sw128(a + 32 * j);
-                        mma_f16(d, ad, sdesc_k_sw128(bh + 32 * j), idesc, j > 0 ? 1u : 0u);
+                        mma_f16(d, ad, sdesc_k_sw128(bh + 32 * j), idesc, (j > 0 || !first) ? 1u : 0u);
                         mma_f16(d, ad, sdesc_k_sw128(bl + 32 * j), idesc, 1u);
                     }
                     mma_commit(&empty[s]);
-                    mma_commit(&pfull[b]);
+                    if (last) mma_commit(&pfull[b]);
                 }
                 mma_commit(accf);  // completes once every MMA issued above has completed (abort path included)
             }
@@ -240,9 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             // ------------------------------------------------------------------ producers (96 threads)
             const int pt = threadIdx.x - 32;
             const int64_t wrow0 = (int64_t)e * p.a_rows + m0;
-            const uint8_t* wc = p.wc + wrow0 * (p.K / 4);
             const uint16_t* ws = p.ws + wrow0 * (p.K / 32);
-            const int items = 128 + 128 + N * 4 + N;  // weight code rows, weight scale pairs, row chunks, row scales
+            const int groups = (rows + 3) >> 2;  // gather4 loads of this tile's rows
+            const uint32_t tx_bytes = 2048u + (uint32_t)groups * 256u;
             for (int kt = 0; kt < nk; ++kt) {
                 const int r = kt % depth;
                 if (kt >= depth && !mbar_wait(&rempty[r], (uint32_t)(kt / depth - 1) & 1u, abort_flag)) {
@@ -250,22 +264,22 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     break;
                 }
                 const uint32_t slot = smem_u32(ring) + (uint32_t)(r * sbytes);
-                for (int i = pt; i < items; i += kProducers) {
-                    if (i < 128) {
-                        cp_async_16(slot + i * 16, wc + (int64_t)i * (p.K / 4) + kt * 16);
-                    } else if (i < 256) {
-                        const int row = i - 128;
-                        cp_async_4(slot + o_as + row * 4, ws + (int64_t)row * (p.K / 32) + kt * 2);
-                    } else if (i < 256 + N * 4) {
-                        const int row = (i - 256) >> 2, ch = (i - 256) & 3;
-                        const int32_t sr = srcs[row];
-                        if (sr >= 0) cp_async_16(slot + o_bc + row * 64 + ch * 16, p.bc + (int64_t)sr * p.K + kt * kBK + ch * 16);
-                    } else {
-                        const int row = i - 256 - N * 4;
-                        const int32_t sr = srcs[row];
-                        if (sr >= 0) cp_async_4(slot + o_bs + row * 4, p.bs + (int64_t)sr * (p.K / 32) + kt * 2);
-                    }
+                if (pt == 0) {
+                    mbar_arrive_expect_tx(&rfull[r], tx_bytes);
+                    tma_load_2d(slot, &maps.w, kt * 16, (int)wrow0, &rfull[r]);
                 }
+                for (int g = pt; g < groups; g += kProducers) {
+                    const int r0 = 4 * g;
+                    const int y0 = srcs[r0];
+                    const int y1 = r0 + 1 < rows ? srcs[r0 + 1] : y0;
+                    const int y2 = r0 + 2 < rows ? srcs[r0 + 2] : y0;
+                    const int y3 = r0 + 3 < rows ? srcs[r0 + 3] : y0;
+                    tma_gather4(slot + o_bc + r0 * 64, &maps.b, kt * kBK, y0, y1, y2, y3, &rfull[r]);
+                }
+                for (int row = pt; row < 128; row += kProducers)
+                    cp_async_4(slot + o_as + row * 4, ws + (int64_t)row * (p.K / 32) + kt * 2);
+                for (int row = pt; row < rows; row += kProducers)
+                    cp_async_4(slot + o_bs + row * 4, p.bs + (int64_t)srcs[row] * (p.K / 32) + kt * 2);
                 cp_async_arrive(&rfull[r]);
             }
             cp_async_wait_all();  // no copy may land after the CTA has moved on
@@ -274,29 +288,38 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         setmaxnreg_inc<kRegsConv>();
         // ------------------------------------------------------------------ converters (256 threads)
         const int ct = threadIdx.x - 128;
-        const int ar = ct >> 1, half = ct & 1;  // weight row of this thread, and which 32 of the slice's 64 K
-        const int br0 = ar, br1 = ar + 128;     // routed rows of this thread (two passes)
-        const bool has0 = srcs[br0] >= 0, has1 = srcs[br1] >= 0;
-        // promotion: this thread owns TMEM lane 32*q + lane (weight row mrow) and columns [chalf*128, +128)
+        // work items of 16 K values: weight items ct and ct + 256 (row = item / 4, quarter = item % 4); row items
+        // ct + 256 i of the tile's 4 N (row, quarter) pairs
+        const int nb = (4 * N - ct + 255) / 256;     // row items of this thread (0..4)
+        // promotion: this thread owns TMEM lane 32*q + lane (weight row mrow) and the 32-column chunks
+        // 2 i + chalf, i = 0..3
         const int q = warp & 3;                 // the TMEM lane quarter this warp may access
-        const int chalf = (warp - 4) >> 2;      // warpgroup 1: columns [0, 128); warpgroup 2: [128, 256)
+        const int chalf = (warp - 4) >> 2;      // warpgroup 1: even chunks; warpgroup 2: odd chunks
         const int mrow = 32 * q + lane;
-        float acc[128];
+        float acc[4][32];
 #pragma unroll
-        for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-        auto promote = [&](int k) -> bool {
-            const int b = k & 1;
-            if (!mbar_wait(&pfull[b], (uint32_t)(k / 2) & 1u, abort_flag)) return false;
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int k = 0; k < 32; ++k) acc[i][k] = 0.0f;
+        auto promote = [&](int g) -> bool {
+            const int b = g & 1;
+            if (!mbar_wait(&pfull[b], (uint32_t)(g / 2) & 1u, abort_flag)) return false;
             tc_fence_after();
+            const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)b;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int c0 = chalf * 128 + 32 * c;
+            for (int i = 0; i < 4; i += 2) {
+                const int c0 = 32 * (2 * i + chalf), c1 = 32 * (2 * i + 2 + chalf);
                 if (c0 < N) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)b + (uint32_t)c0, v);
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(base + (uint32_t)c0, v0);
+                    if (c1 < N) tmem_ld_32x32b_x32(base + (uint32_t)c1, v1);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[32 * c + i] += __uint_as_float(v[i]);
+                    for (int k = 0; k < 32; ++k) acc[i][k] += __uint_as_float(v0[k]);
+                    if (c1 < N) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) acc[i + 1][k] += __uint_as_float(v1[k]);
+                    }
                 }
             }
             tc_fence_before();
@@ -311,21 +334,27 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 break;
             }
             const uint8_t* slot = ring + r * sbytes;
-            const uint2 acodes = *reinterpret_cast<const uint2*>(slot + ar * 16 + half * 8);
-            const uint16_t ascale = *reinterpret_cast<const uint16_t*>(slot + o_as + ar * 4 + half * 2);
-            uint4 b0c0 = make_uint4(0, 0, 0, 0), b0c1 = b0c0, b1c0 = b0c0, b1c1 = b0c0;
-            uint16_t b0s = 0, b1s = 0;
-            if (has0) {
-                const uint4* c = reinterpret_cast<const uint4*>(slot + o_bc + br0 * 64 + half * 32);
-                b0c0 = c[0];
-                b0c1 = c[1];
-                b0s = *reinterpret_cast<const uint16_t*>(slot + o_bs + br0 * 4 + half * 2);
+            // read this thread's raw values, then give the ring slot back
+            uint32_t wcode[2];
+            uint16_t wscale[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
+                wcode[i] = *reinterpret_cast<const uint32_t*>(slot + row * 16 + qu * 4);
+                wscale[i] = *reinterpret_cast<const uint16_t*>(slot + o_as + row * 4 + (qu >> 1) * 2);
             }
-            if (has1) {
-                const uint4* c = reinterpret_cast<const uint4*>(slot + o_bc + br1 * 64 + half * 32);
-                b1c0 = c[0];
-                b1c1 = c[1];
-                b1s = *reinterpret_cast<const uint16_t*>(slot + o_bs + br1 * 4 + half * 2);
+            uint4 bcode[4];
+            uint16_t bscale[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
+                if (i < nb && row < rows) {
+                    bcode[i] = *reinterpret_cast<const uint4*>(slot + o_bc + row * 64 + qu * 16);
+                    bscale[i] = *reinterpret_cast<const uint16_t*>(slot + o_bs + row * 4 + (qu >> 1) * 2);
+                } else {
+                    bcode[i] = make_uint4(0u, 0u, 0u, 0u);
+                    bscale[i] = 0;
+                }
             }
             mbar_arrive(&rempty[r]);
             const int s = kt % kStages;
@@ -337,29 +366,34 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             uint4* a_tile = reinterpret_cast<uint4*>(st);
             uint4* hi_tile = reinterpret_cast<uint4*>(st + kATile);
             uint4* lo_tile = reinterpret_cast<uint4*>(st + kATile + kBTile);
-            decode_weights(acodes, ascale, a_tile + ar * 8, ar, half);
-            if (br0 < N) {
-                if (has0) split_activations(b0c0, b0c1, b0s, hi_tile + br0 * 8, lo_tile + br0 * 8, br0, half);
-                else zero_activations(hi_tile + br0 * 8, lo_tile + br0 * 8, br0, half);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
+                decode_weights16(wcode[i], wscale[i], a_tile + row * 8, row, qu);
             }
-            if (br1 < N) {
-                if (has1) split_activations(b1c0, b1c1, b1s, hi_tile + br1 * 8, lo_tile + br1 * 8, br1, half);
-                else zero_activations(hi_tile + br1 * 8, lo_tile + br1 * 8, br1, half);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
+                if (i < nb) {
+                    if (row < rows) split_activations16(bcode[i], bscale[i], hi_tile + row * 8, lo_tile + row * 8, row, qu);
+                    else zero_activations16(hi_tile + row * 8, lo_tile + row * 8, row, qu);
+                }
             }
             fence_async_smem();
             mbar_arrive(&full[s]);
-            if (kt >= 1 && !promote(kt - 1)) ok = false;
+            // after the first slice of partial g has been handed over, add partial g - 1
+            if (kt % kPromote == 0 && kt >= kPromote && !promote(kt / kPromote - 1)) ok = false;
         }
-        if (ok && !promote(nk - 1)) ok = false;
+        if (ok && !promote((nk - 1) / kPromote)) ok = false;
         if (ok) {
             // ------------------------------------------------------------------ epilogue: fp32 rows out
             float* outcol = p.out + (m0 + mrow);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int i = 0; i < 4; ++i) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int col = chalf * 128 + 32 * c + i;
-                    if (col < rows) outcol[(int64_t)(row0 + col) * p.a_rows] = acc[32 * c + i];
+                for (int k = 0; k < 32; ++k) {
+                    const int col = 32 * (2 * i + chalf) + k;
+                    if (col < rows) outcol[(int64_t)(row0 + col) * p.a_rows] = acc[i][k];
                 }
             }
         }
@@ -377,6 +411,36 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     }
 }
 
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2D uint8 tensor [rows][row_bytes] (row stride row_bytes), box box_x bytes x box_y rows, no swizzle
+bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_x, uint32_t box_y) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {row_bytes, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_x, box_y};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s) {
@@ -390,8 +454,12 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
         attr_done |= 1ull << dev;
     }
     if (max_tiles <= 0) return cudaSuccess;
+    GemmMaps maps;
+    if (!make_map(&maps.w, a.wc, (uint64_t)a.K / 4, (uint64_t)a.n_experts * a.a_rows, 16, kBM) ||
+        !make_map(&maps.b, a.bc, (uint64_t)a.K, (uint64_t)a.b_rows, kBK, 1))
+        return cudaErrorInvalidValue;
     const dim3 grid((unsigned)(a.a_rows / kBM), (unsigned)max_tiles);
-    experts_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(a);
+    experts_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, maps);
     return cudaGetLastError();
 }
 

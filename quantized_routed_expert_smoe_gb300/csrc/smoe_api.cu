@@ -108,17 +108,18 @@ static smoe_status check_gemm_shape(int64_t n, int E, int H, int F) {
     return SMOE_OK;
 }
 
-smoe_status smoe_experts_gateup(const int8_t* xc, const uint16_t* xs, const int32_t* src, int32_t* tiles,
+smoe_status smoe_experts_gateup(const int8_t* xc, const uint16_t* xs, int64_t T, const int32_t* src, int32_t* tiles,
                                 int64_t n, int E, const uint8_t* wc, const uint16_t* ws, int H, int F, float* gu,
                                 void* stream) {
     const smoe_status st = check_gemm_shape(n, E, H, F);
     if (st != SMOE_OK) return st;
     if (n == 0) return SMOE_OK;
+    if (T < 1 || T > INT32_MAX) return SMOE_ERR_ARG;
     if (!aligned16(xc) || !aligned16(xs) || !aligned16(src) || !aligned16(tiles) || !aligned16(wc) ||
         !aligned16(ws) || !aligned16(gu))
         return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{xc, xs, src, tiles, wc, ws, 2 * F, H, gu};
+    smoe::ExpertsGemmArgs a{xc, xs, src, tiles, wc, ws, 2 * F, H, gu, T, E};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 
@@ -138,7 +139,7 @@ smoe_status smoe_experts_down(const int8_t* hc, const uint16_t* hs, int32_t* til
     if (!aligned16(hc) || !aligned16(hs) || !aligned16(tiles) || !aligned16(wc) || !aligned16(ws) || !aligned16(dm))
         return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{hc, hs, nullptr, tiles, wc, ws, H, F, dm};
+    smoe::ExpertsGemmArgs a{hc, hs, nullptr, tiles, wc, ws, H, F, dm, n, E};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 

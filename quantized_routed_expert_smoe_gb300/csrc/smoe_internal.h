@@ -32,6 +32,8 @@ struct ExpertsGemmArgs {
     int a_rows;           // weight rows per expert (2F or H)
     int K;                // contraction length (H or F)
     float* out;           // [n][a_rows]
+    int64_t b_rows;       // rows of the q8 B matrix (T for gate/up, n for down)
+    int n_experts;        // E
 };
 cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s);
 

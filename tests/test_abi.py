@@ -63,7 +63,7 @@ def test_host_side_rejections_need_no_gpu(lib):
     # q8: cols not a multiple of 32
     assert lib.smoe_quantize_q8(fake, 4, 48, fake, fake, null) == ARG
     # gemm shapes the kernels do not cover
-    assert lib.smoe_experts_gateup(fake, fake, fake, fake, 10, 4, fake, fake, 96, 64, fake, null) == UNSUP
+    assert lib.smoe_experts_gateup(fake, fake, 5, fake, fake, 10, 4, fake, fake, 96, 64, fake, null) == UNSUP
     assert lib.smoe_experts_down(fake, fake, fake, 10, 4, fake, fake, 256, 48, fake, null) == UNSUP
     # group: tiles buffer too small
     assert lib.smoe_group(fake, 8, 2, 4, fake, fake, fake, fake, fake, 16, fake, 1 << 20, null) == ARG
