@@ -102,6 +102,18 @@ smoe_status smoe_group(const int32_t* ids, int64_t T, int K, int E, int32_t* cou
                        int32_t* slot, int32_t* tiles, size_t tiles_bytes, void* work, size_t work_bytes,
                        void* stream);
 
+/* smoe_group without a caller-provided scratch buffer (the paper has no counterpart: this is a library service).
+ * For callers that cannot allocate device memory themselves -- e.g. a runtime whose device memory is planned once up
+ * front, or a serving loop that must not call cudaMalloc between requests because it can synchronise the device.
+ * Same arguments, outputs and errors as smoe_group, minus `work`: the scratch (at most 48 x 1024 int32 counts,
+ * 192 KiB) lives in a __device__ array inside the library that every GPU loading it keeps until the process exits.
+ * No cudaMalloc, cudaFree or allocating routine is called.  The first call on a device looks the array's device
+ * address up (cudaGetSymbolAddress, with that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array: calls whose kernels overlap on the GPU race and give wrong tables.
+ * A size whose scratch would not fit is refused with SMOE_ERR_UNSUPPORTED (no valid T, K, E reaches it). */
+smoe_status smoe_group_noalloc(const int32_t* ids, int64_t T, int K, int E, int32_t* counts, int32_t* offsets,
+                               int32_t* src, int32_t* slot, int32_t* tiles, size_t tiles_bytes, void* stream);
+
 /* Step 3 -- q8 activations.  Page "Strata compare v0.1.35...v0.1.37", moe_fused.hpp quantize_act: the layer input is
  * rounded to int8 once per TOKEN (not per routed slot) with one scale per 32 values.
  *   x fp32 [rows][cols] (|x| < 65504) -> codes int8 [rows][cols], scales fp16 [rows][cols/32].  cols % 32 == 0. */

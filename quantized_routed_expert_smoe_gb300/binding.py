@@ -43,6 +43,9 @@ _SIGS = {
     "smoe_group": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                     ctypes.c_size_t, ctypes.c_void_p], ctypes.c_int),
+    "smoe_group_noalloc": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+                            ctypes.c_void_p], ctypes.c_int),
     "smoe_quantize_q8": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                           ctypes.c_void_p], ctypes.c_int),
     "smoe_experts_gateup": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
@@ -141,6 +144,15 @@ def smoe_group(ids, E, counts, offsets, src, slot, tiles, work, stream=None):
         _dev(offsets, torch.int32, "offsets"), _dev(src, torch.int32, "src"), _dev(slot, torch.int32, "slot"),
         _dev(tiles, torch.int32, "tiles"), tiles.numel() * 4, _dev(work, torch.uint8, "work"), work.numel(),
         _stream(stream)))
+
+
+def smoe_group_noalloc(ids, E, counts, offsets, src, slot, tiles, stream=None):
+    """smoe_group with the library's built-in scratch (for callers that cannot allocate device memory)."""
+    T, K = ids.shape
+    _check("smoe_group_noalloc", load_library().smoe_group_noalloc(
+        _dev(ids, torch.int32, "ids"), T, K, E, _dev(counts, torch.int32, "counts"),
+        _dev(offsets, torch.int32, "offsets"), _dev(src, torch.int32, "src"), _dev(slot, torch.int32, "slot"),
+        _dev(tiles, torch.int32, "tiles"), tiles.numel() * 4, _stream(stream)))
 
 
 def smoe_quantize_q8(x, codes, scales, stream=None):
