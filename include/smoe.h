@@ -23,6 +23,12 @@
  *                    bits 2i..2i+1 of byte j; scales fp16 [E][rows][cols/32].  The value of a weight is d * (q - 2),
  *                    q in {0,1,2,3}.  Gate/up matrix: rows [0, F) gate, [F, 2F) up, cols H.  Down matrix: rows H,
  *                    cols F.
+ *   q8 slice form    what the expert products read (written by smoe_quantize_q8 / smoe_swiglu_requant beside the
+ *                    planar form): per row and per 64 values, 80 bytes = the 64 codes, the two fp16 scales of the
+ *                    slice's two 32-value blocks, 12 zero bytes; [rows][cols/64][80].  smoe_slices_bytes sizes it.
+ *   packed Q2        what the expert products read as weights (smoe_pack_q2 writes it once from the row-major form):
+ *                    per (expert, 128-row tile, 64-value slice) a 2560-byte block = the tile's 128 rows x 16 code
+ *                    bytes, then its 128 rows x 2 fp16 scales; blocks ordered by expert, tile, slice.
  *   tiles            int32 [4 + 4 * smoe_max_tiles(n, E)]: header {n_tiles, group_status, n, kernel_status}, then
  *                    per tile {expert, first row, rows, 0}; each expert's c rows split into ceil(c/256) near-equal
  *                    tiles [floor(i*c/nt), floor((i+1)*c/nt)), experts in id order.
@@ -116,34 +122,49 @@ smoe_status smoe_group_noalloc(const int32_t* ids, int64_t T, int K, int E, int3
 
 /* Step 3 -- q8 activations.  Page "Strata compare v0.1.35...v0.1.37", moe_fused.hpp quantize_act: the layer input is
  * rounded to int8 once per TOKEN (not per routed slot) with one scale per 32 values.
- *   x fp32 [rows][cols] (|x| < 65504) -> codes int8 [rows][cols], scales fp16 [rows][cols/32].  cols % 32 == 0. */
-smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales, void* stream);
+ *   x fp32 [rows][cols] (|x| < 65504) -> codes int8 [rows][cols], scales fp16 [rows][cols/32].  cols % 32 == 0.
+ *   slices   optional (NULL: not written): the same codes and scales in slice form, smoe_slices_bytes(rows, cols)
+ *            bytes; needs cols % 64 == 0. */
+smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales,
+                             uint8_t* slices, void* stream);
+/* Bytes of the slice form of rows x cols q8 values: rows * (cols / 64) * 80. */
+size_t smoe_slices_bytes(int64_t rows, int cols);
+
+/* Weight preparation (once per weight set): the row-major Q2 matrices of E experts (codes [E][rows][cols/4], scales
+ * [E][rows][cols/32]) into the packed form the expert products read.  rows % 128 == 0, cols % 64 == 0.
+ * packed: smoe_pack_q2_bytes(E, rows, cols) bytes (the same size as codes + scales). */
+smoe_status smoe_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, uint8_t* packed,
+                         void* stream);
+size_t smoe_pack_q2_bytes(int E, int rows, int cols);
 
 /* Step 4 -- grouped gate/up.  moe_fused.hpp experts(): gate/up from the per-token int8 activations through the rows
  * `src` of group; per routed row r of expert e and output j in [0, 2F):
  *   GU[r][j] = sum_b dW[e][j][b] * dX[src r][b] * sum_{i in block b} (qW - 2) * qX     (fp32 result)
- *   xc, xs   q8 activations of the chunk, [T][H] and [T][H/32]; T >= 1 (every src entry is < T).
+ *   xsl      q8 activations of the chunk in slice form ([T][H/64][80], from smoe_quantize_q8); T >= 1, every src
+ *            entry is < T.
  *   src, tiles  from smoe_group (tiles header[3] receives SMOE_ERR_TIMEOUT).   n = T*K (sizes the launch).
- *   wc, ws   gate/up weights, codes [E][2F][H/4], scales [E][2F][H/32].
+ *   wgu      gate/up weights [E][2F][H] packed by smoe_pack_q2.
  *   gu       fp32 [n][2F] out, row r = routed row r.
  *   H % 128 == 0, F % 64 == 0. */
-smoe_status smoe_experts_gateup(const int8_t* xc, const uint16_t* xs, int64_t T, const int32_t* src, int32_t* tiles,
-                                int64_t n, int E, const uint8_t* wc, const uint16_t* ws, int H, int F, float* gu,
-                                void* stream);
+smoe_status smoe_experts_gateup(const uint8_t* xsl, int64_t T, const int32_t* src, int32_t* tiles, int64_t n, int E,
+                                const uint8_t* wgu, int H, int F, float* gu, void* stream);
 
 /* Step 5 -- SwiGLU and requantisation.  Page "src/prefill/prefill.cpp": mmq::swiglu(GU, H, rows, ...) then the
  * int8 rounding of H; moe_fused.hpp: "SwiGLU, H as int8".
  *   gu fp32 [n][2F] -> h_j = silu(gu[r][j]) * gu[r][F + j] (fp32; silu(g) = g / (1 + exp(-g))), then the q8 rule:
- *   hc int8 [n][F], hs fp16 [n][F/32].  F % 32 == 0. */
-smoe_status smoe_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, void* stream);
+ *   hc int8 [n][F], hs fp16 [n][F/32].  F % 32 == 0.
+ *   slices   optional (NULL: not written): H in slice form, smoe_slices_bytes(n, F) bytes; needs F % 64 == 0. */
+smoe_status smoe_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint8_t* slices,
+                                void* stream);
 
 /* Step 6 -- grouped down.  moe_fused.hpp experts(): "down into dm [n][2560] FP32 at the rows of group":
  *   Dm[r][o] = sum_b dW[e][o][b] * dH[r][b] * sum_{i in block b} (qW - 2) * qH,   o in [0, H)
- *   hc, hs   q8 H rows [n][F], [n][F/32] (routed-row order).   tiles from smoe_group.
- *   wc, ws   down weights, codes [E][H][F/4], scales [E][H][F/32].
+ *   hsl      q8 H rows in slice form ([n][F/64][80], routed-row order, from smoe_swiglu_requant).  tiles from
+ *            smoe_group.
+ *   wd       down weights [E][H][F] packed by smoe_pack_q2.
  *   dm       fp32 [n][H] out.   H % 128 == 0, F % 64 == 0. */
-smoe_status smoe_experts_down(const int8_t* hc, const uint16_t* hs, int32_t* tiles, int64_t n, int E,
-                              const uint8_t* wc, const uint16_t* ws, int H, int F, float* dm, void* stream);
+smoe_status smoe_experts_down(const uint8_t* hsl, int32_t* tiles, int64_t n, int E, const uint8_t* wd, int H, int F,
+                              float* dm, void* stream);
 
 /* Step 7 -- combine.  The combine that reads the per-slot rows (page "src/prefill/prefill.cpp", the engine's
  * "fused CUDA weighted reduction"): Y[t][o] = sum_{k=0}^{K-1} w[t][k] * dm[slot[t*K+k]][o], summed in k order in

@@ -47,16 +47,18 @@ _SIGS = {
                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                             ctypes.c_void_p], ctypes.c_int),
     "smoe_quantize_q8": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
-                          ctypes.c_void_p], ctypes.c_int),
-    "smoe_experts_gateup": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
-                             ctypes.c_int64,
-                             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
-                             ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
-    "smoe_swiglu_requant": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                          ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_slices_bytes": ([ctypes.c_int64, ctypes.c_int], ctypes.c_size_t),
+    "smoe_pack_q2": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                      ctypes.c_void_p], ctypes.c_int),
+    "smoe_pack_q2_bytes": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
+    "smoe_experts_gateup": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                             ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                              ctypes.c_void_p], ctypes.c_int),
-    "smoe_experts_down": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
-                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
-                           ctypes.c_void_p], ctypes.c_int),
+    "smoe_swiglu_requant": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                             ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_experts_down": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                           ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_combine": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                       ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
 }
@@ -128,6 +130,18 @@ def group_work_bytes(n: int, E: int) -> int:
     return int(load_library().smoe_group_work_bytes(n, E))
 
 
+def slices_bytes(rows: int, cols: int) -> int:
+    return int(load_library().smoe_slices_bytes(rows, cols))
+
+
+def pack_q2_bytes(E: int, rows: int, cols: int) -> int:
+    return int(load_library().smoe_pack_q2_bytes(E, rows, cols))
+
+
+def _opt(t, dtype, name):
+    return ctypes.c_void_p(0) if t is None else _dev(t, dtype, name)
+
+
 # ------------------------------------------------------------------------------------------------ the seven calls
 def smoe_route_topk(logits, ids, w, stream=None):
     T, E = logits.shape
@@ -155,34 +169,38 @@ def smoe_group_noalloc(ids, E, counts, offsets, src, slot, tiles, stream=None):
         _dev(tiles, torch.int32, "tiles"), tiles.numel() * 4, _stream(stream)))
 
 
-def smoe_quantize_q8(x, codes, scales, stream=None):
+def smoe_quantize_q8(x, codes, scales, slices=None, stream=None):
     rows, cols = x.shape
     _check("smoe_quantize_q8", load_library().smoe_quantize_q8(
         _dev(x, torch.float32, "x"), rows, cols, _dev(codes, torch.int8, "codes"),
-        _dev(scales, torch.int16, "scales"), _stream(stream)))
+        _dev(scales, torch.int16, "scales"), _opt(slices, torch.uint8, "slices"), _stream(stream)))
 
 
-def smoe_experts_gateup(xc, xs, src, tiles, n, wc, ws, gu, stream=None):
-    E, twoF, H4 = wc.shape
+def smoe_pack_q2(codes, scales, packed, stream=None):
+    """Row-major Q2 weights (codes uint8 [E][rows][cols/4], scales int16 bits [E][rows][cols/32]) -> packed."""
+    E, rows, c4 = codes.shape
+    _check("smoe_pack_q2", load_library().smoe_pack_q2(
+        _dev(codes, torch.uint8, "codes"), _dev(scales, torch.int16, "scales"), E, rows, c4 * 4,
+        _dev(packed, torch.uint8, "packed"), _stream(stream)))
+
+
+def smoe_experts_gateup(xsl, T, src, tiles, n, E, wgu, H, F, gu, stream=None):
     _check("smoe_experts_gateup", load_library().smoe_experts_gateup(
-        _dev(xc, torch.int8, "xc"), _dev(xs, torch.int16, "xs"), xc.shape[0], _dev(src, torch.int32, "src"),
-        _dev(tiles, torch.int32, "tiles"), n, E, _dev(wc, torch.uint8, "wc"), _dev(ws, torch.int16, "ws"),
-        H4 * 4, twoF // 2, _dev(gu, torch.float32, "gu"), _stream(stream)))
+        _dev(xsl, torch.uint8, "xsl"), T, _dev(src, torch.int32, "src"), _dev(tiles, torch.int32, "tiles"), n, E,
+        _dev(wgu, torch.uint8, "wgu"), H, F, _dev(gu, torch.float32, "gu"), _stream(stream)))
 
 
-def smoe_swiglu_requant(gu, hc, hs, stream=None):
+def smoe_swiglu_requant(gu, hc, hs, slices=None, stream=None):
     n, twoF = gu.shape
     _check("smoe_swiglu_requant", load_library().smoe_swiglu_requant(
         _dev(gu, torch.float32, "gu"), n, twoF // 2, _dev(hc, torch.int8, "hc"), _dev(hs, torch.int16, "hs"),
-        _stream(stream)))
+        _opt(slices, torch.uint8, "slices"), _stream(stream)))
 
 
-def smoe_experts_down(hc, hs, tiles, n, wc, ws, dm, stream=None):
-    E, H, F4 = wc.shape
+def smoe_experts_down(hsl, tiles, n, E, wd, H, F, dm, stream=None):
     _check("smoe_experts_down", load_library().smoe_experts_down(
-        _dev(hc, torch.int8, "hc"), _dev(hs, torch.int16, "hs"), _dev(tiles, torch.int32, "tiles"), n, E,
-        _dev(wc, torch.uint8, "wc"), _dev(ws, torch.int16, "ws"), H, F4 * 4, _dev(dm, torch.float32, "dm"),
-        _stream(stream)))
+        _dev(hsl, torch.uint8, "hsl"), _dev(tiles, torch.int32, "tiles"), n, E, _dev(wd, torch.uint8, "wd"), H, F,
+        _dev(dm, torch.float32, "dm"), _stream(stream)))
 
 
 def smoe_combine(dm, slot, w, y, stream=None):
@@ -204,10 +222,9 @@ class SmoeBlock:
         self.T, self.H, self.E, self.K, self.F = T, H, E, K, F
         dev = torch.device(device)
         as_t = lambda a, dt: torch.as_tensor(a).to(device=dev, dtype=dt).contiguous()
-        self.wgu_c = as_t(wgu_c, torch.uint8) if not isinstance(wgu_c, torch.Tensor) else wgu_c.to(dev).contiguous()
-        self.wgu_s = _as_i16(wgu_s, dev)
-        self.wd_c = as_t(wd_c, torch.uint8) if not isinstance(wd_c, torch.Tensor) else wd_c.to(dev).contiguous()
-        self.wd_s = _as_i16(wd_s, dev)
+        # the expert weights, packed once for the expert products (the row-major copies are not kept)
+        self.wgu = pack_weights(wgu_c, wgu_s, dev)
+        self.wd = pack_weights(wd_c, wd_s, dev)
         n = T * K
         self.n = n
         e = lambda *s, dt: torch.empty(*s, dtype=dt, device=dev)
@@ -221,9 +238,11 @@ class SmoeBlock:
         self.work = e(max(group_work_bytes(n, E), 16), dt=torch.uint8)
         self.xc = e(T, H, dt=torch.int8)
         self.xs = e(T, H // 32, dt=torch.int16)
+        self.xsl = e(max(slices_bytes(T, H), 16), dt=torch.uint8)
         self.gu = e(n, 2 * F, dt=torch.float32)
         self.hc = e(n, F, dt=torch.int8)
         self.hs = e(n, F // 32, dt=torch.int16)
+        self.hsl = e(max(slices_bytes(n, F), 16), dt=torch.uint8)
         self.dm = e(n, H, dt=torch.float32)
         self.y = e(T, H, dt=torch.float32)
 
@@ -231,10 +250,11 @@ class SmoeBlock:
         smoe_route_topk(logits, self.ids, self.w, stream)
         smoe_group(self.ids, self.E, self.counts, self.offsets, self.src[:self.n], self.slot[:self.n], self.tiles,
                    self.work, stream)
-        smoe_quantize_q8(x, self.xc, self.xs, stream)
-        smoe_experts_gateup(self.xc, self.xs, self.src, self.tiles, self.n, self.wgu_c, self.wgu_s, self.gu, stream)
-        smoe_swiglu_requant(self.gu, self.hc, self.hs, stream)
-        smoe_experts_down(self.hc, self.hs, self.tiles, self.n, self.wd_c, self.wd_s, self.dm, stream)
+        smoe_quantize_q8(x, self.xc, self.xs, self.xsl, stream)
+        smoe_experts_gateup(self.xsl, self.T, self.src, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.gu,
+                            stream)
+        smoe_swiglu_requant(self.gu, self.hc, self.hs, self.hsl, stream)
+        smoe_experts_down(self.hsl, self.tiles, self.n, self.E, self.wd, self.H, self.F, self.dm, stream)
         smoe_combine(self.dm, self.slot, self.w, self.y, stream)
         return self.y
 
@@ -242,6 +262,18 @@ class SmoeBlock:
         """(group status, kernel status) from the tiles header; reads the device (synchronises)."""
         h = self.tiles[:4].cpu().tolist()
         return h[1], h[3]
+
+
+def pack_weights(codes, scales, device="cuda"):
+    """Row-major Q2 weights (numpy or torch: codes [E][rows][cols/4], scales fp16 bits [E][rows][cols/32]) packed on
+    the device for the expert products."""
+    dev = torch.device(device)
+    c = codes.to(dev).contiguous() if isinstance(codes, torch.Tensor) else torch.from_numpy(codes).to(dev).contiguous()
+    s = _as_i16(scales, dev)
+    E, rows, c4 = c.shape
+    packed = torch.empty(pack_q2_bytes(E, rows, c4 * 4), dtype=torch.uint8, device=dev)
+    smoe_pack_q2(c, s, packed)
+    return packed
 
 
 def _as_i16(a, dev):

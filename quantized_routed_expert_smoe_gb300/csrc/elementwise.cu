@@ -9,6 +9,10 @@
 // The q8 rule (the library's activation format): for 32 fp32 values, amax = max |x|, d = fp16_rne(amax / 127) with
 // an IEEE fp32 division, and q = clamp(roundf(x / float(d)), -127, 127), again an IEEE fp32 division, roundf
 // rounding half away from zero; d == 0 gives zero codes.  Four threads share a block, eight values each.
+//
+// Both q8 writers can also emit the expert products' slice form of the same codes: per row and per 64 values, 80
+// bytes = the 64 codes, the two fp16 scales of the slice's 32-value blocks, 12 zero bytes (one 80-byte row piece per
+// slice, so a single TMA row load brings a slice's codes with their scales).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -17,6 +21,19 @@
 
 namespace smoe {
 namespace {
+
+// 8 codes at value offset c of a row into the slice form: 80 bytes per 64 values of the row
+__device__ __forceinline__ void put_slice(uint8_t* slices, int64_t row, int cols, int c, uint2 q, uint16_t scale,
+                                          bool block_leader) {
+    uint8_t* piece = slices + (row * (cols / 64) + c / 64) * 80;
+    const int w = c % 64;
+    *reinterpret_cast<uint2*>(piece + w) = q;
+    if (block_leader) *reinterpret_cast<uint16_t*>(piece + 64 + (w / 32) * 2) = scale;
+    if (w == 56) {
+        uint32_t* pad = reinterpret_cast<uint32_t*>(piece + 68);
+        pad[0] = pad[1] = pad[2] = 0u;
+    }
+}
 
 // q8 of the 8 values v held by this thread, its block being spread over 4 consecutive lanes; returns the 8 codes
 // packed little-endian and the block's fp16 scale bits.
@@ -46,8 +63,9 @@ __device__ __forceinline__ uint2 q8_encode8(const float (&v)[8], uint16_t* scale
 }
 
 // step 3: x [rows][cols] -> codes, scales; thread i covers elements [8i, 8i + 8) of the flattened rows
-__global__ void __launch_bounds__(256) quantize_q8_kernel(const float4* __restrict__ x, int64_t n8,
-                                                          uint2* __restrict__ codes, uint16_t* __restrict__ scales) {
+__global__ void __launch_bounds__(256) quantize_q8_kernel(const float4* __restrict__ x, int64_t n8, int cols,
+                                                          uint2* __restrict__ codes, uint16_t* __restrict__ scales,
+                                                          uint8_t* __restrict__ slices) {
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < n8; base += (int64_t)gridDim.x * blockDim.x) {
         const int64_t i = base + threadIdx.x;
         // n8 is a multiple of 4 (cols % 32 == 0), so every group of 4 lanes is either all in range or all out;
@@ -64,6 +82,10 @@ __global__ void __launch_bounds__(256) quantize_q8_kernel(const float4* __restri
         if (in) {
             codes[i] = q;
             if ((i & 3) == 0) scales[i >> 2] = sb;
+            if (slices) {
+                const int64_t r = (8 * i) / cols;
+                put_slice(slices, r, cols, (int)(8 * i - r * cols), q, sb, (i & 3) == 0);
+            }
         }
     }
 }
@@ -71,7 +93,8 @@ __global__ void __launch_bounds__(256) quantize_q8_kernel(const float4* __restri
 // step 5: per routed row, h_j = silu(g_j) * u_j with g = gu[r][j], u = gu[r][F + j], then the q8 rule per 32 of h.
 // thread i covers h values [8c, 8c + 8) of row r = i / (F/8), c = i % (F/8).
 __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __restrict__ gu, int64_t n, int F,
-                                                             uint2* __restrict__ hc, uint16_t* __restrict__ hs) {
+                                                             uint2* __restrict__ hc, uint16_t* __restrict__ hs,
+                                                             uint8_t* __restrict__ slices) {
     const int64_t per_row = F / 8;
     const int64_t total = n * per_row;
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
@@ -93,6 +116,10 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
         if (in) {
             hc[i] = q;  // row r's codes start at r * F = 8 * (r * per_row): element offset 8i
             if ((i & 3) == 0) hs[i >> 2] = sb;
+            if (slices) {
+                const int64_t r = i / per_row;
+                put_slice(slices, r, F, (int)(8 * (i - r * per_row)), q, sb, (i & 3) == 0);
+            }
         }
     }
 }
@@ -119,6 +146,33 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     reinterpret_cast<float4*>(y + t * H)[o4] = acc;
 }
 
+// Q2 weights, row-major [E][rows][cols/4] codes + [E][rows][cols/32] scales, to the expert products' packed form:
+// per (expert, 128-row tile, 64-value slice) one 2560-byte block = the tile's 128 x 16 code bytes, then its 128 x 2
+// scales.  One thread per 16-byte piece of a block (128 code pieces, 32 scale pieces).
+__global__ void __launch_bounds__(160) pack_q2_kernel(const uint8_t* __restrict__ codes,
+                                                      const uint16_t* __restrict__ scales, int rows, int cols,
+                                                      uint8_t* __restrict__ packed) {
+    const int64_t blk = blockIdx.x;  // ((e * rows/128 + mt) * cols/64 + kt)
+    const int nkt = cols / 64, nmt = rows / 128;
+    const int kt = (int)(blk % nkt);
+    const int64_t emt = blk / nkt;  // e * nmt + mt
+    const int64_t row0 = emt * 128;  // first row of the tile in [E * rows]
+    (void)nmt;
+    uint8_t* out = packed + blk * 2560;
+    const int t = threadIdx.x;
+    if (t < 128) {
+        const uint4 v = *reinterpret_cast<const uint4*>(codes + (row0 + t) * (cols / 4) + kt * 16);
+        *reinterpret_cast<uint4*>(out + t * 16) = v;
+    } else {
+        const int r = (t - 128) * 4;  // four rows' scale pairs per piece
+        uint32_t v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[j] = *reinterpret_cast<const uint32_t*>(scales + (row0 + r + j) * (cols / 32) + kt * 2);
+        *reinterpret_cast<uint4*>(out + 2048 + r * 4) = make_uint4(v[0], v[1], v[2], v[3]);
+    }
+}
+
 int grid_for(int64_t threads, int block) {
     const int64_t blocks = (threads + block - 1) / block;
     const int64_t cap = 152 * 16;  // a few waves of resident blocks; the kernels stride beyond this
@@ -128,18 +182,27 @@ int grid_for(int64_t threads, int block) {
 }  // namespace
 
 cudaError_t launch_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales,
-                               cudaStream_t s) {
+                               uint8_t* slices, cudaStream_t s) {
     const int64_t n8 = rows * (int64_t)cols / 8;
     if (n8 == 0) return cudaSuccess;
-    quantize_q8_kernel<<<grid_for(n8, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(x), n8,
-                                                        reinterpret_cast<uint2*>(codes), scales);
+    quantize_q8_kernel<<<grid_for(n8, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(x), n8, cols,
+                                                        reinterpret_cast<uint2*>(codes), scales, slices);
     return cudaGetLastError();
 }
 
-cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, cudaStream_t s) {
+cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint8_t* slices,
+                                  cudaStream_t s) {
     const int64_t total = n * (int64_t)(F / 8);
     if (total == 0) return cudaSuccess;
-    swiglu_requant_kernel<<<grid_for(total, 256), 256, 0, s>>>(gu, n, F, reinterpret_cast<uint2*>(hc), hs);
+    swiglu_requant_kernel<<<grid_for(total, 256), 256, 0, s>>>(gu, n, F, reinterpret_cast<uint2*>(hc), hs, slices);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, uint8_t* packed,
+                           cudaStream_t s) {
+    const int64_t blocks = (int64_t)E * (rows / 128) * (cols / 64);
+    if (blocks == 0) return cudaSuccess;
+    pack_q2_kernel<<<(unsigned)blocks, 160, 0, s>>>(codes, scales, rows, cols, packed);
     return cudaGetLastError();
 }
 

@@ -24,9 +24,9 @@
 // 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB: weights are the M operand so that a
 // small expert wastes little).  Warp roles (three warpgroups, registers rebalanced with setmaxnreg):
 //   warpgroup 0   warp 0: tensor-memory allocation and, on one lane, the MMAs of each slice;
-//                 warps 1-3: producers -- each slice's 2-bit weight codes (one TMA tile load), int8 rows (TMA
-//                 tile::gather4 loads through src, four rows each) and scales (cp.async) into a ring of up to 16
-//                 slices in shared memory;
+//                 warps 1-3: producers -- each slice's packed weight block (codes and scales: one 2560-byte bulk
+//                 copy) and the tile's q8 rows in slice form (codes and scales, 80 bytes a row: TMA tile::gather4
+//                 loads through src, four rows each) into a ring of up to 16 slices in shared memory;
 //   warpgroups 1-2  converters: decode a ring slice into the fp16 operand tiles of one of two stages (K-major,
 //                 128-byte swizzle), 16 K values of one row per work item, then add the previous partial from tensor
 //                 memory into their registers; at the end they write the fp32 rows.
@@ -65,26 +65,21 @@ constexpr int kSmemBytes = 1024 + kStages * kStage + kRingBytes + 1024 + 512;
 constexpr int kRegsWg0 = 56;
 constexpr int kRegsConv = 224;
 
-// Raw slice layout in the ring (one 64-wide K slice of the tile): weight codes [128][16 B], weight scales [128][4 B],
-// activation codes [N][64 B], activation scales [N][4 B].  TMA destinations are 128-byte aligned.
-__host__ __device__ constexpr int raw_slice_bytes(int N) { return (2048 + 512 + N * 68 + 127) & ~127; }
+// Raw slice layout in the ring (one 64-wide K slice of the tile): the packed weight block (codes [128][16 B], scales
+// [128][4 B]), then the tile's rows in slice form (80 B a row: 64 codes, 2 scales, padding), four rows per gather4
+// load placed at a 384-byte stride so that every TMA destination is 128-byte aligned.
+constexpr int kWBlock = 2560;
+constexpr int kRowPiece = 80;
+constexpr int kGroupStride = 384;  // 4 rows x 80 bytes, rounded up to 128
+__host__ __device__ constexpr int raw_slice_bytes(int N) { return kWBlock + (N / 4) * kGroupStride; }
 
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+// bulk copy (no tensor map) of `bytes` (a multiple of 16) into shared memory, completing on `bar`
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
-// arrive on `bar` once every cp.async this thread issued so far has landed (the arrival counts toward the phase)
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-// TMA: a 2D tile (x bytes along the row, y rows) into shared memory, completing `bytes` on `bar`
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
 }
 // TMA: four rows (y0..y3) of a one-row-high box, placed one after another in shared memory
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
@@ -153,8 +148,7 @@ __device__ __forceinline__ void zero_activations16(uint4* hi_line, uint4* lo_lin
 }
 
 struct GemmMaps {
-    CUtensorMap w;  // weight codes: [E * a_rows rows][K/4 bytes], box 16 bytes x 128 rows
-    CUtensorMap b;  // int8 rows:    [rows][K bytes], box 64 bytes x 1 row (gather4)
+    CUtensorMap b;  // q8 rows in slice form: [rows][K/64 * 80 bytes], box 80 bytes x 1 row (gather4)
 };
 
 __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const ExpertsGemmArgs p,
@@ -186,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
 
     const int sbytes = raw_slice_bytes(N);
     const int depth = min(kMaxRing, kRingBytes / sbytes);
-    const int o_as = 2048, o_bc = 2560, o_bs = 2560 + N * 64;
+    const int o_as = 2048, o_b = kWBlock;  // weight scales, row pieces
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -199,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             mbar_init(&pempty[b], kConverters);
         }
         for (int r = 0; r < kMaxRing; ++r) {
-            mbar_init(&rfull[r], kProducers + 1);  // cp.async arrivals + the TMA byte count's arrival
+            mbar_init(&rfull[r], 1);  // the arrival that posts the slice's byte count
             mbar_init(&rempty[r], kConverters);
         }
         mbar_init(accf, 1);
@@ -253,10 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         } else {
             // ------------------------------------------------------------------ producers (96 threads)
             const int pt = threadIdx.x - 32;
-            const int64_t wrow0 = (int64_t)e * p.a_rows + m0;
-            const uint16_t* ws = p.ws + wrow0 * (p.K / 32);
+            const uint8_t* wblocks = p.wp + ((int64_t)e * (p.a_rows / kBM) + blockIdx.x) * nk * (int64_t)kWBlock;
             const int groups = (rows + 3) >> 2;  // gather4 loads of this tile's rows
-            const uint32_t tx_bytes = 2048u + (uint32_t)groups * 256u;
+            const uint32_t tx_bytes = (uint32_t)kWBlock + (uint32_t)groups * 4u * kRowPiece;
             for (int kt = 0; kt < nk; ++kt) {
                 const int r = kt % depth;
                 if (kt >= depth && !mbar_wait(&rempty[r], (uint32_t)(kt / depth - 1) & 1u, abort_flag)) {
@@ -266,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 const uint32_t slot = smem_u32(ring) + (uint32_t)(r * sbytes);
                 if (pt == 0) {
                     mbar_arrive_expect_tx(&rfull[r], tx_bytes);
-                    tma_load_2d(slot, &maps.w, kt * 16, (int)wrow0, &rfull[r]);
+                    bulk_load(slot, wblocks + (int64_t)kt * kWBlock, kWBlock, &rfull[r]);
                 }
                 for (int g = pt; g < groups; g += kProducers) {
                     const int r0 = 4 * g;
@@ -274,15 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     const int y1 = r0 + 1 < rows ? srcs[r0 + 1] : y0;
                     const int y2 = r0 + 2 < rows ? srcs[r0 + 2] : y0;
                     const int y3 = r0 + 3 < rows ? srcs[r0 + 3] : y0;
-                    tma_gather4(slot + o_bc + r0 * 64, &maps.b, kt * kBK, y0, y1, y2, y3, &rfull[r]);
+                    tma_gather4(slot + o_b + g * kGroupStride, &maps.b, kt * kRowPiece, y0, y1, y2, y3, &rfull[r]);
                 }
-                for (int row = pt; row < 128; row += kProducers)
-                    cp_async_4(slot + o_as + row * 4, ws + (int64_t)row * (p.K / 32) + kt * 2);
-                for (int row = pt; row < rows; row += kProducers)
-                    cp_async_4(slot + o_bs + row * 4, p.bs + (int64_t)srcs[row] * (p.K / 32) + kt * 2);
-                cp_async_arrive(&rfull[r]);
             }
-            cp_async_wait_all();  // no copy may land after the CTA has moved on
         }
     } else {
         setmaxnreg_inc<kRegsConv>();
@@ -349,8 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             for (int i = 0; i < 4; ++i) {
                 const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
                 if (i < nb && row < rows) {
-                    bcode[i] = *reinterpret_cast<const uint4*>(slot + o_bc + row * 64 + qu * 16);
-                    bscale[i] = *reinterpret_cast<const uint16_t*>(slot + o_bs + row * 4 + (qu >> 1) * 2);
+                    const uint8_t* piece = slot + o_b + (row >> 2) * kGroupStride + (row & 3) * kRowPiece;
+                    bcode[i] = *reinterpret_cast<const uint4*>(piece + qu * 16);
+                    bscale[i] = *reinterpret_cast<const uint16_t*>(piece + 64 + (qu >> 1) * 2);
                 } else {
                     bcode[i] = make_uint4(0u, 0u, 0u, 0u);
                     bscale[i] = 0;
@@ -455,8 +443,7 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     }
     if (max_tiles <= 0) return cudaSuccess;
     GemmMaps maps;
-    if (!make_map(&maps.w, a.wc, (uint64_t)a.K / 4, (uint64_t)a.n_experts * a.a_rows, 16, kBM) ||
-        !make_map(&maps.b, a.bc, (uint64_t)a.K, (uint64_t)a.b_rows, kBK, 1))
+    if (!make_map(&maps.b, a.bsl, (uint64_t)(a.K / kBK) * kRowPiece, (uint64_t)a.b_rows, kRowPiece, 1))
         return cudaErrorInvalidValue;
     const dim3 grid((unsigned)(a.a_rows / kBM), (unsigned)max_tiles);
     experts_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, maps);

@@ -92,12 +92,30 @@ smoe_status smoe_group(const int32_t* ids, int64_t T, int K, int E, int32_t* cou
                                             reinterpret_cast<int32_t*>(work), (cudaStream_t)stream));
 }
 
-smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales, void* stream) {
+smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales,
+                             uint8_t* slices, void* stream) {
     if (rows < 0 || cols < 32 || cols % 32 != 0) return SMOE_ERR_ARG;
+    if (slices != nullptr && cols % 64 != 0) return SMOE_ERR_ARG;
     if (rows == 0) return SMOE_OK;
     if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return SMOE_ERR_ARG;
+    if (slices != nullptr && !aligned16(slices)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    return launch_status(smoe::launch_quantize_q8(x, rows, cols, codes, scales, (cudaStream_t)stream));
+    return launch_status(smoe::launch_quantize_q8(x, rows, cols, codes, scales, slices, (cudaStream_t)stream));
+}
+
+size_t smoe_slices_bytes(int64_t rows, int cols) { return rows <= 0 || cols <= 0 ? 0 : (size_t)rows * (cols / 64) * 80; }
+
+size_t smoe_pack_q2_bytes(int E, int rows, int cols) {
+    return E <= 0 || rows <= 0 || cols <= 0 ? 0 : (size_t)E * rows * (cols / 4 + cols / 16);
+}
+
+smoe_status smoe_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, uint8_t* packed,
+                         void* stream) {
+    if (E < 1 || rows < 128 || cols < 64 || rows % 128 != 0 || cols % 64 != 0) return SMOE_ERR_ARG;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(packed)) return SMOE_ERR_ARG;
+    if ((int64_t)E * (rows / 128) * (cols / 64) > INT32_MAX) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_pack_q2(codes, scales, E, rows, cols, packed, (cudaStream_t)stream));
 }
 
 static smoe_status check_gemm_shape(int64_t n, int E, int H, int F) {
@@ -108,38 +126,38 @@ static smoe_status check_gemm_shape(int64_t n, int E, int H, int F) {
     return SMOE_OK;
 }
 
-smoe_status smoe_experts_gateup(const int8_t* xc, const uint16_t* xs, int64_t T, const int32_t* src, int32_t* tiles,
-                                int64_t n, int E, const uint8_t* wc, const uint16_t* ws, int H, int F, float* gu,
-                                void* stream) {
+smoe_status smoe_experts_gateup(const uint8_t* xsl, int64_t T, const int32_t* src, int32_t* tiles, int64_t n, int E,
+                                const uint8_t* wgu, int H, int F, float* gu, void* stream) {
     const smoe_status st = check_gemm_shape(n, E, H, F);
     if (st != SMOE_OK) return st;
     if (n == 0) return SMOE_OK;
     if (T < 1 || T > INT32_MAX) return SMOE_ERR_ARG;
-    if (!aligned16(xc) || !aligned16(xs) || !aligned16(src) || !aligned16(tiles) || !aligned16(wc) ||
-        !aligned16(ws) || !aligned16(gu))
+    if (!aligned16(xsl) || !aligned16(src) || !aligned16(tiles) || !aligned16(wgu) || !aligned16(gu))
         return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{xc, xs, src, tiles, wc, ws, 2 * F, H, gu, T, E};
+    smoe::ExpertsGemmArgs a{xsl, src, tiles, wgu, 2 * F, H, gu, T, E};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 
-smoe_status smoe_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, void* stream) {
+smoe_status smoe_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint8_t* slices,
+                                void* stream) {
     if (n < 0 || F < 32 || F % 32 != 0) return SMOE_ERR_ARG;
+    if (slices != nullptr && F % 64 != 0) return SMOE_ERR_ARG;
     if (n == 0) return SMOE_OK;
     if (!aligned16(gu) || !aligned16(hc) || !aligned16(hs)) return SMOE_ERR_ARG;
+    if (slices != nullptr && !aligned16(slices)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    return launch_status(smoe::launch_swiglu_requant(gu, n, F, hc, hs, (cudaStream_t)stream));
+    return launch_status(smoe::launch_swiglu_requant(gu, n, F, hc, hs, slices, (cudaStream_t)stream));
 }
 
-smoe_status smoe_experts_down(const int8_t* hc, const uint16_t* hs, int32_t* tiles, int64_t n, int E,
-                              const uint8_t* wc, const uint16_t* ws, int H, int F, float* dm, void* stream) {
+smoe_status smoe_experts_down(const uint8_t* hsl, int32_t* tiles, int64_t n, int E, const uint8_t* wd, int H, int F,
+                              float* dm, void* stream) {
     const smoe_status st = check_gemm_shape(n, E, H, F);
     if (st != SMOE_OK) return st;
     if (n == 0) return SMOE_OK;
-    if (!aligned16(hc) || !aligned16(hs) || !aligned16(tiles) || !aligned16(wc) || !aligned16(ws) || !aligned16(dm))
-        return SMOE_ERR_ARG;
+    if (!aligned16(hsl) || !aligned16(tiles) || !aligned16(wd) || !aligned16(dm)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{hc, hs, nullptr, tiles, wc, ws, H, F, dm, n, E};
+    smoe::ExpertsGemmArgs a{hsl, nullptr, tiles, wd, H, F, dm, n, E};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 

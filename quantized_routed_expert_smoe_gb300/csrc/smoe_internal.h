@@ -14,8 +14,11 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int K, int3
 cudaError_t launch_group(const int32_t* ids, int64_t n, int K, int E, int32_t* counts, int32_t* offsets,
                          int32_t* src, int32_t* slot, int32_t* tiles, int32_t* hist, cudaStream_t s);
 cudaError_t launch_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales,
-                               cudaStream_t s);
-cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, cudaStream_t s);
+                               uint8_t* slices, cudaStream_t s);
+cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint8_t* slices,
+                                  cudaStream_t s);
+cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, uint8_t* packed,
+                           cudaStream_t s);
 cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
                            cudaStream_t s);
 
@@ -23,12 +26,10 @@ cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w,
 // slice of the expert's weight matrix, OUT[row][j] = sum over K of W[e][j] . B[row], W the 2-bit weights and B the
 // q8 rows (gathered through `src` when it is not null).
 struct ExpertsGemmArgs {
-    const int8_t* bc;     // q8 codes of the B rows, [*][K]
-    const uint16_t* bs;   // q8 scales of the B rows, [*][K/32]
+    const uint8_t* bsl;   // q8 B rows in slice form, [*][K/64][80 bytes]
     const int32_t* src;   // B row of routed row r = src[r] (gate/up), or null: B row = r (down)
     int32_t* tiles;       // tile list; header[3] receives SMOE_ERR_TIMEOUT
-    const uint8_t* wc;    // weight codes [E][a_rows][K/4]
-    const uint16_t* ws;   // weight scales [E][a_rows][K/32]
+    const uint8_t* wp;    // packed weights: per (expert, 128-row tile, 64-value slice) 2560 bytes
     int a_rows;           // weight rows per expert (2F or H)
     int K;                // contraction length (H or F)
     float* out;           // [n][a_rows]

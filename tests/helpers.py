@@ -17,3 +17,27 @@ def deq_a(codes, scales):
 
 def i16(a):
     return np.ascontiguousarray(a).view(np.int16)
+
+
+def to_slices(codes, scales):
+    """q8 rows in the expert products' slice form: per row and per 64 values, the 64 codes, the two fp16 scales of
+    the slice's 32-value blocks (little-endian), 12 zero bytes -> uint8 [rows][cols/64][80]."""
+    rows, cols = codes.shape
+    out = np.zeros((rows, cols // 64, 80), np.uint8)
+    out[:, :, :64] = np.ascontiguousarray(codes).view(np.uint8).reshape(rows, cols // 64, 64)
+    out[:, :, 64:68] = np.ascontiguousarray(scales).view(np.uint8).reshape(rows, cols // 64, 4)
+    return out
+
+
+def packed_q2(codes, scales):
+    """Row-major Q2 matrices [E][rows][cols/4] + [E][rows][cols/32] -> the packed block sequence (uint8)."""
+    E, rows, c4 = codes.shape
+    cols = c4 * 4
+    sc = np.ascontiguousarray(scales).view(np.uint8).reshape(E, rows, cols // 16)
+    blocks = []
+    for e in range(E):
+        for mt in range(rows // 128):
+            for kt in range(cols // 64):
+                blocks.append(codes[e, mt * 128:(mt + 1) * 128, kt * 16:(kt + 1) * 16].ravel())
+                blocks.append(sc[e, mt * 128:(mt + 1) * 128, kt * 4:(kt + 1) * 4].ravel())
+    return np.concatenate(blocks)

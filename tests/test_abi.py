@@ -47,6 +47,8 @@ def test_sizing_helpers(lib):
     assert binding.max_tiles(0, 16) == 0
     assert binding.tiles_bytes(128, 16) == 16 * 18
     assert binding.group_work_bytes(81920, 512) >= 512 * 4
+    assert binding.slices_bytes(3, 256) == 3 * 4 * 80
+    assert binding.pack_q2_bytes(2, 128, 64) == 2 * 128 * (16 + 4)
 
 
 def test_host_side_rejections_need_no_gpu(lib):
@@ -61,10 +63,12 @@ def test_host_side_rejections_need_no_gpu(lib):
     assert lib.smoe_route_topk(odd, 4, 16, 2, fake, fake, null) == ARG
     assert lib.smoe_route_topk(fake, 0, 16, 2, fake, fake, null) == 0  # empty chunk: nothing to do
     # q8: cols not a multiple of 32
-    assert lib.smoe_quantize_q8(fake, 4, 48, fake, fake, null) == ARG
+    assert lib.smoe_quantize_q8(fake, 4, 48, fake, fake, null, null) == ARG
+    assert lib.smoe_quantize_q8(fake, 4, 96, fake, fake, fake, null) == ARG  # slice form needs cols % 64 == 0
     # gemm shapes the kernels do not cover
-    assert lib.smoe_experts_gateup(fake, fake, 5, fake, fake, 10, 4, fake, fake, 96, 64, fake, null) == UNSUP
-    assert lib.smoe_experts_down(fake, fake, fake, 10, 4, fake, fake, 256, 48, fake, null) == UNSUP
+    assert lib.smoe_experts_gateup(fake, 5, fake, fake, 10, 4, fake, 96, 64, fake, null) == UNSUP
+    assert lib.smoe_experts_down(fake, fake, 10, 4, fake, 256, 48, fake, null) == UNSUP
+    assert lib.smoe_pack_q2(fake, fake, 2, 100, 64, fake, null) == ARG  # rows % 128
     # group: tiles buffer too small
     assert lib.smoe_group(fake, 8, 2, 4, fake, fake, fake, fake, fake, 16, fake, 1 << 20, null) == ARG
     # well-formed arguments on a machine without an sm_103 device: a clean error, never a fallback

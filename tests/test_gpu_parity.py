@@ -19,7 +19,7 @@ import scipy.special
 import oracle
 from quantized_routed_expert_smoe_gb300 import synth
 
-from helpers import deq_a, deq_w, i16
+from helpers import deq_a, deq_w, i16, packed_q2, to_slices
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -155,19 +155,23 @@ def test_group_edge_cases(B):
 
 
 # ------------------------------------------------------------------------------------------------ q8
-def gpu_q8(B, x):
+def gpu_q8(B, x, with_slices=False):
     rows, cols = x.shape
     codes = torch.empty(rows, cols, dtype=torch.int8, device="cuda")
     scales = torch.empty(rows, cols // 32, dtype=torch.int16, device="cuda")
-    B.smoe_quantize_q8(dev(x), codes, scales)
+    slices = torch.full((B.slices_bytes(rows, cols),), 0xAB, dtype=torch.uint8, device="cuda") if with_slices else None
+    B.smoe_quantize_q8(dev(x), codes, scales, slices)
+    if with_slices:
+        return host(codes), host(scales).view(np.uint16), host(slices).reshape(rows, cols // 64, 80)
     return host(codes), host(scales).view(np.uint16)
 
 
 def test_quantize_bit_exact_full_and_edges(B):
     x = layer_inputs("t8192")["x"]
-    c, s = gpu_q8(B, x)
+    c, s, sl = gpu_q8(B, x, with_slices=True)
     co, so = oracle.quantize_q8(x)
     assert np.array_equal(c, co) and np.array_equal(s, so)
+    assert np.array_equal(sl, to_slices(co, so))
     # edge blocks: zeros, exact .5 ties at d = 1, subnormal and zero-rounding scales, clamping, huge values
     rng = np.random.default_rng(1)
     e = rng.standard_normal((9, 64)).astype(np.float32)
@@ -193,33 +197,43 @@ def test_quantize_bit_exact_full_and_edges(B):
 
 
 # ------------------------------------------------------------------------------------------------ expert products
+def _tiles_dev(B, g, n, E):
+    raw = np.zeros(B.tiles_bytes(n, E) // 4, np.int32)
+    nt = g["tiles"].shape[0]
+    raw[0], raw[2] = nt, n
+    raw[4:4 + 4 * nt] = g["tiles"].ravel()
+    return dev(raw)
+
+
 def gpu_gateup(B, xc, xs, g, wgu_c, wgu_s, n, E):
-    tiles = dev(g["tiles_raw"]) if "tiles_raw" in g else None
-    if tiles is None:
-        raw = np.zeros(B.tiles_bytes(n, E) // 4, np.int32)
-        nt = g["tiles"].shape[0]
-        raw[0], raw[2] = nt, n
-        raw[4:4 + 4 * nt] = g["tiles"].ravel()
-        tiles = dev(raw)
+    """gate/up through the C ABI: the oracle's q8 rows laid out in slice form, the weights packed by the library."""
+    tiles = _tiles_dev(B, g, n, E)
+    T, H = xc.shape
     F = wgu_c.shape[1] // 2
     gu = torch.full((n, 2 * F), float("nan"), dtype=torch.float32, device="cuda")
-    B.smoe_experts_gateup(dev(xc), dev(i16(xs)), dev(g["src"]), tiles, n, dev(wgu_c), dev(i16(wgu_s)), gu)
+    wp = B.pack_weights(wgu_c, wgu_s)
+    B.smoe_experts_gateup(dev(to_slices(xc, xs)), T, dev(g["src"]), tiles, n, E, wp, H, F, gu)
     t = host(tiles)
     assert t[3] == 0, "kernel reported a timeout"
     return gu
 
 
 def gpu_down(B, hc, hs, g, wd_c, wd_s, n, E):
-    raw = np.zeros(B.tiles_bytes(n, E) // 4, np.int32)
-    nt = g["tiles"].shape[0]
-    raw[0], raw[2] = nt, n
-    raw[4:4 + 4 * nt] = g["tiles"].ravel()
-    tiles = dev(raw)
+    tiles = _tiles_dev(B, g, n, E)
     H = wd_c.shape[1]
+    F = hc.shape[1]
     dm = torch.full((n, H), float("nan"), dtype=torch.float32, device="cuda")
-    B.smoe_experts_down(dev(hc), dev(i16(hs)), tiles, n, dev(wd_c), dev(i16(wd_s)), dm)
+    wp = B.pack_weights(wd_c, wd_s)
+    B.smoe_experts_down(dev(to_slices(hc, hs)), tiles, n, E, wp, H, F, dm)
     assert host(tiles)[3] == 0
     return dm
+
+
+def test_pack_q2_layout(B):
+    inp = synth.make_custom(T=4, H=256, E=3, K=1, F=128, seed=17)
+    for c, s in ((inp["wgu_c"], inp["wgu_s"]), (inp["wd_c"], inp["wd_s"])):
+        got = host(B.pack_weights(c, s))
+        assert np.array_equal(got, packed_q2(c, s))
 
 
 def rows_of(t, rows):
@@ -343,8 +357,10 @@ def test_swiglu_requant_parity(B):
     gu = synth.make_gu(n, F, seed=11, scale=2.0)
     hc = torch.empty(n, F, dtype=torch.int8, device="cuda")
     hs = torch.empty(n, F // 32, dtype=torch.int16, device="cuda")
-    B.smoe_swiglu_requant(dev(gu), hc, hs)
+    hsl = torch.full((B.slices_bytes(n, F),), 0xAB, dtype=torch.uint8, device="cuda")
+    B.smoe_swiglu_requant(dev(gu), hc, hs, hsl)
     c, s = host(hc), host(hs).view(np.uint16)
+    assert np.array_equal(host(hsl).reshape(n, F // 64, 80), to_slices(c, s))
     co, so = oracle.swiglu_requant(gu, F)
     g = gu[:, :F].astype(np.float64)
     u = gu[:, F:].astype(np.float64)
