@@ -15,10 +15,11 @@
 // sum of the exact products d_w (q_w - 2) d_a q_a.  The K loop runs two MMAs per 16-wide K step (A x B_hi,
 // A x B_lo).  The tensor core's fp32 accumulation aligns its addends with truncation, which over the 2 * K / 16 steps
 // of a whole row costs about 3e-6 of the result -- enough to flip requantised H codes -- so the accumulation is
-// two-level: each 64-wide K slice (kPromote slices) accumulates from zero into one of two tensor-memory buffers (the
-// partial is small, so its truncation error is too), and the converter warps add each finished partial into fp32
-// registers with round-to-nearest while the tensor core fills the other buffer.  One slice per partial keeps the
-// requantised H of the smallest test chunk identical to the oracle's; two slices flipped one H scale there.
+// two-level for gate/up (whose output is requantised): each 64-wide K slice accumulates from zero into one of two
+// tensor-memory buffers (the partial is small, so its truncation error is too), and the converter warps add each
+// finished partial into fp32 registers with round-to-nearest while the tensor core fills the other buffer.  One slice per partial keeps the
+// requantised H of the smallest test chunk identical to the oracle's; two slices flipped one H scale there.  The down
+// product feeds the fp32 combine only, so it accumulates the whole K in one buffer.
 //
 // Tile: one CTA = one tile of the tile list (an expert and up to 256 of its routed rows, the MMA's N, a multiple of
 // 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB: weights are the M operand so that a
@@ -57,7 +58,6 @@ constexpr int kStage = kATile + 2 * kBTile;
 constexpr int kRingBytes = 64 * 1024;          // raw-data ring
 constexpr int kMaxRing = 16;                   // slices in flight at most
 constexpr uint32_t kTmemCols = 512;            // two fp32 partial buffers, 128 lanes x N <= 256 columns each
-constexpr int kPromote = 1;                    // slices per tensor-memory partial
 // shared memory: [1 KB alignment slack][stages][ring][src rows 1 KB][barriers]
 constexpr int kSmemBytes = 1024 + kStages * kStage + kRingBytes + 1024 + 512;
 // registers: launched at 168 a thread (384 x 168 = 64,512 of 65,536); warpgroup 0 gives back to 56 and the two
@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const int N = (rows + 15) & ~15;
     const int m0 = blockIdx.x * kBM;
     const int nk = p.K / kBK;
+    const int P = p.two_level ? 1 : nk;  // slices per tensor-memory partial
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -221,9 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             if (lane == 0) {
                 const uint32_t idesc = idesc_f16_f32(kBM, N);
                 for (int kt = 0; kt < nk; ++kt) {
-                    // slices kt of partial g = kt / kPromote go to buffer g & 1, which partial g - 2 has left
-                    const int s = kt % kStages, g = kt / kPromote, b = g & 1;
-                    const bool first = kt % kPromote == 0, last = kt % kPromote == kPromote - 1 || kt == nk - 1;
+                    // slices kt of partial g = kt / P go to buffer g & 1, which partial g - 2 has left
+                    const int s = kt % kStages, g = kt / P, b = g & 1;
+                    const bool first = kt % P == 0, last = kt % P == P - 1 || kt == nk - 1;
                     if (!mbar_wait(&full[s], (uint32_t)(kt / kStages) & 1u, abort_flag) ||
                         (first && g >= 2 && !mbar_wait(&pempty[b], (uint32_t)(g / 2 - 1) & 1u, abort_flag))) {
                         ok = false;
@@ -370,9 +371,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             fence_async_smem();
             mbar_arrive(&full[s]);
             // after the first slice of partial g has been handed over, add partial g - 1
-            if (kt % kPromote == 0 && kt >= kPromote && !promote(kt / kPromote - 1)) ok = false;
+            if (kt % P == 0 && kt >= P && !promote(kt / P - 1)) ok = false;
         }
-        if (ok && !promote((nk - 1) / kPromote)) ok = false;
+        if (ok && !promote((nk - 1) / P)) ok = false;
         if (ok) {
             // ------------------------------------------------------------------ epilogue: fp32 rows out
             float* outcol = p.out + (m0 + mrow);

@@ -135,7 +135,7 @@ smoe_status smoe_experts_gateup(const uint8_t* xsl, int64_t T, const int32_t* sr
     if (!aligned16(xsl) || !aligned16(src) || !aligned16(tiles) || !aligned16(wgu) || !aligned16(gu))
         return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{xsl, src, tiles, wgu, 2 * F, H, gu, T, E};
+    smoe::ExpertsGemmArgs a{xsl, src, tiles, wgu, 2 * F, H, gu, T, E, true};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 
@@ -157,7 +157,7 @@ smoe_status smoe_experts_down(const uint8_t* hsl, int32_t* tiles, int64_t n, int
     if (n == 0) return SMOE_OK;
     if (!aligned16(hsl) || !aligned16(tiles) || !aligned16(wd) || !aligned16(dm)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{hsl, nullptr, tiles, wd, H, F, dm, n, E};
+    smoe::ExpertsGemmArgs a{hsl, nullptr, tiles, wd, H, F, dm, n, E, false};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 

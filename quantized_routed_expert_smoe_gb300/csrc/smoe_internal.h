@@ -35,6 +35,7 @@ struct ExpertsGemmArgs {
     float* out;           // [n][a_rows]
     int64_t b_rows;       // rows of the q8 B matrix (T for gate/up, n for down)
     int n_experts;        // E
+    bool two_level;       // promote every 64-wide K slice into fp32 registers (gate/up); else one accumulator
 };
 cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s);
 
