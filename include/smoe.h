@@ -1,14 +1,15 @@
 /* smoe.h -- C ABI of libsmoe: the prompt-chunk (prefill) routed-expert block of a mixture-of-experts layer on one
  * GB300 (sm_103a).
  *
- * The block, for a chunk of T tokens of hidden size H, E experts, top-K routing and expert FFN width F, runs as seven
- * calls in this order (each the step of the same name in the Strata engine's prompt path -- page
+ * The block, for a chunk of T tokens of hidden size H, E experts, top-K routing and expert FFN width F, runs as these
+ * eight calls in this order (each the step of the same name in the Strata engine's prompt path -- page
  * "src/prefill/prefill.cpp", Prefill::run, MoE half -- and its fused int8 expert contract -- page "Strata compare
  * v0.1.35...v0.1.37", include/strata/prefill/moe_fused.hpp):
  *
  *   smoe_route_topk      router softmax, top-K of the E logits, weights renormalised over the K
  *   smoe_group           stable counting sort of the T*K (token, k) pairs by expert: counts, offsets, src, slot, tiles
  *   smoe_quantize_q8     activations to int8 once per token, one fp16 scale per 32 values
+ *   smoe_gather_slices   the q8 rows of the routed pairs in routed-row order
  *   smoe_experts_gateup  grouped gate/up product of each routed row against its expert's 2-bit weights
  *   smoe_swiglu_requant  h = silu(gate) * up, requantised to int8 per 32 values
  *   smoe_experts_down    grouped down product into one fp32 row per routed pair
@@ -137,17 +138,27 @@ smoe_status smoe_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, in
                          void* stream);
 size_t smoe_pack_q2_bytes(int E, int rows, int cols);
 
-/* Step 4 -- grouped gate/up.  moe_fused.hpp experts(): gate/up from the per-token int8 activations through the rows
- * `src` of group; per routed row r of expert e and output j in [0, 2F):
- *   GU[r][j] = sum_b dW[e][j][b] * dX[src r][b] * sum_{i in block b} (qW - 2) * qX     (fp32 result)
- *   xsl      q8 activations of the chunk in slice form ([T][H/64][80], from smoe_quantize_q8); T >= 1, every src
- *            entry is < T.
- *   src, tiles  from smoe_group (tiles header[3] receives SMOE_ERR_TIMEOUT).   n = T*K (sizes the launch).
+/* Step 4a -- routed rows of the q8 activations.  moe_fused.hpp experts() reads each routed row's activations
+ * "through the rows of group": this call lays them out once in routed-row order, so that every tile of the expert
+ * products reads its rows as one contiguous block.
+ *   slices   q8 rows in slice form, [in_rows][cols/64][80] (from smoe_quantize_q8).
+ *   src      int32 [n], from smoe_group; every entry in [0, in_rows) (an entry outside it is not read: its output row
+ *            is zero-filled and the call still returns SMOE_OK, which a bad grouping has already reported).
+ *   out      [n][cols/64][80] out: out row r = slices row src[r], byte for byte.   cols % 64 == 0. */
+smoe_status smoe_gather_slices(const uint8_t* slices, int64_t in_rows, int cols, const int32_t* src, int64_t n,
+                               uint8_t* out, void* stream);
+
+/* Step 4b -- grouped gate/up.  moe_fused.hpp experts(): gate/up of the routed rows; per routed row r of expert e and
+ * output j in [0, 2F):
+ *   GU[r][j] = sum_b dW[e][j][b] * dX[r][b] * sum_{i in block b} (qW - 2) * qX     (fp32 result)
+ *   xsl      q8 activations of the n routed rows in slice form, routed-row order ([n][H/64][80], from
+ *            smoe_gather_slices).
+ *   tiles    from smoe_group (header[3] receives SMOE_ERR_TIMEOUT).   n = T*K (sizes the launch).
  *   wgu      gate/up weights [E][2F][H] packed by smoe_pack_q2.
  *   gu       fp32 [n][2F] out, row r = routed row r.
  *   H % 128 == 0, F % 64 == 0. */
-smoe_status smoe_experts_gateup(const uint8_t* xsl, int64_t T, const int32_t* src, int32_t* tiles, int64_t n, int E,
-                                const uint8_t* wgu, int H, int F, float* gu, void* stream);
+smoe_status smoe_experts_gateup(const uint8_t* xsl, int32_t* tiles, int64_t n, int E, const uint8_t* wgu, int H, int F,
+                                float* gu, void* stream);
 
 /* Step 5 -- SwiGLU and requantisation.  Page "src/prefill/prefill.cpp": mmq::swiglu(GU, H, rows, ...) then the
  * int8 rounding of H; moe_fused.hpp: "SwiGLU, H as int8".

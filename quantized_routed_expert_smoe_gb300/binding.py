@@ -1,10 +1,10 @@
-"""Thin Python binding of libsmoe's C ABI (include/smoe.h): the same seven calls, argument marshalling only.
+"""Thin Python binding of libsmoe's C ABI (include/smoe.h): the calls of include/smoe.h, argument marshalling only.
 
 Every step runs in the CUDA kernels of libsmoe.so; this module checks tensor types and shapes, passes raw device
 pointers and the current CUDA stream, and raises SmoeError on a non-OK status.  There is no fallback: when the
 library is missing or the device is not an sm_103 part, the calls raise.
 
-``SmoeBlock`` holds the intermediate buffers of one chunk size (allocated once with PyTorch) and runs the seven
+``SmoeBlock`` holds the intermediate buffers of one chunk size (allocated once with PyTorch) and runs the eight
 calls in order; it is what the tests and the benchmark drive.
 """
 from __future__ import annotations
@@ -52,9 +52,10 @@ _SIGS = {
     "smoe_pack_q2": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                       ctypes.c_void_p], ctypes.c_int),
     "smoe_pack_q2_bytes": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
-    "smoe_experts_gateup": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
-                             ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
-                             ctypes.c_void_p], ctypes.c_int),
+    "smoe_gather_slices": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
+                            ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_experts_gateup": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                             ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_swiglu_requant": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                              ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_experts_down": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
@@ -142,7 +143,7 @@ def _opt(t, dtype, name):
     return ctypes.c_void_p(0) if t is None else _dev(t, dtype, name)
 
 
-# ------------------------------------------------------------------------------------------------ the seven calls
+# ------------------------------------------------------------------------------------------------ the calls
 def smoe_route_topk(logits, ids, w, stream=None):
     T, E = logits.shape
     K = ids.shape[1]
@@ -184,10 +185,17 @@ def smoe_pack_q2(codes, scales, packed, stream=None):
         _dev(packed, torch.uint8, "packed"), _stream(stream)))
 
 
-def smoe_experts_gateup(xsl, T, src, tiles, n, E, wgu, H, F, gu, stream=None):
+def smoe_gather_slices(slices, in_rows, cols, src, out, stream=None):
+    """out row r = slices row src[r] (q8 rows in slice form, cols values a row); n = src.numel()."""
+    _check("smoe_gather_slices", load_library().smoe_gather_slices(
+        _dev(slices, torch.uint8, "slices"), in_rows, cols, _dev(src, torch.int32, "src"), src.numel(),
+        _dev(out, torch.uint8, "out"), _stream(stream)))
+
+
+def smoe_experts_gateup(xsl, tiles, n, E, wgu, H, F, gu, stream=None):
     _check("smoe_experts_gateup", load_library().smoe_experts_gateup(
-        _dev(xsl, torch.uint8, "xsl"), T, _dev(src, torch.int32, "src"), _dev(tiles, torch.int32, "tiles"), n, E,
-        _dev(wgu, torch.uint8, "wgu"), H, F, _dev(gu, torch.float32, "gu"), _stream(stream)))
+        _dev(xsl, torch.uint8, "xsl"), _dev(tiles, torch.int32, "tiles"), n, E, _dev(wgu, torch.uint8, "wgu"), H, F,
+        _dev(gu, torch.float32, "gu"), _stream(stream)))
 
 
 def smoe_swiglu_requant(gu, hc, hs, slices=None, stream=None):
@@ -214,7 +222,7 @@ def smoe_combine(dm, slot, w, y, stream=None):
 # ------------------------------------------------------------------------------------------------ one block
 class SmoeBlock:
     """The routed-expert block for chunks of up to T tokens: weights resident on the device, every intermediate
-    buffer allocated once.  run(logits, x) issues the seven calls on the current stream and returns y [T][H]."""
+    buffer allocated once.  run(logits, x) issues the eight calls on the current stream and returns y [T][H]."""
 
     def __init__(self, T: int, H: int, E: int, K: int, F: int, wgu_c, wgu_s, wd_c, wd_s, device="cuda"):
         load_library()
@@ -239,6 +247,7 @@ class SmoeBlock:
         self.xc = e(T, H, dt=torch.int8)
         self.xs = e(T, H // 32, dt=torch.int16)
         self.xsl = e(max(slices_bytes(T, H), 16), dt=torch.uint8)
+        self.xslr = e(max(slices_bytes(n, H), 16), dt=torch.uint8)  # routed-row order
         self.gu = e(n, 2 * F, dt=torch.float32)
         self.hc = e(n, F, dt=torch.int8)
         self.hs = e(n, F // 32, dt=torch.int16)
@@ -251,8 +260,8 @@ class SmoeBlock:
         smoe_group(self.ids, self.E, self.counts, self.offsets, self.src[:self.n], self.slot[:self.n], self.tiles,
                    self.work, stream)
         smoe_quantize_q8(x, self.xc, self.xs, self.xsl, stream)
-        smoe_experts_gateup(self.xsl, self.T, self.src, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.gu,
-                            stream)
+        smoe_gather_slices(self.xsl, self.T, self.H, self.src[:self.n], self.xslr, stream)
+        smoe_experts_gateup(self.xslr, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.gu, stream)
         smoe_swiglu_requant(self.gu, self.hc, self.hs, self.hsl, stream)
         smoe_experts_down(self.hsl, self.tiles, self.n, self.E, self.wd, self.H, self.F, self.dm, stream)
         smoe_combine(self.dm, self.slot, self.w, self.y, stream)

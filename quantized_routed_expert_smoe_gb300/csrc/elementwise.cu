@@ -173,6 +173,26 @@ __global__ void __launch_bounds__(160) pack_q2_kernel(const uint8_t* __restrict_
     }
 }
 
+// Routed rows of the q8 activations in slice form: out row r = in row src[r] (80-byte pieces per 64 values, so a row
+// is a whole number of 16-byte words).  One warp per output row, its lanes striding over the row's words; an src
+// entry outside [0, in_rows) gives a zero row.
+__global__ void __launch_bounds__(256) gather_slices_kernel(const uint4* __restrict__ in, int64_t in_rows,
+                                                            int words, const int32_t* __restrict__ src, int64_t n,
+                                                            uint4* __restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n; r += warps) {
+        const int32_t t = __ldg(src + r);
+        uint4* o = out + r * words;
+        if (t < 0 || t >= in_rows) {
+            for (int w = lane; w < words; w += 32) o[w] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            const uint4* i = in + (int64_t)t * words;
+            for (int w = lane; w < words; w += 32) o[w] = __ldg(i + w);
+        }
+    }
+}
+
 int grid_for(int64_t threads, int block) {
     const int64_t blocks = (threads + block - 1) / block;
     const int64_t cap = 152 * 16;  // a few waves of resident blocks; the kernels stride beyond this
@@ -203,6 +223,15 @@ cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, 
     const int64_t blocks = (int64_t)E * (rows / 128) * (cols / 64);
     if (blocks == 0) return cudaSuccess;
     pack_q2_kernel<<<(unsigned)blocks, 160, 0, s>>>(codes, scales, rows, cols, packed);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_slices(const uint8_t* slices, int64_t in_rows, int cols, const int32_t* src, int64_t n,
+                                 uint8_t* out, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    const int words = cols / 64 * 5;
+    gather_slices_kernel<<<grid_for(n * 32, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(slices), in_rows, words,
+                                                               src, n, reinterpret_cast<uint4*>(out));
     return cudaGetLastError();
 }
 

@@ -2,8 +2,8 @@
 // tensor cores (tcgen05.mma, accumulators in tensor memory), sm_103a.
 //
 // Page "Strata compare v0.1.35...v0.1.37", include/strata/prefill/moe_fused.hpp experts(): for each expert, gate/up
-// of its routed rows from the per-token int8 activations (gathered through src) against its 2-bit weights, then
-// down into one fp32 row per routed pair.  Per output:  sum_b dW[b] * dA[b] * sum_{i in b} (qW - 2) * qA.
+// of its routed rows from the per-token int8 activations against its 2-bit weights, then down into one fp32 row per
+// routed pair.  Per output:  sum_b dW[b] * dA[b] * sum_{i in b} (qW - 2) * qA.
 //
 // GB300 design.  The int8 tensor rate of this part is far below its fp16 rate, so the contraction runs as
 // tcgen05.mma.kind::f16 on EXACT fp16 re-encodings of the two quantised operands:
@@ -15,22 +15,24 @@
 // sum of the exact products d_w (q_w - 2) d_a q_a.  The K loop runs two MMAs per 16-wide K step (A x B_hi,
 // A x B_lo).  The tensor core's fp32 accumulation aligns its addends with truncation, which over the 2 * K / 16 steps
 // of a whole row costs about 3e-6 of the result -- enough to flip requantised H codes -- so the accumulation is
-// two-level for gate/up (whose output is requantised): each 64-wide K slice accumulates from zero into one of two
-// tensor-memory buffers (the partial is small, so its truncation error is too), and the converter warps add each
-// finished partial into fp32 registers with round-to-nearest while the tensor core fills the other buffer.  One slice per partial keeps the
-// requantised H of the smallest test chunk identical to the oracle's; two slices flipped one H scale there.  The down
-// product feeds the fp32 combine only, so it accumulates the whole K in one buffer.
+// two-level where it matters: for gate/up, whose output is requantised, each 64-wide K slice accumulates from zero
+// into one of two tensor-memory buffers (the partial is small, so its truncation error is too) and the promoter
+// warps add each finished partial into fp32 registers with round-to-nearest while the tensor core fills the other
+// buffer (one slice per partial: two flipped one H scale of the smallest test chunk).  The down product feeds the
+// fp32 combine only, where 4e-6 is far inside the output bound, so it accumulates the whole K in one buffer.
 //
-// Tile: one CTA = one tile of the tile list (an expert and up to 256 of its routed rows, the MMA's N, a multiple of
-// 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB: weights are the M operand so that a
-// small expert wastes little).  Warp roles (three warpgroups, registers rebalanced with setmaxnreg):
+// Tile: one CTA = one tile of the tile list (an expert and up to 256 of its routed rows, contiguous in routed-row
+// order; the MMA's N, a multiple of 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB:
+// weights are the M operand so that a small expert wastes little).  Five warpgroups, registers rebalanced with
+// setmaxnreg:
 //   warpgroup 0   warp 0: tensor-memory allocation and, on one lane, the MMAs of each slice;
-//                 warps 1-3: producers -- each slice's packed weight block (codes and scales: one 2560-byte bulk
-//                 copy) and the tile's q8 rows in slice form (codes and scales, 80 bytes a row: TMA tile::gather4
-//                 loads through src, four rows each) into a ring of up to 16 slices in shared memory;
-//   warpgroups 1-2  converters: decode a ring slice into the fp16 operand tiles of one of two stages (K-major,
-//                 128-byte swizzle), 16 K values of one row per work item, then add the previous partial from tensor
-//                 memory into their registers; at the end they write the fp32 rows.
+//                 warp 1, one lane: the producer -- per 64-wide K slice one bulk copy of the packed weight block
+//                 (codes and scales) and TMA tile loads of the tile's q8 rows in slice form (codes and scales, 80
+//                 bytes a row, 16 rows a load), into a ring of up to 16 slices in shared memory;
+//   warpgroups 1-2  promoters: add each finished partial from tensor memory into fp32 registers (128 columns of
+//                 one TMEM lane a thread), then write the fp32 rows;
+//   warpgroups 3-4  converters: decode a ring slice into the fp16 operand tiles of one of two stages (K-major,
+//                 128-byte swizzle), 16 K values of one row per work item.
 //
 // K order inside the operand tiles: within each group of 16 K values, shared-memory position 2m holds value m and
 // position 2m+1 holds value m+8 (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so
@@ -49,29 +51,32 @@ constexpr int kBM = 128;                       // weight rows per CTA (MMA M)
 constexpr int kBK = 64;                        // K values per slice: one 128-byte swizzle row of fp16
 constexpr int kMaxBN = SMOE_TILE_ROWS;         // routed rows per tile (MMA N <= 256)
 constexpr int kStages = 2;                     // fp16 operand stages
-constexpr int kThreads = 384;                  // three warpgroups
-constexpr int kProducers = 96;                 // warps 1-3
-constexpr int kConverters = 256;               // warpgroups 1-2
+constexpr int kThreads = 640;                  // five warpgroups
+constexpr int kPromoters = 256;                // warpgroups 1-2
+constexpr int kConverters = 256;               // warpgroups 3-4
 constexpr int kATile = kBM * 128;              // 16 KB of fp16 weights
 constexpr int kBTile = kMaxBN * 128;           // 32 KB of fp16 activations (one of hi / lo)
 constexpr int kStage = kATile + 2 * kBTile;
-constexpr int kRingBytes = 64 * 1024;          // raw-data ring
+constexpr int kRingBytes = 65 * 1024;          // raw-data ring
 constexpr int kMaxRing = 16;                   // slices in flight at most
 constexpr uint32_t kTmemCols = 512;            // two fp32 partial buffers, 128 lanes x N <= 256 columns each
-// shared memory: [1 KB alignment slack][stages][ring][src rows 1 KB][barriers]
-constexpr int kSmemBytes = 1024 + kStages * kStage + kRingBytes + 1024 + 512;
-// registers: launched at 168 a thread (384 x 168 = 64,512 of 65,536); warpgroup 0 gives back to 56 and the two
-// converter warpgroups take 224: 128 x 56 + 256 x 224 = 64,512.
-constexpr int kRegsWg0 = 56;
-constexpr int kRegsConv = 224;
+// shared memory: [1 KB alignment slack][stages][ring][barriers]
+constexpr int kSmemBytes = 1024 + kStages * kStage + kRingBytes + 512;
+// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 24, the converters to
+// 40 and the promoters take 176: 128 x 24 + 256 x 40 + 256 x 176 = 58,368 <= 61,440.  Per SM sub-partition (one
+// warp of each warpgroup): 32 x (24 + 176 + 176 + 40 + 40) = 14,592 <= 16,384.
+constexpr int kRegsWg0 = 24;
+constexpr int kRegsConv = 40;
+constexpr int kRegsProm = 176;
+static_assert(128 * kRegsWg0 + 256 * kRegsConv + 256 * kRegsProm <= 640 * 96, "register split exceeds the launch");
 
 // Raw slice layout in the ring (one 64-wide K slice of the tile): the packed weight block (codes [128][16 B], scales
-// [128][4 B]), then the tile's rows in slice form (80 B a row: 64 codes, 2 scales, padding), four rows per gather4
-// load placed at a 384-byte stride so that every TMA destination is 128-byte aligned.
+// [128][4 B]), then the tile's N rows in slice form (80 B a row: 64 codes, 2 scales, padding).  Every TMA
+// destination (the block, each 16-row box) is 128-byte aligned.
 constexpr int kWBlock = 2560;
 constexpr int kRowPiece = 80;
-constexpr int kGroupStride = 384;  // 4 rows x 80 bytes, rounded up to 128
-__host__ __device__ constexpr int raw_slice_bytes(int N) { return kWBlock + (N / 4) * kGroupStride; }
+constexpr int kRowBox = 16;                    // rows per TMA box
+__host__ __device__ constexpr int raw_slice_bytes(int N) { return kWBlock + N * kRowPiece; }
 
 // bulk copy (no tensor map) of `bytes` (a multiple of 16) into shared memory, completing on `bar`
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -81,13 +86,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
-// TMA: four rows (y0..y3) of a one-row-high box, placed one after another in shared memory
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int y0, int y1, int y2, int y3,
-                                            uint64_t* bar) {
+// TMA: a 2D tile (x bytes along the row, y the first row) into shared memory, completing its bytes on `bar`
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
-        ::"r"(dst), "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)) : "memory");
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
 }
 
 template <uint32_t N>
@@ -148,7 +151,7 @@ __device__ __forceinline__ void zero_activations16(uint4* hi_line, uint4* lo_lin
 }
 
 struct GemmMaps {
-    CUtensorMap b;  // q8 rows in slice form: [rows][K/64 * 80 bytes], box 80 bytes x 1 row (gather4)
+    CUtensorMap b;  // q8 rows in slice form: [rows][K/64 * 80 bytes], box 80 bytes x 16 rows
 };
 
 __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const ExpertsGemmArgs p,
@@ -158,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     if (ti >= tiles[0] || tiles[1] != 0) return;  // no such tile, or the grouping failed: nothing to do
     const int4 tile = reinterpret_cast<const int4*>(tiles)[1 + ti];
     const int e = tile.x, row0 = tile.y, rows = tile.z;
-    if (rows <= 0 || rows > kMaxBN) return;
+    // a tile the grouping cannot have written (a bad expert id or row range): nothing is read or written for it
+    if (rows <= 0 || rows > kMaxBN || e < 0 || e >= p.n_experts || row0 < 0 || row0 + (int64_t)rows > p.b_rows) return;
     const int N = (rows + 15) & ~15;
     const int m0 = blockIdx.x * kBM;
     const int nk = p.K / kBK;
@@ -168,11 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t* smem = smem_raw + pad;
     uint8_t* ring = smem + kStages * kStage;
-    int32_t* srcs = reinterpret_cast<int32_t*>(ring + kRingBytes);          // [256] B row of each tile row
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kRingBytes + 1024);  // operand stage s is filled
-    uint64_t* empty = full + kStages;                                         // ... and consumed by the MMAs
-    uint64_t* pfull = empty + kStages;     // a slice's partial is complete in tensor-memory buffer b
-    uint64_t* pempty = pfull + 2;          // the converters have added buffer b into their registers
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kRingBytes);  // operand stage s is filled
+    uint64_t* empty = full + kStages;      // ... and consumed by the MMAs
+    uint64_t* pfull = empty + kStages;     // a partial is complete in tensor-memory buffer b
+    uint64_t* pempty = pfull + 2;          // the promoters have added buffer b into their registers
     uint64_t* rfull = pempty + 2;          // ring slot r holds its slice [kMaxRing]
     uint64_t* rempty = rfull + kMaxRing;   // ring slot r has been read [kMaxRing]
     uint64_t* accf = rempty + kMaxRing;    // every MMA has completed
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&pfull[b], 1);
-            mbar_init(&pempty[b], kConverters);
+            mbar_init(&pempty[b], kPromoters);
         }
         for (int r = 0; r < kMaxRing; ++r) {
             mbar_init(&rfull[r], 1);  // the arrival that posts the slice's byte count
@@ -201,9 +204,6 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // the B row of every tile row (rows past the tile: -1)
-    for (int r = threadIdx.x; r < kMaxBN; r += kThreads)
-        srcs[r] = r < rows ? (p.src ? p.src[row0 + r] : row0 + r) : -1;
     if (warp == 0) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -217,163 +217,89 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
 
     if (warp < 4) {
         setmaxnreg_dec<kRegsWg0>();
-        if (warp == 0) {
+        if (warp == 0 && lane == 0) {
             // ------------------------------------------------------------------ MMA issue (one thread)
-            if (lane == 0) {
-                const uint32_t idesc = idesc_f16_f32(kBM, N);
-                for (int kt = 0; kt < nk; ++kt) {
-                    // slices kt of partial g = kt / P go to buffer g & 1, which partial g - 2 has left
-                    const int s = kt % kStages, g = kt / P, b = g & 1;
-                    const bool first = kt % P == 0, last = kt % P == P - 1 || kt == nk - 1;
-                    if (!mbar_wait(&full[s], (uint32_t)(kt / kStages) & 1u, abort_flag) ||
-                        (first && g >= 2 && !mbar_wait(&pempty[b], (uint32_t)(g / 2 - 1) & 1u, abort_flag))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a = sbase + s * kStage, bh = a + kATile, bl = bh + kBTile;
-                    const uint32_t d = tmem + 256u * (uint32_t)b;
-#pragma unroll
-                    for (int j = 0; j < kBK / 16; ++j) {
-                        const uint64_t ad = sdesc_k_sw128(a + 32 * j);
-                        mma_f16(d, ad, sdesc_k_sw128(bh + 32 * j), idesc, (j > 0 || !first) ? 1u : 0u);
-                        mma_f16(d, ad, sdesc_k_sw128(bl + 32 * j), idesc, 1u);
-                    }
-                    mma_commit(&empty[s]);
-                    if (last) mma_commit(&pfull[b]);
-                }
-                mma_commit(accf);  // completes once every MMA issued above has completed (abort path included)
-            }
-            __syncwarp();
-        } else {
-            // ------------------------------------------------------------------ producers (96 threads)
-            const int pt = threadIdx.x - 32;
-            const uint8_t* wblocks = p.wp + ((int64_t)e * (p.a_rows / kBM) + blockIdx.x) * nk * (int64_t)kWBlock;
-            const int groups = (rows + 3) >> 2;  // gather4 loads of this tile's rows
-            const uint32_t tx_bytes = (uint32_t)kWBlock + (uint32_t)groups * 4u * kRowPiece;
+            const uint32_t idesc = idesc_f16_f32(kBM, N);
             for (int kt = 0; kt < nk; ++kt) {
+                // slice kt of partial g = kt / P goes to buffer g & 1, which partial g - 2 has left
+                const int s = kt % kStages, g = kt / P, b = g & 1;
+                const bool first = kt % P == 0, last = kt % P == P - 1 || kt == nk - 1;
+                if (!mbar_wait(&full[s], (uint32_t)(kt / kStages) & 1u, abort_flag) ||
+                    (first && g >= 2 && !mbar_wait(&pempty[b], (uint32_t)(g / 2 - 1) & 1u, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = sbase + s * kStage, bh = a + kATile, bl = bh + kBTile;
+                const uint32_t d = tmem + 256u * (uint32_t)b;
+#pragma unroll
+                for (int j = 0; j < kBK / 16; ++j) {
+                    const uint64_t ad = sdesc_k_sw128(a + 32 * j);
+                    mma_f16(d, ad, sdesc_k_sw128(bh + 32 * j), idesc, (j > 0 || !first) ? 1u : 0u);
+                    mma_f16(d, ad, sdesc_k_sw128(bl + 32 * j), idesc, 1u);
+                }
+                mma_commit(&empty[s]);
+                if (last) mma_commit(&pfull[b]);
+            }
+            mma_commit(accf);  // completes once every MMA issued above has completed (abort path included)
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------------ producer (one thread)
+            const uint8_t* wblocks = p.wp + ((int64_t)e * (p.a_rows / kBM) + blockIdx.x) * nk * (int64_t)kWBlock;
+            const uint32_t tx_bytes = (uint32_t)kWBlock + (uint32_t)N * kRowPiece;
+            int issued = 0;
+            for (int kt = 0; kt < nk; ++kt, ++issued) {
                 const int r = kt % depth;
                 if (kt >= depth && !mbar_wait(&rempty[r], (uint32_t)(kt / depth - 1) & 1u, abort_flag)) {
                     ok = false;
                     break;
                 }
                 const uint32_t slot = smem_u32(ring) + (uint32_t)(r * sbytes);
-                if (pt == 0) {
-                    mbar_arrive_expect_tx(&rfull[r], tx_bytes);
-                    bulk_load(slot, wblocks + (int64_t)kt * kWBlock, kWBlock, &rfull[r]);
-                }
-                for (int g = pt; g < groups; g += kProducers) {
-                    const int r0 = 4 * g;
-                    const int y0 = srcs[r0];
-                    const int y1 = r0 + 1 < rows ? srcs[r0 + 1] : y0;
-                    const int y2 = r0 + 2 < rows ? srcs[r0 + 2] : y0;
-                    const int y3 = r0 + 3 < rows ? srcs[r0 + 3] : y0;
-                    tma_gather4(slot + o_b + g * kGroupStride, &maps.b, kt * kRowPiece, y0, y1, y2, y3, &rfull[r]);
-                }
+                mbar_arrive_expect_tx(&rfull[r], tx_bytes);
+                bulk_load(slot, wblocks + (int64_t)kt * kWBlock, kWBlock, &rfull[r]);
+                for (int b0 = 0; b0 < N; b0 += kRowBox)
+                    tma_load_2d(slot + o_b + b0 * kRowPiece, &maps.b, kt * kRowPiece, row0 + b0, &rfull[r]);
             }
+            // no copy may still be writing shared memory when the CTA exits (on the abort path the converters have
+            // not waited for the last slices): wait, bounded, for the last `depth` slices issued
+            for (int kt = max(0, issued - depth); kt < issued; ++kt)
+                mbar_wait(&rfull[kt % depth], (uint32_t)(kt / depth) & 1u, nullptr);
         }
-    } else {
-        setmaxnreg_inc<kRegsConv>();
-        // ------------------------------------------------------------------ converters (256 threads)
-        const int ct = threadIdx.x - 128;
-        // work items of 16 K values: weight items ct and ct + 256 (row = item / 4, quarter = item % 4); row items
-        // ct + 256 i of the tile's 4 N (row, quarter) pairs
-        const int nb = (4 * N - ct + 255) / 256;     // row items of this thread (0..4)
-        // promotion: this thread owns TMEM lane 32*q + lane (weight row mrow) and the 32-column chunks
-        // 2 i + chalf, i = 0..3
-        const int q = warp & 3;                 // the TMEM lane quarter this warp may access
-        const int chalf = (warp - 4) >> 2;      // warpgroup 1: even chunks; warpgroup 2: odd chunks
+        __syncwarp();
+    } else if (warp < 12) {
+        setmaxnreg_inc<kRegsProm>();
+        // ------------------------------------------------------------------ promoters (256 threads)
+        // this thread owns TMEM lane 32*q + lane (weight row mrow) and the 32-column chunks 2 i + chalf, i = 0..3
+        const int q = warp & 3;
+        const int chalf = (warp - 4) >> 2;  // warpgroup 1: even chunks; warpgroup 2: odd chunks
         const int mrow = 32 * q + lane;
         float acc[4][32];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int k = 0; k < 32; ++k) acc[i][k] = 0.0f;
-        auto promote = [&](int g) -> bool {
+        const int groups = (nk + P - 1) / P;
+        for (int g = 0; g < groups && ok; ++g) {
             const int b = g & 1;
-            if (!mbar_wait(&pfull[b], (uint32_t)(g / 2) & 1u, abort_flag)) return false;
+            if (!mbar_wait(&pfull[b], (uint32_t)(g / 2) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)b;
 #pragma unroll
-            for (int i = 0; i < 4; i += 2) {
-                const int c0 = 32 * (2 * i + chalf), c1 = 32 * (2 * i + 2 + chalf);
+            for (int i = 0; i < 4; ++i) {
+                const int c0 = 32 * (2 * i + chalf);
                 if (c0 < N) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld_32x32b_x32(base + (uint32_t)c0, v0);
-                    if (c1 < N) tmem_ld_32x32b_x32(base + (uint32_t)c1, v1);
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(base + (uint32_t)c0, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) acc[i][k] += __uint_as_float(v0[k]);
-                    if (c1 < N) {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) acc[i + 1][k] += __uint_as_float(v1[k]);
-                    }
+                    for (int k = 0; k < 32; ++k) acc[i][k] += __uint_as_float(v[k]);
                 }
             }
             tc_fence_before();
             mbar_arrive(&pempty[b]);
-            return true;
-        };
-
-        for (int kt = 0; kt < nk && ok; ++kt) {
-            const int r = kt % depth;
-            if (!mbar_wait(&rfull[r], (uint32_t)(kt / depth) & 1u, abort_flag)) {
-                ok = false;
-                break;
-            }
-            const uint8_t* slot = ring + r * sbytes;
-            // read this thread's raw values, then give the ring slot back
-            uint32_t wcode[2];
-            uint16_t wscale[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
-                wcode[i] = *reinterpret_cast<const uint32_t*>(slot + row * 16 + qu * 4);
-                wscale[i] = *reinterpret_cast<const uint16_t*>(slot + o_as + row * 4 + (qu >> 1) * 2);
-            }
-            uint4 bcode[4];
-            uint16_t bscale[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
-                if (i < nb && row < rows) {
-                    const uint8_t* piece = slot + o_b + (row >> 2) * kGroupStride + (row & 3) * kRowPiece;
-                    bcode[i] = *reinterpret_cast<const uint4*>(piece + qu * 16);
-                    bscale[i] = *reinterpret_cast<const uint16_t*>(piece + 64 + (qu >> 1) * 2);
-                } else {
-                    bcode[i] = make_uint4(0u, 0u, 0u, 0u);
-                    bscale[i] = 0;
-                }
-            }
-            mbar_arrive(&rempty[r]);
-            const int s = kt % kStages;
-            if (kt >= kStages && !mbar_wait(&empty[s], (uint32_t)(kt / kStages - 1) & 1u, abort_flag)) {
-                ok = false;
-                break;
-            }
-            uint8_t* st = smem + s * kStage;
-            uint4* a_tile = reinterpret_cast<uint4*>(st);
-            uint4* hi_tile = reinterpret_cast<uint4*>(st + kATile);
-            uint4* lo_tile = reinterpret_cast<uint4*>(st + kATile + kBTile);
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
-                decode_weights16(wcode[i], wscale[i], a_tile + row * 8, row, qu);
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
-                if (i < nb) {
-                    if (row < rows) split_activations16(bcode[i], bscale[i], hi_tile + row * 8, lo_tile + row * 8, row, qu);
-                    else zero_activations16(hi_tile + row * 8, lo_tile + row * 8, row, qu);
-                }
-            }
-            fence_async_smem();
-            mbar_arrive(&full[s]);
-            // after the first slice of partial g has been handed over, add partial g - 1
-            if (kt % P == 0 && kt >= P && !promote(kt / P - 1)) ok = false;
         }
-        if (ok && !promote((nk - 1) / P)) ok = false;
         if (ok) {
             // ------------------------------------------------------------------ epilogue: fp32 rows out
             float* outcol = p.out + (m0 + mrow);
@@ -385,6 +311,50 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     if (col < rows) outcol[(int64_t)(row0 + col) * p.a_rows] = acc[i][k];
                 }
             }
+        }
+    } else {
+        setmaxnreg_dec<kRegsConv>();
+        // ------------------------------------------------------------------ converters (256 threads)
+        // work items of 16 K values: weight items ct and ct + 256 (row = item / 4, quarter = item % 4); row items
+        // ct + 256 i of the tile's 4 N (row, quarter) pairs
+        const int ct = threadIdx.x - 384;
+        const int nb = (4 * N - ct + 255) / 256;  // row items of this thread (0..4)
+        for (int kt = 0; kt < nk && ok; ++kt) {
+            const int r = kt % depth, s = kt % kStages;
+            if (!mbar_wait(&rfull[r], (uint32_t)(kt / depth) & 1u, abort_flag) ||
+                (kt >= kStages && !mbar_wait(&empty[s], (uint32_t)(kt / kStages - 1) & 1u, abort_flag))) {
+                ok = false;
+                break;
+            }
+            const uint8_t* slot = ring + r * sbytes;
+            uint8_t* st = smem + s * kStage;
+            uint4* a_tile = reinterpret_cast<uint4*>(st);
+            uint4* hi_tile = reinterpret_cast<uint4*>(st + kATile);
+            uint4* lo_tile = reinterpret_cast<uint4*>(st + kATile + kBTile);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
+                const uint32_t code = *reinterpret_cast<const uint32_t*>(slot + row * 16 + qu * 4);
+                const uint16_t scale = *reinterpret_cast<const uint16_t*>(slot + o_as + row * 4 + (qu >> 1) * 2);
+                decode_weights16(code, scale, a_tile + row * 8, row, qu);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
+                if (i < nb) {
+                    if (row < rows) {
+                        const uint8_t* piece = slot + o_b + row * kRowPiece;
+                        const uint4 code = *reinterpret_cast<const uint4*>(piece + qu * 16);
+                        const uint16_t scale = *reinterpret_cast<const uint16_t*>(piece + 64 + (qu >> 1) * 2);
+                        split_activations16(code, scale, hi_tile + row * 8, lo_tile + row * 8, row, qu);
+                    } else {
+                        zero_activations16(hi_tile + row * 8, lo_tile + row * 8, row, qu);
+                    }
+                }
+            }
+            mbar_arrive(&rempty[r]);
+            fence_async_smem();
+            mbar_arrive(&full[s]);
         }
     }
     if (!ok) {
@@ -444,7 +414,7 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     }
     if (max_tiles <= 0) return cudaSuccess;
     GemmMaps maps;
-    if (!make_map(&maps.b, a.bsl, (uint64_t)(a.K / kBK) * kRowPiece, (uint64_t)a.b_rows, kRowPiece, 1))
+    if (!make_map(&maps.b, a.bsl, (uint64_t)(a.K / kBK) * kRowPiece, (uint64_t)a.b_rows, kRowPiece, kRowBox))
         return cudaErrorInvalidValue;
     const dim3 grid((unsigned)(a.a_rows / kBM), (unsigned)max_tiles);
     experts_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, maps);

@@ -126,16 +126,24 @@ static smoe_status check_gemm_shape(int64_t n, int E, int H, int F) {
     return SMOE_OK;
 }
 
-smoe_status smoe_experts_gateup(const uint8_t* xsl, int64_t T, const int32_t* src, int32_t* tiles, int64_t n, int E,
-                                const uint8_t* wgu, int H, int F, float* gu, void* stream) {
+smoe_status smoe_gather_slices(const uint8_t* slices, int64_t in_rows, int cols, const int32_t* src, int64_t n,
+                               uint8_t* out, void* stream) {
+    if (in_rows < 0 || n < 0 || cols < 64 || cols % 64 != 0) return SMOE_ERR_ARG;
+    if (n == 0) return SMOE_OK;
+    if (in_rows < 1 || n > INT32_MAX) return SMOE_ERR_ARG;
+    if (!aligned16(slices) || !aligned16(src) || !aligned16(out)) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_gather_slices(slices, in_rows, cols, src, n, out, (cudaStream_t)stream));
+}
+
+smoe_status smoe_experts_gateup(const uint8_t* xsl, int32_t* tiles, int64_t n, int E, const uint8_t* wgu, int H, int F,
+                                float* gu, void* stream) {
     const smoe_status st = check_gemm_shape(n, E, H, F);
     if (st != SMOE_OK) return st;
     if (n == 0) return SMOE_OK;
-    if (T < 1 || T > INT32_MAX) return SMOE_ERR_ARG;
-    if (!aligned16(xsl) || !aligned16(src) || !aligned16(tiles) || !aligned16(wgu) || !aligned16(gu))
-        return SMOE_ERR_ARG;
+    if (!aligned16(xsl) || !aligned16(tiles) || !aligned16(wgu) || !aligned16(gu)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{xsl, src, tiles, wgu, 2 * F, H, gu, T, E, true};
+    smoe::ExpertsGemmArgs a{xsl, tiles, wgu, 2 * F, H, gu, n, E, true};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 
@@ -157,7 +165,7 @@ smoe_status smoe_experts_down(const uint8_t* hsl, int32_t* tiles, int64_t n, int
     if (n == 0) return SMOE_OK;
     if (!aligned16(hsl) || !aligned16(tiles) || !aligned16(wd) || !aligned16(dm)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{hsl, nullptr, tiles, wd, H, F, dm, n, E, false};
+    smoe::ExpertsGemmArgs a{hsl, tiles, wd, H, F, dm, n, E, false};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 

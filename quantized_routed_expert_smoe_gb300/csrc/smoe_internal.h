@@ -19,21 +19,22 @@ cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc,
                                   cudaStream_t s);
 cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, uint8_t* packed,
                            cudaStream_t s);
+cudaError_t launch_gather_slices(const uint8_t* slices, int64_t in_rows, int cols, const int32_t* src, int64_t n,
+                                 uint8_t* out, cudaStream_t s);
 cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
                            cudaStream_t s);
 
 // Grouped expert product (both the gate/up and the down step): for every tile of the tile list and every 128-row
 // slice of the expert's weight matrix, OUT[row][j] = sum over K of W[e][j] . B[row], W the 2-bit weights and B the
-// q8 rows (gathered through `src` when it is not null).
+// q8 rows in routed-row order.
 struct ExpertsGemmArgs {
-    const uint8_t* bsl;   // q8 B rows in slice form, [*][K/64][80 bytes]
-    const int32_t* src;   // B row of routed row r = src[r] (gate/up), or null: B row = r (down)
+    const uint8_t* bsl;   // q8 B rows in slice form, routed-row order, [n][K/64][80 bytes]
     int32_t* tiles;       // tile list; header[3] receives SMOE_ERR_TIMEOUT
     const uint8_t* wp;    // packed weights: per (expert, 128-row tile, 64-value slice) 2560 bytes
     int a_rows;           // weight rows per expert (2F or H)
     int K;                // contraction length (H or F)
     float* out;           // [n][a_rows]
-    int64_t b_rows;       // rows of the q8 B matrix (T for gate/up, n for down)
+    int64_t b_rows;       // rows of the q8 B matrix (n)
     int n_experts;        // E
     bool two_level;       // promote every 64-wide K slice into fp32 registers (gate/up); else one accumulator
 };

@@ -27,8 +27,8 @@ def declared_functions():
 
 def test_header_declares_the_seven_steps():
     names = declared_functions()
-    for step in ["smoe_route_topk", "smoe_group", "smoe_quantize_q8", "smoe_experts_gateup", "smoe_swiglu_requant",
-                 "smoe_experts_down", "smoe_combine"]:
+    for step in ["smoe_route_topk", "smoe_group", "smoe_quantize_q8", "smoe_gather_slices", "smoe_experts_gateup",
+                 "smoe_swiglu_requant", "smoe_experts_down", "smoe_combine"]:
         assert step in names
 
 
@@ -66,7 +66,11 @@ def test_host_side_rejections_need_no_gpu(lib):
     assert lib.smoe_quantize_q8(fake, 4, 48, fake, fake, null, null) == ARG
     assert lib.smoe_quantize_q8(fake, 4, 96, fake, fake, fake, null) == ARG  # slice form needs cols % 64 == 0
     # gemm shapes the kernels do not cover
-    assert lib.smoe_experts_gateup(fake, 5, fake, fake, 10, 4, fake, 96, 64, fake, null) == UNSUP
+    assert lib.smoe_experts_gateup(fake, fake, 10, 4, fake, 96, 64, fake, null) == UNSUP
+    # gather: cols not a multiple of 64, misaligned output
+    assert lib.smoe_gather_slices(fake, 4, 96, fake, 8, fake, null) == ARG
+    assert lib.smoe_gather_slices(fake, 4, 128, fake, 8, odd, null) == ARG
+    assert lib.smoe_gather_slices(fake, 4, 128, fake, 0, fake, null) == 0  # nothing routed: nothing to do
     assert lib.smoe_experts_down(fake, fake, 10, 4, fake, 256, 48, fake, null) == UNSUP
     assert lib.smoe_pack_q2(fake, fake, 2, 100, 64, fake, null) == ARG  # rows % 128
     # group: tiles buffer too small

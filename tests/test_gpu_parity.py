@@ -196,6 +196,31 @@ def test_quantize_bit_exact_full_and_edges(B):
     assert np.array_equal(c, co) and np.array_equal(s, so)
 
 
+def test_gather_slices_routed_rows(B):
+    """Routed-row order of the q8 slice form: byte for byte the source row, for the full t8192 grouping (ragged
+    per-expert counts) and for hand-made src lists (repeats, out-of-range entries give zero rows, a single row)."""
+    inp = layer_inputs("t8192")
+    cfg = synth.CONFIGS["t8192"]
+    ids, _ = oracle.route(inp["logits"], cfg.K)
+    g = oracle.group(ids, cfg.E)
+    co, so = oracle.quantize_q8(inp["x"])
+    sl = to_slices(co, so)
+    n = cfg.T * cfg.K
+    out = torch.full((B.slices_bytes(n, cfg.H),), 0xCD, dtype=torch.uint8, device="cuda")
+    B.smoe_gather_slices(dev(sl.reshape(-1)), cfg.T, cfg.H, dev(g["src"]), out)
+    assert np.array_equal(host(out).reshape(n, -1, 80), sl[g["src"].astype(np.int64)])
+    rng = np.random.default_rng(5)
+    rows, cols = 7, 192
+    raw = rng.integers(0, 256, size=(rows, cols // 64, 80), dtype=np.uint8)
+    for src in (np.array([3, 3, 0, 6, -1, 7, 2, 1 << 30, 5], np.int32), np.array([4], np.int32)):
+        out = torch.full((B.slices_bytes(len(src), cols),), 0xCD, dtype=torch.uint8, device="cuda")
+        B.smoe_gather_slices(dev(raw.reshape(-1)), rows, cols, dev(src), out)
+        want = np.zeros((len(src), cols // 64, 80), np.uint8)
+        ok = (src >= 0) & (src < rows)
+        want[ok] = raw[src[ok]]
+        assert np.array_equal(host(out).reshape(len(src), cols // 64, 80), want)
+
+
 # ------------------------------------------------------------------------------------------------ expert products
 def _tiles_dev(B, g, n, E):
     raw = np.zeros(B.tiles_bytes(n, E) // 4, np.int32)
@@ -206,13 +231,15 @@ def _tiles_dev(B, g, n, E):
 
 
 def gpu_gateup(B, xc, xs, g, wgu_c, wgu_s, n, E):
-    """gate/up through the C ABI: the oracle's q8 rows laid out in slice form, the weights packed by the library."""
+    """gate/up through the C ABI: the oracle's q8 rows in routed-row order and slice form, the weights packed by the
+    library."""
     tiles = _tiles_dev(B, g, n, E)
     T, H = xc.shape
     F = wgu_c.shape[1] // 2
     gu = torch.full((n, 2 * F), float("nan"), dtype=torch.float32, device="cuda")
     wp = B.pack_weights(wgu_c, wgu_s)
-    B.smoe_experts_gateup(dev(to_slices(xc, xs)), T, dev(g["src"]), tiles, n, E, wp, H, F, gu)
+    src = g["src"].astype(np.int64)
+    B.smoe_experts_gateup(dev(to_slices(xc[src], xs[src])), tiles, n, E, wp, H, F, gu)
     t = host(tiles)
     assert t[3] == 0, "kernel reported a timeout"
     return gu
