@@ -9,7 +9,7 @@
  *   smoe_route_topk      router softmax, top-K of the E logits, weights renormalised over the K
  *   smoe_group           stable counting sort of the T*K (token, k) pairs by expert: counts, offsets, src, slot, tiles
  *   smoe_quantize_q8     activations to int8 once per token, one fp16 scale per 32 values
- *   smoe_gather_slices   the q8 rows of the routed pairs in routed-row order
+ *   smoe_gather_q8       the q8 rows of the routed pairs in routed-row order, in operand form
  *   smoe_experts_gateup  grouped gate/up product of each routed row against its expert's 2-bit weights
  *   smoe_swiglu_requant  h = silu(gate) * up, requantised to int8 per 32 values
  *   smoe_experts_down    grouped down product into one fp32 row per routed pair
@@ -24,14 +24,16 @@
  *                    bits 2i..2i+1 of byte j; scales fp16 [E][rows][cols/32].  The value of a weight is d * (q - 2),
  *                    q in {0,1,2,3}.  Gate/up matrix: rows [0, F) gate, [F, 2F) up, cols H.  Down matrix: rows H,
  *                    cols F.
- *   q8 slice form    what the expert products read (written by smoe_quantize_q8 / smoe_swiglu_requant beside the
- *                    planar form): per row and per 64 values, 80 bytes = the 64 codes, the two fp16 scales of the
- *                    slice's two 32-value blocks, 12 zero bytes; [rows][cols/64][80].  smoe_slices_bytes sizes it.
+ *   q8 operand form  the q8 values as the expert products read them: two fp16 planes [2][rows][cols], plane 0
+ *                    hi = fp16_rn(d * q) and plane 1 lo = d * q - hi (exact: d * q has at most 18 significant
+ *                    bits), and within every group of 16 values position 2j holds value j and position 2j+1 value
+ *                    j+8 (j = 0..7).  hi + lo = d * q exactly.  Written by smoe_gather_q8 (routed activations) and
+ *                    smoe_swiglu_requant (H).
  *   packed Q2        what the expert products read as weights (smoe_pack_q2 writes it once from the row-major form):
  *                    per (expert, 128-row tile, 64-value slice) a 2560-byte block = the tile's 128 rows x 16 code
  *                    bytes, then its 128 rows x 2 fp16 scales; blocks ordered by expert, tile, slice.
  *   tiles            int32 [4 + 4 * smoe_max_tiles(n, E)]: header {n_tiles, group_status, n, kernel_status}, then
- *                    per tile {expert, first row, rows, 0}; each expert's c rows split into ceil(c/256) near-equal
+ *                    per tile {expert, first row, rows, 0}; each expert's c rows split into ceil(c/224) near-equal
  *                    tiles [floor(i*c/nt), floor((i+1)*c/nt)), experts in id order.
  *
  * CONVENTIONS
@@ -67,7 +69,7 @@ typedef int smoe_status;
 /* Largest supported sizes. */
 #define SMOE_MAX_EXPERTS 1024
 #define SMOE_MAX_TOPK 32
-#define SMOE_TILE_ROWS 256
+#define SMOE_TILE_ROWS 224
 
 /* Human-readable name of a status code (static storage). */
 const char* smoe_status_string(smoe_status s);
@@ -78,7 +80,7 @@ const char* smoe_last_error_string(void);
 /* SMOE_OK when the current CUDA device is an sm_103 part the kernels were built for. */
 smoe_status smoe_device_check(void);
 
-/* Most tiles smoe_group can emit for n pairs over E experts: ceil(n / 256) + min(E, n). */
+/* Most tiles smoe_group can emit for n pairs over E experts: ceil(n / 224) + min(E, n). */
 int64_t smoe_max_tiles(int64_t n, int E);
 /* Bytes of the tiles buffer: 16 * (1 + smoe_max_tiles(n, E)). */
 size_t smoe_tiles_bytes(int64_t n, int E);
@@ -123,13 +125,8 @@ smoe_status smoe_group_noalloc(const int32_t* ids, int64_t T, int K, int E, int3
 
 /* Step 3 -- q8 activations.  Page "Strata compare v0.1.35...v0.1.37", moe_fused.hpp quantize_act: the layer input is
  * rounded to int8 once per TOKEN (not per routed slot) with one scale per 32 values.
- *   x fp32 [rows][cols] (|x| < 65504) -> codes int8 [rows][cols], scales fp16 [rows][cols/32].  cols % 32 == 0.
- *   slices   optional (NULL: not written): the same codes and scales in slice form, smoe_slices_bytes(rows, cols)
- *            bytes; needs cols % 64 == 0. */
-smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales,
-                             uint8_t* slices, void* stream);
-/* Bytes of the slice form of rows x cols q8 values: rows * (cols / 64) * 80. */
-size_t smoe_slices_bytes(int64_t rows, int cols);
+ *   x fp32 [rows][cols] (|x| < 65504) -> codes int8 [rows][cols], scales fp16 [rows][cols/32].  cols % 32 == 0. */
+smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales, void* stream);
 
 /* Weight preparation (once per weight set): the row-major Q2 matrices of E experts (codes [E][rows][cols/4], scales
  * [E][rows][cols/32]) into the packed form the expert products read.  rows % 128 == 0, cols % 64 == 0.
@@ -139,42 +136,40 @@ smoe_status smoe_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, in
 size_t smoe_pack_q2_bytes(int E, int rows, int cols);
 
 /* Step 4a -- routed rows of the q8 activations.  moe_fused.hpp experts() reads each routed row's activations
- * "through the rows of group": this call lays them out once in routed-row order, so that every tile of the expert
- * products reads its rows as one contiguous block.
- *   slices   q8 rows in slice form, [in_rows][cols/64][80] (from smoe_quantize_q8).
- *   src      int32 [n], from smoe_group; every entry in [0, in_rows) (an entry outside it is not read: its output row
- *            is zero-filled and the call still returns SMOE_OK, which a bad grouping has already reported).
- *   out      [n][cols/64][80] out: out row r = slices row src[r], byte for byte.   cols % 64 == 0. */
-smoe_status smoe_gather_slices(const uint8_t* slices, int64_t in_rows, int cols, const int32_t* src, int64_t n,
-                               uint8_t* out, void* stream);
+ * "through the rows of group": this call lays them out once in routed-row order and operand form, so that every
+ * tile of the expert products reads its rows as one contiguous block.
+ *   codes, scales  int8 [in_rows][cols] and fp16 [in_rows][cols/32] (from smoe_quantize_q8).
+ *   src      int32 [n], from smoe_group; every entry in [0, in_rows) (an entry outside it is not read: its output rows
+ *            are zero-filled and the call still returns SMOE_OK, which a bad grouping has already reported).
+ *   out      fp16 [2][n][cols] out, operand form: row r = row src[r].   cols % 32 == 0. */
+smoe_status smoe_gather_q8(const int8_t* codes, const uint16_t* scales, int64_t in_rows, int cols, const int32_t* src,
+                           int64_t n, uint16_t* out, void* stream);
 
 /* Step 4b -- grouped gate/up.  moe_fused.hpp experts(): gate/up of the routed rows; per routed row r of expert e and
  * output j in [0, 2F):
- *   GU[r][j] = sum_b dW[e][j][b] * dX[r][b] * sum_{i in block b} (qW - 2) * qX     (fp32 result)
- *   xsl      q8 activations of the n routed rows in slice form, routed-row order ([n][H/64][80], from
- *            smoe_gather_slices).
+ *   GU[r][j] = sum_b dX[src r][b] * dW[e][j][b] * sum_{i in block b} (qW - 2) * qX[src r][i]     (fp32 result)
+ *   xop      the routed rows in operand form, fp16 [2][n][H] (from smoe_gather_q8).
  *   tiles    from smoe_group (header[3] receives SMOE_ERR_TIMEOUT).   n = T*K (sizes the launch).
  *   wgu      gate/up weights [E][2F][H] packed by smoe_pack_q2.
  *   gu       fp32 [n][2F] out, row r = routed row r.
  *   H % 128 == 0, F % 64 == 0. */
-smoe_status smoe_experts_gateup(const uint8_t* xsl, int32_t* tiles, int64_t n, int E, const uint8_t* wgu, int H, int F,
+smoe_status smoe_experts_gateup(const uint16_t* xop, int32_t* tiles, int64_t n, int E, const uint8_t* wgu, int H, int F,
                                 float* gu, void* stream);
 
 /* Step 5 -- SwiGLU and requantisation.  Page "src/prefill/prefill.cpp": mmq::swiglu(GU, H, rows, ...) then the
  * int8 rounding of H; moe_fused.hpp: "SwiGLU, H as int8".
  *   gu fp32 [n][2F] -> h_j = silu(gu[r][j]) * gu[r][F + j] (fp32; silu(g) = g / (1 + exp(-g))), then the q8 rule:
  *   hc int8 [n][F], hs fp16 [n][F/32].  F % 32 == 0.
- *   slices   optional (NULL: not written): H in slice form, smoe_slices_bytes(n, F) bytes; needs F % 64 == 0. */
-smoe_status smoe_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint8_t* slices,
+ *   hop      optional (NULL: not written): H in operand form, fp16 [2][n][F]; needs F % 64 == 0. */
+smoe_status smoe_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint16_t* hop,
                                 void* stream);
 
 /* Step 6 -- grouped down.  moe_fused.hpp experts(): "down into dm [n][2560] FP32 at the rows of group":
- *   Dm[r][o] = sum_b dW[e][o][b] * dH[r][b] * sum_{i in block b} (qW - 2) * qH,   o in [0, H)
- *   hsl      q8 H rows in slice form ([n][F/64][80], routed-row order, from smoe_swiglu_requant).  tiles from
- *            smoe_group.
+ *   Dm[r][o] = sum_b dH[r][b] * dW[e][o][b] * sum_{i in block b} (qW - 2) * qH[r][i],   o in [0, H)
+ *   hop      H in operand form, fp16 [2][n][F] (from smoe_swiglu_requant).   tiles from smoe_group.
  *   wd       down weights [E][H][F] packed by smoe_pack_q2.
  *   dm       fp32 [n][H] out.   H % 128 == 0, F % 64 == 0. */
-smoe_status smoe_experts_down(const uint8_t* hsl, int32_t* tiles, int64_t n, int E, const uint8_t* wd, int H, int F,
+smoe_status smoe_experts_down(const uint16_t* hop, int32_t* tiles, int64_t n, int E, const uint8_t* wd, int H, int F,
                               float* dm, void* stream);
 
 /* Step 7 -- combine.  The combine that reads the per-slot rows (page "src/prefill/prefill.cpp", the engine's

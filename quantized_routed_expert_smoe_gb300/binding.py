@@ -19,7 +19,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsmoe.so")
 
 SMOE_OK, SMOE_ERR_ARG, SMOE_ERR_LAUNCH, SMOE_ERR_UNSUPPORTED, SMOE_ERR_RANGE, SMOE_ERR_TIMEOUT = range(6)
-TILE_ROWS = 256
+TILE_ROWS = 224
 
 
 class SmoeError(RuntimeError):
@@ -47,13 +47,12 @@ _SIGS = {
                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
                             ctypes.c_void_p], ctypes.c_int),
     "smoe_quantize_q8": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
-                          ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
-    "smoe_slices_bytes": ([ctypes.c_int64, ctypes.c_int], ctypes.c_size_t),
+                          ctypes.c_void_p], ctypes.c_int),
     "smoe_pack_q2": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                       ctypes.c_void_p], ctypes.c_int),
     "smoe_pack_q2_bytes": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
-    "smoe_gather_slices": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
-                            ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_gather_q8": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                        ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_experts_gateup": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
                              ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_swiglu_requant": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
@@ -131,10 +130,6 @@ def group_work_bytes(n: int, E: int) -> int:
     return int(load_library().smoe_group_work_bytes(n, E))
 
 
-def slices_bytes(rows: int, cols: int) -> int:
-    return int(load_library().smoe_slices_bytes(rows, cols))
-
-
 def pack_q2_bytes(E: int, rows: int, cols: int) -> int:
     return int(load_library().smoe_pack_q2_bytes(E, rows, cols))
 
@@ -170,11 +165,11 @@ def smoe_group_noalloc(ids, E, counts, offsets, src, slot, tiles, stream=None):
         _dev(tiles, torch.int32, "tiles"), tiles.numel() * 4, _stream(stream)))
 
 
-def smoe_quantize_q8(x, codes, scales, slices=None, stream=None):
+def smoe_quantize_q8(x, codes, scales, stream=None):
     rows, cols = x.shape
     _check("smoe_quantize_q8", load_library().smoe_quantize_q8(
         _dev(x, torch.float32, "x"), rows, cols, _dev(codes, torch.int8, "codes"),
-        _dev(scales, torch.int16, "scales"), _opt(slices, torch.uint8, "slices"), _stream(stream)))
+        _dev(scales, torch.int16, "scales"), _stream(stream)))
 
 
 def smoe_pack_q2(codes, scales, packed, stream=None):
@@ -185,29 +180,31 @@ def smoe_pack_q2(codes, scales, packed, stream=None):
         _dev(packed, torch.uint8, "packed"), _stream(stream)))
 
 
-def smoe_gather_slices(slices, in_rows, cols, src, out, stream=None):
-    """out row r = slices row src[r] (q8 rows in slice form, cols values a row); n = src.numel()."""
-    _check("smoe_gather_slices", load_library().smoe_gather_slices(
-        _dev(slices, torch.uint8, "slices"), in_rows, cols, _dev(src, torch.int32, "src"), src.numel(),
-        _dev(out, torch.uint8, "out"), _stream(stream)))
+def smoe_gather_q8(codes, scales, src, out, stream=None):
+    """out = the q8 rows src[r] of (codes int8 [in_rows][cols], scales [in_rows][cols/32]) in operand form, fp16
+    [2][n][cols] (n = src.numel())."""
+    in_rows, cols = codes.shape
+    _check("smoe_gather_q8", load_library().smoe_gather_q8(
+        _dev(codes, torch.int8, "codes"), _dev(scales, torch.int16, "scales"), in_rows, cols,
+        _dev(src, torch.int32, "src"), src.numel(), _dev(out, torch.float16, "out"), _stream(stream)))
 
 
-def smoe_experts_gateup(xsl, tiles, n, E, wgu, H, F, gu, stream=None):
+def smoe_experts_gateup(xop, tiles, n, E, wgu, H, F, gu, stream=None):
     _check("smoe_experts_gateup", load_library().smoe_experts_gateup(
-        _dev(xsl, torch.uint8, "xsl"), _dev(tiles, torch.int32, "tiles"), n, E, _dev(wgu, torch.uint8, "wgu"), H, F,
+        _dev(xop, torch.float16, "xop"), _dev(tiles, torch.int32, "tiles"), n, E, _dev(wgu, torch.uint8, "wgu"), H, F,
         _dev(gu, torch.float32, "gu"), _stream(stream)))
 
 
-def smoe_swiglu_requant(gu, hc, hs, slices=None, stream=None):
+def smoe_swiglu_requant(gu, hc, hs, hop=None, stream=None):
     n, twoF = gu.shape
     _check("smoe_swiglu_requant", load_library().smoe_swiglu_requant(
         _dev(gu, torch.float32, "gu"), n, twoF // 2, _dev(hc, torch.int8, "hc"), _dev(hs, torch.int16, "hs"),
-        _opt(slices, torch.uint8, "slices"), _stream(stream)))
+        _opt(hop, torch.float16, "hop"), _stream(stream)))
 
 
-def smoe_experts_down(hsl, tiles, n, E, wd, H, F, dm, stream=None):
+def smoe_experts_down(hop, tiles, n, E, wd, H, F, dm, stream=None):
     _check("smoe_experts_down", load_library().smoe_experts_down(
-        _dev(hsl, torch.uint8, "hsl"), _dev(tiles, torch.int32, "tiles"), n, E, _dev(wd, torch.uint8, "wd"), H, F,
+        _dev(hop, torch.float16, "hop"), _dev(tiles, torch.int32, "tiles"), n, E, _dev(wd, torch.uint8, "wd"), H, F,
         _dev(dm, torch.float32, "dm"), _stream(stream)))
 
 
@@ -246,12 +243,11 @@ class SmoeBlock:
         self.work = e(max(group_work_bytes(n, E), 16), dt=torch.uint8)
         self.xc = e(T, H, dt=torch.int8)
         self.xs = e(T, H // 32, dt=torch.int16)
-        self.xsl = e(max(slices_bytes(T, H), 16), dt=torch.uint8)
-        self.xslr = e(max(slices_bytes(n, H), 16), dt=torch.uint8)  # routed-row order
+        self.xop = e(2, max(n, 1), H, dt=torch.float16)  # routed rows, operand form (hi, lo)
         self.gu = e(n, 2 * F, dt=torch.float32)
         self.hc = e(n, F, dt=torch.int8)
         self.hs = e(n, F // 32, dt=torch.int16)
-        self.hsl = e(max(slices_bytes(n, F), 16), dt=torch.uint8)
+        self.hop = e(2, max(n, 1), F, dt=torch.float16)
         self.dm = e(n, H, dt=torch.float32)
         self.y = e(T, H, dt=torch.float32)
 
@@ -259,11 +255,11 @@ class SmoeBlock:
         smoe_route_topk(logits, self.ids, self.w, stream)
         smoe_group(self.ids, self.E, self.counts, self.offsets, self.src[:self.n], self.slot[:self.n], self.tiles,
                    self.work, stream)
-        smoe_quantize_q8(x, self.xc, self.xs, self.xsl, stream)
-        smoe_gather_slices(self.xsl, self.T, self.H, self.src[:self.n], self.xslr, stream)
-        smoe_experts_gateup(self.xslr, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.gu, stream)
-        smoe_swiglu_requant(self.gu, self.hc, self.hs, self.hsl, stream)
-        smoe_experts_down(self.hsl, self.tiles, self.n, self.E, self.wd, self.H, self.F, self.dm, stream)
+        smoe_quantize_q8(x, self.xc, self.xs, stream)
+        smoe_gather_q8(self.xc, self.xs, self.src[:self.n], self.xop, stream)
+        smoe_experts_gateup(self.xop, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.gu, stream)
+        smoe_swiglu_requant(self.gu, self.hc, self.hs, self.hop, stream)
+        smoe_experts_down(self.hop, self.tiles, self.n, self.E, self.wd, self.H, self.F, self.dm, stream)
         smoe_combine(self.dm, self.slot, self.w, self.y, stream)
         return self.y
 

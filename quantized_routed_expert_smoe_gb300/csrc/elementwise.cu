@@ -10,9 +10,11 @@
 // an IEEE fp32 division, and q = clamp(roundf(x / float(d)), -127, 127), again an IEEE fp32 division, roundf
 // rounding half away from zero; d == 0 gives zero codes.  Four threads share a block, eight values each.
 //
-// Both q8 writers can also emit the expert products' slice form of the same codes: per row and per 64 values, 80
-// bytes = the 64 codes, the two fp16 scales of the slice's 32-value blocks, 12 zero bytes (one 80-byte row piece per
-// slice, so a single TMA row load brings a slice's codes with their scales).
+// The expert products read q8 rows in OPERAND FORM: the value d * q of every code split exactly into two fp16
+// planes [2][rows][cols], hi = fp16_rn(d * q) and lo = d * q - hi (d * q has at most 18 significant bits, so the
+// remainder is exact in fp16); within every group of 16 values position 2j holds value j and position 2j+1 value
+// j+8 (j = 0..7) -- the K order in which the products unpack 2-bit weights in pairs.  SwiGLU writes it for H beside
+// the planar codes; the routed-row gather writes it for the activations of every routed pair.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -22,17 +24,35 @@
 namespace smoe {
 namespace {
 
-// 8 codes at value offset c of a row into the slice form: 80 bytes per 64 values of the row
-__device__ __forceinline__ void put_slice(uint8_t* slices, int64_t row, int cols, int c, uint2 q, uint16_t scale,
-                                          bool block_leader) {
-    uint8_t* piece = slices + (row * (cols / 64) + c / 64) * 80;
-    const int w = c % 64;
-    *reinterpret_cast<uint2*>(piece + w) = q;
-    if (block_leader) *reinterpret_cast<uint16_t*>(piece + 64 + (w / 32) * 2) = scale;
-    if (w == 56) {
-        uint32_t* pad = reinterpret_cast<uint32_t*>(piece + 68);
-        pad[0] = pad[1] = pad[2] = 0u;
+// codes a[k] (bytes of a) and b[k] (bytes of b), k = 0..3, as the four fp16 pairs (a[k], b[k]): for a signed byte
+// q, (q ^ 0x80) = q + 128, so the half with low byte (q ^ 0x80) and high byte 0x64 reads 1024 + 128 + q
+__device__ __forceinline__ uint4 interleave_codes8(uint32_t a, uint32_t b) {
+    const __half2 k1152 = __float2half2_rn(1152.0f);
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t t = __byte_perm(a, b, k | ((4 + k) << 8));
+        const uint32_t v = (t & 0x00FF00FFu) ^ 0x64806480u;
+        const __half2 q = __hsub2(*reinterpret_cast<const __half2*>(&v), k1152);
+        h[k] = *reinterpret_cast<const uint32_t*>(&q);
     }
+    return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+// fp16 code pairs q (exact integers) scaled by d and split: hi = fp16_rn(q d), lo = q d - hi (exact)
+__device__ __forceinline__ void split_pairs(uint4 qp, __half2 d2, uint4& hi, uint4& lo) {
+    const uint32_t w[4] = {qp.x, qp.y, qp.z, qp.w};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __half2 q = *reinterpret_cast<const __half2*>(&w[k]);
+        const __half2 ph = __hmul2(q, d2);
+        const __half2 pl = __hfma2(q, d2, __hneg2(ph));
+        h[k] = *reinterpret_cast<const uint32_t*>(&ph);
+        l[k] = *reinterpret_cast<const uint32_t*>(&pl);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // q8 of the 8 values v held by this thread, its block being spread over 4 consecutive lanes; returns the 8 codes
@@ -64,8 +84,7 @@ __device__ __forceinline__ uint2 q8_encode8(const float (&v)[8], uint16_t* scale
 
 // step 3: x [rows][cols] -> codes, scales; thread i covers elements [8i, 8i + 8) of the flattened rows
 __global__ void __launch_bounds__(256) quantize_q8_kernel(const float4* __restrict__ x, int64_t n8, int cols,
-                                                          uint2* __restrict__ codes, uint16_t* __restrict__ scales,
-                                                          uint8_t* __restrict__ slices) {
+                                                          uint2* __restrict__ codes, uint16_t* __restrict__ scales) {
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < n8; base += (int64_t)gridDim.x * blockDim.x) {
         const int64_t i = base + threadIdx.x;
         // n8 is a multiple of 4 (cols % 32 == 0), so every group of 4 lanes is either all in range or all out;
@@ -82,19 +101,17 @@ __global__ void __launch_bounds__(256) quantize_q8_kernel(const float4* __restri
         if (in) {
             codes[i] = q;
             if ((i & 3) == 0) scales[i >> 2] = sb;
-            if (slices) {
-                const int64_t r = (8 * i) / cols;
-                put_slice(slices, r, cols, (int)(8 * i - r * cols), q, sb, (i & 3) == 0);
-            }
         }
     }
 }
 
 // step 5: per routed row, h_j = silu(g_j) * u_j with g = gu[r][j], u = gu[r][F + j], then the q8 rule per 32 of h.
-// thread i covers h values [8c, 8c + 8) of row r = i / (F/8), c = i % (F/8).
+// thread i covers h values [8c, 8c + 8) of row r = i / (F/8), c = i % (F/8); lanes 2l and 2l+1 hold the two halves of
+// one group of 16 (one scale), so after one exchange each writes 8 operand-form values of both planes at its own
+// planar offset.
 __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __restrict__ gu, int64_t n, int F,
                                                              uint2* __restrict__ hc, uint16_t* __restrict__ hs,
-                                                             uint8_t* __restrict__ slices) {
+                                                             uint4* __restrict__ hop, int64_t plane) {
     const int64_t per_row = F / 8;
     const int64_t total = n * per_row;
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
@@ -113,12 +130,19 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
         }
         uint16_t sb;
         const uint2 q = q8_encode8(v, &sb);
+        // the even lane holds values 0..7 of its group of 16, the odd lane 8..15; F % 16 == 0 keeps the pairs aligned
+        const bool even = (threadIdx.x & 1) == 0;
+        const uint32_t other = __shfl_xor_sync(0xffffffffu, even ? q.y : q.x, 1);
         if (in) {
             hc[i] = q;  // row r's codes start at r * F = 8 * (r * per_row): element offset 8i
             if ((i & 3) == 0) hs[i >> 2] = sb;
-            if (slices) {
-                const int64_t r = i / per_row;
-                put_slice(slices, r, F, (int)(8 * (i - r * per_row)), q, sb, (i & 3) == 0);
+            // even lane: positions 0..7 = (v0, v8, v1, v9, ...); odd lane: positions 8..15 = (v4, v12, v5, v13, ...)
+            if (hop) {
+                const uint4 qp = even ? interleave_codes8(q.x, other) : interleave_codes8(other, q.y);
+                uint4 hi, lo;
+                split_pairs(qp, __half2half2(__ushort_as_half(sb)), hi, lo);
+                hop[i] = hi;
+                hop[plane + i] = lo;
             }
         }
     }
@@ -173,22 +197,36 @@ __global__ void __launch_bounds__(160) pack_q2_kernel(const uint8_t* __restrict_
     }
 }
 
-// Routed rows of the q8 activations in slice form: out row r = in row src[r] (80-byte pieces per 64 values, so a row
-// is a whole number of 16-byte words).  One warp per output row, its lanes striding over the row's words; an src
-// entry outside [0, in_rows) gives a zero row.
-__global__ void __launch_bounds__(256) gather_slices_kernel(const uint4* __restrict__ in, int64_t in_rows,
-                                                            int words, const int32_t* __restrict__ src, int64_t n,
-                                                            uint4* __restrict__ out) {
+// Routed rows of the q8 activations in operand form: out row r = codes row src[r] scaled by its scales and split
+// into the hi and lo planes, in operand order.  One warp per output row, its lanes striding over the row's groups of
+// 16 codes (16 bytes of codes and one scale in, 2 x 32 bytes out); an src entry outside [0, in_rows) gives zero rows.
+__global__ void __launch_bounds__(256) gather_q8_kernel(const uint4* __restrict__ codes,
+                                                        const uint16_t* __restrict__ scales, int64_t in_rows,
+                                                        int groups, const int32_t* __restrict__ src, int64_t n,
+                                                        uint4* __restrict__ out) {
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t plane = n * groups * 2;  // uint4 words per plane
     for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n; r += warps) {
         const int32_t t = __ldg(src + r);
-        uint4* o = out + r * words;
+        uint4* o = out + r * groups * 2;
         if (t < 0 || t >= in_rows) {
-            for (int w = lane; w < words; w += 32) o[w] = make_uint4(0u, 0u, 0u, 0u);
+            for (int g = lane; g < groups; g += 32)
+                o[2 * g] = o[2 * g + 1] = o[plane + 2 * g] = o[plane + 2 * g + 1] = make_uint4(0u, 0u, 0u, 0u);
         } else {
-            const uint4* i = in + (int64_t)t * words;
-            for (int w = lane; w < words; w += 32) o[w] = __ldg(i + w);
+            const uint4* i = codes + (int64_t)t * groups;
+            const uint16_t* sc = scales + (int64_t)t * (groups / 2);
+            for (int g = lane; g < groups; g += 32) {
+                const uint4 c = __ldg(i + g);  // values 0..3, 4..7, 8..11, 12..15 of the group
+                const __half2 d2 = __half2half2(__ushort_as_half(__ldg(sc + g / 2)));
+                uint4 hi, lo;
+                split_pairs(interleave_codes8(c.x, c.z), d2, hi, lo);
+                o[2 * g] = hi;
+                o[plane + 2 * g] = lo;
+                split_pairs(interleave_codes8(c.y, c.w), d2, hi, lo);
+                o[2 * g + 1] = hi;
+                o[plane + 2 * g + 1] = lo;
+            }
         }
     }
 }
@@ -202,19 +240,20 @@ int grid_for(int64_t threads, int block) {
 }  // namespace
 
 cudaError_t launch_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales,
-                               uint8_t* slices, cudaStream_t s) {
+                               cudaStream_t s) {
     const int64_t n8 = rows * (int64_t)cols / 8;
     if (n8 == 0) return cudaSuccess;
     quantize_q8_kernel<<<grid_for(n8, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(x), n8, cols,
-                                                        reinterpret_cast<uint2*>(codes), scales, slices);
+                                                        reinterpret_cast<uint2*>(codes), scales);
     return cudaGetLastError();
 }
 
-cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint8_t* slices,
+cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint16_t* hop,
                                   cudaStream_t s) {
     const int64_t total = n * (int64_t)(F / 8);
     if (total == 0) return cudaSuccess;
-    swiglu_requant_kernel<<<grid_for(total, 256), 256, 0, s>>>(gu, n, F, reinterpret_cast<uint2*>(hc), hs, slices);
+    swiglu_requant_kernel<<<grid_for(total, 256), 256, 0, s>>>(gu, n, F, reinterpret_cast<uint2*>(hc), hs,
+                                                               reinterpret_cast<uint4*>(hop), total);
     return cudaGetLastError();
 }
 
@@ -226,12 +265,11 @@ cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, 
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather_slices(const uint8_t* slices, int64_t in_rows, int cols, const int32_t* src, int64_t n,
-                                 uint8_t* out, cudaStream_t s) {
+cudaError_t launch_gather_q8(const int8_t* codes, const uint16_t* scales, int64_t in_rows, int cols,
+                             const int32_t* src, int64_t n, uint16_t* out, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    const int words = cols / 64 * 5;
-    gather_slices_kernel<<<grid_for(n * 32, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(slices), in_rows, words,
-                                                               src, n, reinterpret_cast<uint4*>(out));
+    gather_q8_kernel<<<grid_for(n * 32, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(codes), scales, in_rows,
+                                                           cols / 16, src, n, reinterpret_cast<uint4*>(out));
     return cudaGetLastError();
 }
 

@@ -1,42 +1,54 @@
 // experts_gemm.cu -- the grouped expert products of the routed-expert block (steps 4 and 6) on the 5th-generation
-// tensor cores (tcgen05.mma, accumulators in tensor memory), sm_103a.
+// tensor cores (tcgen05.mma, operands in tensor and shared memory, accumulators in tensor memory), sm_103a.
 //
 // Page "Strata compare v0.1.35...v0.1.37", include/strata/prefill/moe_fused.hpp experts(): for each expert, gate/up
 // of its routed rows from the per-token int8 activations against its 2-bit weights, then down into one fp32 row per
-// routed pair.  Per output:  sum_b dW[b] * dA[b] * sum_{i in b} (qW - 2) * qA.
+// routed pair.  Per output:  sum_b dB[b] * (dW[b] * sum_{i in b} (qW - 2) * qB)  over the 32-value blocks b of K.
 //
-// GB300 design.  The int8 tensor rate of this part is far below its fp16 rate, so the contraction runs as
-// tcgen05.mma.kind::f16 on EXACT fp16 re-encodings of the two quantised operands:
-//   - a weight d * (q - 2), q in {0..3}, is d times {-2, -1, 0, 1}: exactly representable in fp16;
-//   - an activation d * q (fp16 d, |q| <= 127) needs up to 18 significant bits; it is split into
-//     hi = fp16_rn(d * q) and lo = d * q - hi, which is exact in fp16 (at most 8 significant bits), so
-//     hi + lo = d * q exactly.
-// Every product of an fp16 weight and an fp16 hi/lo part is exact in the fp32 accumulator, so each output is the
-// sum of the exact products d_w (q_w - 2) d_a q_a.  The K loop runs two MMAs per 16-wide K step (A x B_hi,
-// A x B_lo).  The tensor core's fp32 accumulation aligns its addends with truncation, which over the 2 * K / 16 steps
-// of a whole row costs about 3e-6 of the result -- enough to flip requantised H codes -- so the accumulation is
-// two-level where it matters: for gate/up, whose output is requantised, each 64-wide K slice accumulates from zero
-// into one of two tensor-memory buffers (the partial is small, so its truncation error is too) and the promoter
-// warps add each finished partial into fp32 registers with round-to-nearest while the tensor core fills the other
-// buffer (one slice per partial: two flipped one H scale of the smallest test chunk).  The down product feeds the
-// fp32 combine only, where 4e-6 is far inside the output bound, so it accumulates the whole K in one buffer.
+// Arithmetic.  The int8 tensor rate of this part is far below its fp16 rate, so the contraction runs as
+// tcgen05.mma.kind::f16 on fp16 operands that carry the quantised values EXACTLY:
+//   - the weight operand is d_w * (q_w - 2), q_w in {0..3}: d_w times {-2, -1, 0, 1}, exact in fp16;
+//   - the row operand d * q (at most 18 significant bits) comes as two fp16 parts, hi = fp16_rn(d q) and
+//     lo = d q - hi (exact), written by the routed-row gather (activations) and by SwiGLU (H).
+// Every product of a weight and a part is exact in fp32, and the K loop runs two MMAs per 16-wide K step (A x hi,
+// A x lo).  The tensor core's fp32 accumulation aligns its addends with truncation, which over a whole row of K
+// costs about 3e-6 of the result -- enough to flip requantised H codes -- so for gate/up (whose output is
+// requantised) each 64-wide K slice accumulates from zero into one of two tensor-memory buffers (a small partial,
+// so a small truncation error) and the promoter warps add each finished partial into fp32 registers with
+// round-to-nearest while the tensor core fills the other buffer.  The down product feeds the fp32 combine only,
+// where 4e-6 is far inside the output bound, so it accumulates the whole K in one buffer, read once at the end.
 //
-// Tile: one CTA = one tile of the tile list (an expert and up to 256 of its routed rows, contiguous in routed-row
+// Data movement, chosen to keep the CUDA-core work per slice small (shared-memory traffic and the converters'
+// latency bounded the earlier designs):
+//   - both parts of the row operand are stored in HBM in operand order, so TMA loads them straight into the
+//     canonical K-major 128-byte-swizzled layout the MMA reads (no conversion pass through shared memory);
+//   - the weight operand (A) is decoded from the packed 2-bit block by the converter warps directly into TENSOR
+//     memory (tcgen05.st; lane = weight row, 32-bit column = a pair of K values) and the MMA reads it from there.
+//
+// Tile: one CTA = one tile of the tile list (an expert and up to 224 of its routed rows, contiguous in routed-row
 // order; the MMA's N, a multiple of 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB:
 // weights are the M operand so that a small expert wastes little).  Five warpgroups, registers rebalanced with
 // setmaxnreg:
-//   warpgroup 0   warp 0: tensor-memory allocation and, on one lane, the MMAs of each slice;
-//                 warp 1, one lane: the producer -- per 64-wide K slice one bulk copy of the packed weight block
-//                 (codes and scales) and TMA tile loads of the tile's q8 rows in slice form (codes and scales, 80
-//                 bytes a row, 16 rows a load), into a ring of up to 16 slices in shared memory;
-//   warpgroups 1-2  promoters: add each finished partial from tensor memory into fp32 registers (128 columns of
-//                 one TMEM lane a thread), then write the fp32 rows;
-//   warpgroups 3-4  converters: decode a ring slice into the fp16 operand tiles of one of two stages (K-major,
-//                 128-byte swizzle), 16 K values of one row per work item.
+//   warpgroup 0   warp 0: tensor-memory allocation and, on one lane, the MMAs (four K16 steps x two parts a slice);
+//                 warp 1, one lane: the producer -- per 64-wide K slice, TMA tile loads of the tile's rows of both
+//                 parts (16 rows x 128 bytes a load, 128-byte swizzle) and one bulk copy of the packed weight
+//                 block, into a ring slot;
+//   warpgroups 1-2  promoters: add each finished partial into fp32 registers (a TMEM lane a thread, alternate
+//                 16-column chunks a warpgroup), then write the fp32 rows;
+//   warpgroups 3-4  converters: thread = (weight row, 32-value half of the slice): decode its 32 weights into the
+//                 slice's A buffer in tensor memory.
+// Tensor memory (512 columns): 2 to 8 A buffers of 32 columns (more for small tiles, so that the converters run
+// further ahead), then 1 to 4 partial buffers of N columns rounded up to 32 (two for gate/up, which promotes every
+// slice; one suffices for down); two buffers of a full tile cap the tile at 224 rows.
 //
-// K order inside the operand tiles: within each group of 16 K values, shared-memory position 2m holds value m and
-// position 2m+1 holds value m+8 (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so
-// the contraction is unchanged.
+// Synchronisation: a satisfied mbarrier wait still costs a round trip of a few hundred cycles, so each role waits
+// as little as it can per slice -- the MMA thread only on "A of slice kt decoded" (the converters arrive on it after
+// they have seen the slice's copies land, so it also orders the TMA-written B tiles before the MMAs) and on a free
+// partial buffer when a partial starts.
+//
+// K order: within each group of 16 K values, operand position 2m holds value m and position 2m+1 value m+8
+// (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so the contraction is unchanged
+// and each 32-value half of a slice is two whole K16 steps.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -49,34 +61,34 @@ namespace {
 
 constexpr int kBM = 128;                       // weight rows per CTA (MMA M)
 constexpr int kBK = 64;                        // K values per slice: one 128-byte swizzle row of fp16
-constexpr int kMaxBN = SMOE_TILE_ROWS;         // routed rows per tile (MMA N <= 256)
-constexpr int kStages = 2;                     // fp16 operand stages
+constexpr int kMaxBN = SMOE_TILE_ROWS;         // routed rows per tile (MMA N <= 224)
 constexpr int kThreads = 640;                  // five warpgroups
 constexpr int kPromoters = 256;                // warpgroups 1-2
 constexpr int kConverters = 256;               // warpgroups 3-4
-constexpr int kATile = kBM * 128;              // 16 KB of fp16 weights
-constexpr int kBTile = kMaxBN * 128;           // 32 KB of fp16 activations (one of hi / lo)
-constexpr int kStage = kATile + 2 * kBTile;
-constexpr int kRingBytes = 65 * 1024;          // raw-data ring
 constexpr int kMaxRing = 16;                   // slices in flight at most
-constexpr uint32_t kTmemCols = 512;            // two fp32 partial buffers, 128 lanes x N <= 256 columns each
-// shared memory: [1 KB alignment slack][stages][ring][barriers]
-constexpr int kSmemBytes = 1024 + kStages * kStage + kRingBytes + 512;
-// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 24, the converters to
-// 40 and the promoters take 176: 128 x 24 + 256 x 40 + 256 x 176 = 58,368 <= 61,440.  Per SM sub-partition (one
-// warp of each warpgroup): 32 x (24 + 176 + 176 + 40 + 40) = 14,592 <= 16,384.
-constexpr int kRegsWg0 = 24;
-constexpr int kRegsConv = 40;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kACols = 32;                // one slice of A: 128 lanes x 64 fp16
+constexpr int kMaxA = 8;                       // A buffers at most
+constexpr int kMaxBufs = 4;                    // partial buffers at most
+constexpr int kSmemBytes = 232448;             // the per-CTA maximum (227 KB): [align slack][ring][barriers]
+constexpr int kBarBytes = 512;
+constexpr int kRingBytes = kSmemBytes - 1024 - kBarBytes;
+// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 32, the converters to
+// 48 and the promoters take 176: 128 x 32 + 256 x 48 + 256 x 176 = 61,440.  Per SM sub-partition (one warp of each
+// warpgroup): 32 x (32 + 176 + 176 + 48 + 48) = 15,360 <= 16,384.
+constexpr int kRegsWg0 = 32;
+constexpr int kRegsConv = 48;
 constexpr int kRegsProm = 176;
 static_assert(128 * kRegsWg0 + 256 * kRegsConv + 256 * kRegsProm <= 640 * 96, "register split exceeds the launch");
+static_assert(kMaxBN <= 224 && kMaxBN % 32 == 0, "two partial buffers and two A buffers must fit in tensor memory");
 
-// Raw slice layout in the ring (one 64-wide K slice of the tile): the packed weight block (codes [128][16 B], scales
-// [128][4 B]), then the tile's N rows in slice form (80 B a row: 64 codes, 2 scales, padding).  Every TMA
-// destination (the block, each 16-row box) is 128-byte aligned.
+// Ring slot (one 64-wide K slice of the tile): the tile's N rows of the hi part, then of the lo part (N x 128 bytes
+// each, 128-byte swizzle, 1024-aligned), then the packed weight block (codes [128][16 B], scales [128][4 B]); slots
+// are 1024-byte multiples.
 constexpr int kWBlock = 2560;
-constexpr int kRowPiece = 80;
-constexpr int kRowBox = 16;                    // rows per TMA box
-__host__ __device__ constexpr int raw_slice_bytes(int N) { return kWBlock + N * kRowPiece; }
+constexpr int kRowBox = 16;                    // B rows per TMA load
+__host__ __device__ constexpr int slot_bytes(int N) { return (2 * N * 128 + kWBlock + 1023) & ~1023; }
+static_assert(kRingBytes / slot_bytes(kMaxBN) >= 3, "the ring must hold three slices of a full tile");
 
 // bulk copy (no tensor map) of `bytes` (a multiple of 16) into shared memory, completing on `bar`
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -102,56 +114,54 @@ __device__ __forceinline__ void setmaxnreg_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// 16 weights of one row (codes: value i at bits 2i..2i+1) into chunks 2*quarter and 2*quarter + 1 of the row's
-// swizzled 128-byte line: d * (q - 2).
-__device__ __forceinline__ void decode_weights16(uint32_t codes, uint16_t scale, uint4* row_line, int row,
-                                                 int quarter) {
-    const __half2 d2 = __half2half2(__ushort_as_half(scale));
+// 16 consecutive 32-bit TMEM columns of 32 lanes: thread i of the warp gets / gives lane (base lane + i)
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, fp16 operands, fp32 accumulate; issued by one thread.
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// (a0, a1) += (p0, p1), each rounded to nearest (packed fp32x2 add)
+__device__ __forceinline__ void add2(float& a0, float& a1, uint32_t p0, uint32_t p1) {
+    asm("{\n\t.reg .b64 a, p;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 p, {%2, %3};\n\t"
+        "add.rn.f32x2 a, a, p;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(p0), "r"(p1));
+}
+
+// 16 weights (codes: value i at bits 2i..2i+1) as 8 TMEM columns of fp16 pairs (value m, value m+8): d * (q - 2)
+__device__ __forceinline__ void decode_weights16(uint32_t codes, __half2 d2, uint32_t* col) {
     const __half2 k1026 = __float2half2_rn(1026.0f);
-    uint32_t h[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
         // values m and m+8 as fp16 1024 + q in the two halves, then (1024 + q - 1026) * d = d * (q - 2)
         const uint32_t v = ((codes >> (2 * m)) & 0x00030003u) | 0x64006400u;
-        h[m] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(v), k1026), d2));
+        col[m] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(v), k1026), d2));
     }
-    row_line[(2 * quarter) ^ (row & 7)] = make_uint4(h[0], h[1], h[2], h[3]);
-    row_line[(2 * quarter + 1) ^ (row & 7)] = make_uint4(h[4], h[5], h[6], h[7]);
-}
-
-// 16 int8 activations of one row into the hi and lo tiles: hi = fp16_rn(d q), lo = d q - hi (exact).
-__device__ __forceinline__ void split_activations16(uint4 c, uint16_t scale, uint4* hi_line, uint4* lo_line, int row,
-                                                    int quarter) {
-    const __half2 d2 = __half2half2(__ushort_as_half(scale));
-    const __half2 k1152 = __float2half2_rn(1152.0f);
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-    uint32_t hi[8], lo[8];
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        // bytes of values m and m+8 into the low bytes of two halves; (b ^ 0x80) = b + 128 for a signed byte b, so
-        // the halves read 1024 + 128 + q
-        const uint32_t t = __byte_perm(w[m >> 2], w[2 + (m >> 2)], (m & 3) | ((4 + (m & 3)) << 8));
-        const uint32_t v = (t & 0x00FF00FFu) ^ 0x64806480u;
-        const __half2 q = __hsub2(u32_as_h2(v), k1152);
-        const __half2 ph = __hmul2(q, d2);
-        const __half2 pl = __hfma2(q, d2, __hneg2(ph));
-        hi[m] = h2_as_u32(ph);
-        lo[m] = h2_as_u32(pl);
-    }
-    const int c0 = (2 * quarter) ^ (row & 7), c1 = (2 * quarter + 1) ^ (row & 7);
-    hi_line[c0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    hi_line[c1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-    lo_line[c0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    lo_line[c1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
-}
-
-__device__ __forceinline__ void zero_activations16(uint4* hi_line, uint4* lo_line, int row, int quarter) {
-    const int c0 = (2 * quarter) ^ (row & 7), c1 = (2 * quarter + 1) ^ (row & 7);
-    hi_line[c0] = hi_line[c1] = lo_line[c0] = lo_line[c1] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 struct GemmMaps {
-    CUtensorMap b;  // q8 rows in slice form: [rows][K/64 * 80 bytes], box 80 bytes x 16 rows
+    CUtensorMap hi, lo;  // the two parts of the B rows: fp16 [b_rows][K] each, box 64 x 16, 128-byte swizzle
 };
 
 __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const ExpertsGemmArgs p,
@@ -165,40 +175,44 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     if (rows <= 0 || rows > kMaxBN || e < 0 || e >= p.n_experts || row0 < 0 || row0 + (int64_t)rows > p.b_rows) return;
     const int N = (rows + 15) & ~15;
     const int m0 = blockIdx.x * kBM;
-    const int nk = p.K / kBK;
-    const int P = p.two_level ? 1 : nk;  // slices per tensor-memory partial
+    const int nk = p.K / kBK;                // slices
+    const int P = p.two_level ? 1 : nk;      // slices per tensor-memory partial
+    const int groups = (nk + P - 1) / P;     // partials
+    // tensor memory: na A buffers, then nbuf partial buffers of bstride columns
+    const int bstride = (N + 31) & ~31;
+    const int need = (groups > 1 ? 2 : 1) * bstride;
+    const int na = max(2, min(kMaxA, ((int)kTmemCols - need) / (int)kACols));
+    const uint32_t part_base = (uint32_t)na * kACols;
+    const int nbuf = min(kMaxBufs, ((int)kTmemCols - (int)part_base) / bstride);
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-    uint8_t* smem = smem_raw + pad;
-    uint8_t* ring = smem + kStages * kStage;
-    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kRingBytes);  // operand stage s is filled
-    uint64_t* empty = full + kStages;      // ... and consumed by the MMAs
-    uint64_t* pfull = empty + kStages;     // a partial is complete in tensor-memory buffer b
-    uint64_t* pempty = pfull + 2;          // the promoters have added buffer b into their registers
-    uint64_t* rfull = pempty + 2;          // ring slot r holds its slice [kMaxRing]
-    uint64_t* rempty = rfull + kMaxRing;   // ring slot r has been read [kMaxRing]
-    uint64_t* accf = rempty + kMaxRing;    // every MMA has completed
+    uint8_t* ring = smem_raw + pad;
+    const int sbytes = slot_bytes(N);
+    const int depth = min(kMaxRing, kRingBytes / sbytes);
+    uint64_t* sfull = reinterpret_cast<uint64_t*>(smem_raw + kSmemBytes - kBarBytes);  // slot r holds slice [kMaxRing]
+    uint64_t* sempty = sfull + kMaxRing;    // the MMAs and the converters are done with slot r [kMaxRing]
+    uint64_t* afull = sempty + kMaxRing;    // A buffer a decoded (and its slot's copies landed) [kMaxA]
+    uint64_t* aempty = afull + kMaxA;       // the MMAs are done with A buffer a [kMaxA]
+    uint64_t* pfull = aempty + kMaxA;       // partial in tensor-memory buffer b is complete [kMaxBufs]
+    uint64_t* pempty = pfull + kMaxBufs;    // the promoters have added buffer b into their registers [kMaxBufs]
+    uint64_t* accf = pempty + kMaxBufs;     // every MMA has completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-    const int sbytes = raw_slice_bytes(N);
-    const int depth = min(kMaxRing, kRingBytes / sbytes);
-    const int o_as = 2048, o_b = kWBlock;  // weight scales, row pieces
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], kConverters);
-            mbar_init(&empty[s], 1);
+        for (int r = 0; r < kMaxRing; ++r) {
+            mbar_init(&sfull[r], 1);                 // the arrival that posts the slice's byte count
+            mbar_init(&sempty[r], 1 + kConverters);  // the MMAs' commit and every converter
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int a = 0; a < kMaxA; ++a) {
+            mbar_init(&afull[a], kConverters);
+            mbar_init(&aempty[a], 1);
+        }
+        for (int b = 0; b < kMaxBufs; ++b) {
             mbar_init(&pfull[b], 1);
             mbar_init(&pempty[b], kPromoters);
-        }
-        for (int r = 0; r < kMaxRing; ++r) {
-            mbar_init(&rfull[r], 1);  // the arrival that posts the slice's byte count
-            mbar_init(&rempty[r], kConverters);
         }
         mbar_init(accf, 1);
         *abort_flag = 0;
@@ -212,102 +226,134 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t sbase = smem_u32(smem);
+    const uint32_t ring_s = smem_u32(ring);
     bool ok = true;
 
     if (warp < 4) {
         setmaxnreg_dec<kRegsWg0>();
         if (warp == 0 && lane == 0) {
             // ------------------------------------------------------------------ MMA issue (one thread)
+            // slice kt: A buffer kt mod na, the slot's hi and lo tiles; partial g = kt / P in buffer g mod nbuf, from
+            // zero at its first slice
+            // ring / buffer positions advance by counting (a division by a runtime value costs tens of cycles on
+            // this single thread's critical path)
             const uint32_t idesc = idesc_f16_f32(kBM, N);
-            for (int kt = 0; kt < nk; ++kt) {
-                // slice kt of partial g = kt / P goes to buffer g & 1, which partial g - 2 has left
-                const int s = kt % kStages, g = kt / P, b = g & 1;
-                const bool first = kt % P == 0, last = kt % P == P - 1 || kt == nk - 1;
-                if (!mbar_wait(&full[s], (uint32_t)(kt / kStages) & 1u, abort_flag) ||
-                    (first && g >= 2 && !mbar_wait(&pempty[b], (uint32_t)(g / 2 - 1) & 1u, abort_flag))) {
+            int r = 0, ab = 0, b = 0, kp = 0, g = 0;
+            uint32_t aph = 0, bwrap = 0;
+            for (int kt = 0; kt < nk && ok; ++kt) {
+                const bool first = kp == 0, last = kp == P - 1 || kt == nk - 1;
+                if (!mbar_wait(&afull[ab], aph, abort_flag) ||
+                    (first && g >= nbuf && !mbar_wait(&pempty[b], (bwrap - 1u) & 1u, abort_flag))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a = sbase + s * kStage, bh = a + kATile, bl = bh + kBTile;
-                const uint32_t d = tmem + 256u * (uint32_t)b;
+                const uint32_t hi = ring_s + (uint32_t)(r * sbytes), lo = hi + (uint32_t)(N * 128);
+                const uint32_t d = tmem + part_base + (uint32_t)(b * bstride);
+                const uint32_t a = tmem + (uint32_t)ab * kACols;
 #pragma unroll
-                for (int j = 0; j < kBK / 16; ++j) {
-                    const uint64_t ad = sdesc_k_sw128(a + 32 * j);
-                    mma_f16(d, ad, sdesc_k_sw128(bh + 32 * j), idesc, (j > 0 || !first) ? 1u : 0u);
-                    mma_f16(d, ad, sdesc_k_sw128(bl + 32 * j), idesc, 1u);
+                for (int k16 = 0; k16 < 4; ++k16) {
+                    mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
+                               (first && k16 == 0) ? 0u : 1u);
+                    mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
                 }
-                mma_commit(&empty[s]);
+                mma_commit(&sempty[r]);
+                mma_commit(&aempty[ab]);
                 if (last) mma_commit(&pfull[b]);
+                if (++r == depth) r = 0;
+                if (++ab == na) {
+                    ab = 0;
+                    aph ^= 1u;
+                }
+                if (++kp == P) {
+                    kp = 0;
+                    ++g;
+                    if (++b == nbuf) {
+                        b = 0;
+                        ++bwrap;
+                    }
+                }
             }
             mma_commit(accf);  // completes once every MMA issued above has completed (abort path included)
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------------------------ producer (one thread)
             const uint8_t* wblocks = p.wp + ((int64_t)e * (p.a_rows / kBM) + blockIdx.x) * nk * (int64_t)kWBlock;
-            const uint32_t tx_bytes = (uint32_t)kWBlock + (uint32_t)N * kRowPiece;
-            int issued = 0;
+            const uint32_t tx_bytes = 2u * (uint32_t)N * 128u + (uint32_t)kWBlock;
+            int issued = 0, r = 0;
+            uint32_t eph = 0;  // parity of the sempty phase the next wrap waits for
             for (int kt = 0; kt < nk; ++kt, ++issued) {
-                const int r = kt % depth;
-                if (kt >= depth && !mbar_wait(&rempty[r], (uint32_t)(kt / depth - 1) & 1u, abort_flag)) {
+                if (kt >= depth && !mbar_wait(&sempty[r], eph, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t slot = smem_u32(ring) + (uint32_t)(r * sbytes);
-                mbar_arrive_expect_tx(&rfull[r], tx_bytes);
-                bulk_load(slot, wblocks + (int64_t)kt * kWBlock, kWBlock, &rfull[r]);
-                for (int b0 = 0; b0 < N; b0 += kRowBox)
-                    tma_load_2d(slot + o_b + b0 * kRowPiece, &maps.b, kt * kRowPiece, row0 + b0, &rfull[r]);
+                const uint32_t slot = ring_s + (uint32_t)(r * sbytes);
+                mbar_arrive_expect_tx(&sfull[r], tx_bytes);
+                bulk_load(slot + (uint32_t)(2 * N * 128), wblocks + (int64_t)kt * kWBlock, kWBlock, &sfull[r]);
+                for (int b0 = 0; b0 < N; b0 += kRowBox) {
+                    tma_load_2d(slot + (uint32_t)(b0 * 128), &maps.hi, kt * kBK, row0 + b0, &sfull[r]);
+                    tma_load_2d(slot + (uint32_t)((N + b0) * 128), &maps.lo, kt * kBK, row0 + b0, &sfull[r]);
+                }
+                if (++r == depth) {
+                    r = 0;
+                    if (kt >= depth) eph ^= 1u;
+                }
             }
-            // no copy may still be writing shared memory when the CTA exits (on the abort path the converters have
-            // not waited for the last slices): wait, bounded, for the last `depth` slices issued
+            // no copy may still be writing shared memory when the CTA exits (on the abort path nobody has waited
+            // for the last slices): wait, bounded, for the last `depth` slices issued
             for (int kt = max(0, issued - depth); kt < issued; ++kt)
-                mbar_wait(&rfull[kt % depth], (uint32_t)(kt / depth) & 1u, nullptr);
+                mbar_wait(&sfull[kt % depth], (uint32_t)(kt / depth) & 1u, nullptr);
         }
         __syncwarp();
     } else if (warp < 12) {
         setmaxnreg_inc<kRegsProm>();
         // ------------------------------------------------------------------ promoters (256 threads)
-        // this thread owns TMEM lane 32*q + lane (weight row mrow) and the 32-column chunks 2 i + chalf, i = 0..3
+        // this thread owns TMEM lane 32*q + lane (weight row mrow) and the 16-column chunks chalf + 2 i of the tile;
+        // the next chunk's load is in flight while the current one is added
         const int q = warp & 3;
         const int chalf = (warp - 4) >> 2;  // warpgroup 1: even chunks; warpgroup 2: odd chunks
         const int mrow = 32 * q + lane;
-        float acc[4][32];
+        const int mine = (N / 16 - chalf + 1) / 2;  // chunks of this thread
+        constexpr int kChunks = kMaxBN / 32;        // most chunks of a thread
+        float acc[kChunks][16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < kChunks; ++i)
 #pragma unroll
-            for (int k = 0; k < 32; ++k) acc[i][k] = 0.0f;
-        const int groups = (nk + P - 1) / P;
+            for (int k = 0; k < 16; ++k) acc[i][k] = 0.0f;
+        int b = 0;
+        uint32_t bph = 0;
         for (int g = 0; g < groups && ok; ++g) {
-            const int b = g & 1;
-            if (!mbar_wait(&pfull[b], (uint32_t)(g / 2) & 1u, abort_flag)) {
+            if (!mbar_wait(&pfull[b], bph, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + 256u * (uint32_t)b;
+            const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + part_base + (uint32_t)(b * bstride);
+            uint32_t v[2][16];
+            if (mine > 0) tmem_ld_32x32b_x16(base + (uint32_t)(16 * chalf), v[0]);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int c0 = 32 * (2 * i + chalf);
-                if (c0 < N) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(base + (uint32_t)c0, v);
+            for (int i = 0; i < kChunks; ++i) {
+                if (i < mine) {
                     tmem_ld_wait();
+                    if (i + 1 < mine) tmem_ld_32x32b_x16(base + (uint32_t)(16 * (chalf + 2 * (i + 1))), v[(i + 1) & 1]);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) acc[i][k] += __uint_as_float(v[k]);
+                    for (int k = 0; k < 16; k += 2) add2(acc[i][k], acc[i][k + 1], v[i & 1][k], v[i & 1][k + 1]);
                 }
             }
             tc_fence_before();
             mbar_arrive(&pempty[b]);
+            if (++b == nbuf) {
+                b = 0;
+                bph ^= 1u;
+            }
         }
         if (ok) {
             // ------------------------------------------------------------------ epilogue: fp32 rows out
             float* outcol = p.out + (m0 + mrow);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < kChunks; ++i) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int col = 32 * (2 * i + chalf) + k;
+                for (int k = 0; k < 16; ++k) {
+                    const int col = 16 * (chalf + 2 * i) + k;
                     if (col < rows) outcol[(int64_t)(row0 + col) * p.a_rows] = acc[i][k];
                 }
             }
@@ -315,46 +361,36 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     } else {
         setmaxnreg_dec<kRegsConv>();
         // ------------------------------------------------------------------ converters (256 threads)
-        // work items of 16 K values: weight items ct and ct + 256 (row = item / 4, quarter = item % 4); row items
-        // ct + 256 i of the tile's 4 N (row, quarter) pairs
+        // thread = (row ct % 128 = TMEM lane of its warp, half h = ct / 128 of each slice): 32 weights a slice
         const int ct = threadIdx.x - 384;
-        const int nb = (4 * N - ct + 255) / 256;  // row items of this thread (0..4)
+        const int row = ct & 127, h = ct >> 7;
+        const uint32_t lane_base = (uint32_t)(row & ~31) << 16;
+        int r = 0, ab = 0;
+        uint32_t rph = 0, aph = 0;  // sfull phase parity; aempty parity of the previous use of buffer ab
         for (int kt = 0; kt < nk && ok; ++kt) {
-            const int r = kt % depth, s = kt % kStages;
-            if (!mbar_wait(&rfull[r], (uint32_t)(kt / depth) & 1u, abort_flag) ||
-                (kt >= kStages && !mbar_wait(&empty[s], (uint32_t)(kt / kStages - 1) & 1u, abort_flag))) {
+            if (!mbar_wait(&sfull[r], rph, abort_flag) || (kt >= na && !mbar_wait(&aempty[ab], aph, abort_flag))) {
                 ok = false;
                 break;
             }
-            const uint8_t* slot = ring + r * sbytes;
-            uint8_t* st = smem + s * kStage;
-            uint4* a_tile = reinterpret_cast<uint4*>(st);
-            uint4* hi_tile = reinterpret_cast<uint4*>(st + kATile);
-            uint4* lo_tile = reinterpret_cast<uint4*>(st + kATile + kBTile);
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
-                const uint32_t code = *reinterpret_cast<const uint32_t*>(slot + row * 16 + qu * 4);
-                const uint16_t scale = *reinterpret_cast<const uint16_t*>(slot + o_as + row * 4 + (qu >> 1) * 2);
-                decode_weights16(code, scale, a_tile + row * 8, row, qu);
+            const uint8_t* wb = ring + r * sbytes + 2 * N * 128;
+            const uint2 codes = *reinterpret_cast<const uint2*>(wb + row * 16 + h * 8);
+            const __half2 d2 = __half2half2(*reinterpret_cast<const __half*>(wb + 2048 + row * 4 + h * 2));
+            uint32_t col[16];
+            decode_weights16(codes.x, d2, col);
+            decode_weights16(codes.y, d2, col + 8);
+            tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols + 16u * (uint32_t)h, col);
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&afull[ab]);
+            mbar_arrive(&sempty[r]);
+            if (++r == depth) {
+                r = 0;
+                rph ^= 1u;
             }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int item = ct + 256 * i, row = item >> 2, qu = item & 3;
-                if (i < nb) {
-                    if (row < rows) {
-                        const uint8_t* piece = slot + o_b + row * kRowPiece;
-                        const uint4 code = *reinterpret_cast<const uint4*>(piece + qu * 16);
-                        const uint16_t scale = *reinterpret_cast<const uint16_t*>(piece + 64 + (qu >> 1) * 2);
-                        split_activations16(code, scale, hi_tile + row * 8, lo_tile + row * 8, row, qu);
-                    } else {
-                        zero_activations16(hi_tile + row * 8, lo_tile + row * 8, row, qu);
-                    }
-                }
+            if (++ab == na) {
+                ab = 0;
+                if (kt >= na) aph ^= 1u;
             }
-            mbar_arrive(&rempty[r]);
-            fence_async_smem();
-            mbar_arrive(&full[s]);
         }
     }
     if (!ok) {
@@ -364,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
-        mbar_wait(accf, 0, nullptr);  // every MMA has completed before the accumulator is released
+        mbar_wait(accf, 0, nullptr);  // every MMA has completed before the tensor memory is released
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -387,17 +423,17 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// 2D uint8 tensor [rows][row_bytes] (row stride row_bytes), box box_x bytes x box_y rows, no swizzle
-bool make_map(CUtensorMap* map, const void* base, uint64_t row_bytes, uint64_t rows, uint32_t box_x, uint32_t box_y) {
+// 2D tensor [rows][cols] of `esize`-byte elements (row stride cols * esize), box box_x x box_y elements
+bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint32_t esize, uint64_t cols,
+              uint64_t rows, uint32_t box_x, uint32_t box_y, CUtensorMapSwizzle swizzle) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {row_bytes, rows};
-    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * esize};
     const cuuint32_t box[2] = {box_x, box_y};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -414,7 +450,11 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     }
     if (max_tiles <= 0) return cudaSuccess;
     GemmMaps maps;
-    if (!make_map(&maps.b, a.bsl, (uint64_t)(a.K / kBK) * kRowPiece, (uint64_t)a.b_rows, kRowPiece, kRowBox))
+    const uint16_t* lo = a.bop + a.b_rows * (int64_t)a.K;
+    if (!make_map(&maps.hi, a.bop, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
+                  kRowBox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&maps.lo, lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK, kRowBox,
+                  CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const dim3 grid((unsigned)(a.a_rows / kBM), (unsigned)max_tiles);
     experts_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, maps);

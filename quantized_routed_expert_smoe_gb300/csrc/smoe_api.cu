@@ -92,18 +92,13 @@ smoe_status smoe_group(const int32_t* ids, int64_t T, int K, int E, int32_t* cou
                                             reinterpret_cast<int32_t*>(work), (cudaStream_t)stream));
 }
 
-smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales,
-                             uint8_t* slices, void* stream) {
+smoe_status smoe_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales, void* stream) {
     if (rows < 0 || cols < 32 || cols % 32 != 0) return SMOE_ERR_ARG;
-    if (slices != nullptr && cols % 64 != 0) return SMOE_ERR_ARG;
     if (rows == 0) return SMOE_OK;
     if (!aligned16(x) || !aligned16(codes) || !aligned16(scales)) return SMOE_ERR_ARG;
-    if (slices != nullptr && !aligned16(slices)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    return launch_status(smoe::launch_quantize_q8(x, rows, cols, codes, scales, slices, (cudaStream_t)stream));
+    return launch_status(smoe::launch_quantize_q8(x, rows, cols, codes, scales, (cudaStream_t)stream));
 }
-
-size_t smoe_slices_bytes(int64_t rows, int cols) { return rows <= 0 || cols <= 0 ? 0 : (size_t)rows * (cols / 64) * 80; }
 
 size_t smoe_pack_q2_bytes(int E, int rows, int cols) {
     return E <= 0 || rows <= 0 || cols <= 0 ? 0 : (size_t)E * rows * (cols / 4 + cols / 16);
@@ -126,46 +121,46 @@ static smoe_status check_gemm_shape(int64_t n, int E, int H, int F) {
     return SMOE_OK;
 }
 
-smoe_status smoe_gather_slices(const uint8_t* slices, int64_t in_rows, int cols, const int32_t* src, int64_t n,
-                               uint8_t* out, void* stream) {
-    if (in_rows < 0 || n < 0 || cols < 64 || cols % 64 != 0) return SMOE_ERR_ARG;
+smoe_status smoe_gather_q8(const int8_t* codes, const uint16_t* scales, int64_t in_rows, int cols, const int32_t* src,
+                           int64_t n, uint16_t* out, void* stream) {
+    if (in_rows < 0 || n < 0 || cols < 32 || cols % 32 != 0) return SMOE_ERR_ARG;
     if (n == 0) return SMOE_OK;
     if (in_rows < 1 || n > INT32_MAX) return SMOE_ERR_ARG;
-    if (!aligned16(slices) || !aligned16(src) || !aligned16(out)) return SMOE_ERR_ARG;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(src) || !aligned16(out)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    return launch_status(smoe::launch_gather_slices(slices, in_rows, cols, src, n, out, (cudaStream_t)stream));
+    return launch_status(smoe::launch_gather_q8(codes, scales, in_rows, cols, src, n, out, (cudaStream_t)stream));
 }
 
-smoe_status smoe_experts_gateup(const uint8_t* xsl, int32_t* tiles, int64_t n, int E, const uint8_t* wgu, int H, int F,
+smoe_status smoe_experts_gateup(const uint16_t* xop, int32_t* tiles, int64_t n, int E, const uint8_t* wgu, int H, int F,
                                 float* gu, void* stream) {
     const smoe_status st = check_gemm_shape(n, E, H, F);
     if (st != SMOE_OK) return st;
     if (n == 0) return SMOE_OK;
-    if (!aligned16(xsl) || !aligned16(tiles) || !aligned16(wgu) || !aligned16(gu)) return SMOE_ERR_ARG;
+    if (!aligned16(xop) || !aligned16(tiles) || !aligned16(wgu) || !aligned16(gu)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{xsl, tiles, wgu, 2 * F, H, gu, n, E, true};
+    smoe::ExpertsGemmArgs a{xop, tiles, wgu, 2 * F, H, gu, n, E, true};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 
-smoe_status smoe_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint8_t* slices,
+smoe_status smoe_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint16_t* hop,
                                 void* stream) {
     if (n < 0 || F < 32 || F % 32 != 0) return SMOE_ERR_ARG;
-    if (slices != nullptr && F % 64 != 0) return SMOE_ERR_ARG;
+    if (hop != nullptr && F % 64 != 0) return SMOE_ERR_ARG;
     if (n == 0) return SMOE_OK;
     if (!aligned16(gu) || !aligned16(hc) || !aligned16(hs)) return SMOE_ERR_ARG;
-    if (slices != nullptr && !aligned16(slices)) return SMOE_ERR_ARG;
+    if (hop != nullptr && !aligned16(hop)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    return launch_status(smoe::launch_swiglu_requant(gu, n, F, hc, hs, slices, (cudaStream_t)stream));
+    return launch_status(smoe::launch_swiglu_requant(gu, n, F, hc, hs, hop, (cudaStream_t)stream));
 }
 
-smoe_status smoe_experts_down(const uint8_t* hsl, int32_t* tiles, int64_t n, int E, const uint8_t* wd, int H, int F,
+smoe_status smoe_experts_down(const uint16_t* hop, int32_t* tiles, int64_t n, int E, const uint8_t* wd, int H, int F,
                               float* dm, void* stream) {
     const smoe_status st = check_gemm_shape(n, E, H, F);
     if (st != SMOE_OK) return st;
     if (n == 0) return SMOE_OK;
-    if (!aligned16(hsl) || !aligned16(tiles) || !aligned16(wd) || !aligned16(dm)) return SMOE_ERR_ARG;
+    if (!aligned16(hop) || !aligned16(tiles) || !aligned16(wd) || !aligned16(dm)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{hsl, tiles, wd, H, F, dm, n, E, false};
+    smoe::ExpertsGemmArgs a{hop, tiles, wd, H, F, dm, n, E, false};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 

@@ -14,29 +14,29 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int K, int3
 cudaError_t launch_group(const int32_t* ids, int64_t n, int K, int E, int32_t* counts, int32_t* offsets,
                          int32_t* src, int32_t* slot, int32_t* tiles, int32_t* hist, cudaStream_t s);
 cudaError_t launch_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales,
-                               uint8_t* slices, cudaStream_t s);
-cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint8_t* slices,
+                               cudaStream_t s);
+cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint16_t* hop,
                                   cudaStream_t s);
 cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, uint8_t* packed,
                            cudaStream_t s);
-cudaError_t launch_gather_slices(const uint8_t* slices, int64_t in_rows, int cols, const int32_t* src, int64_t n,
-                                 uint8_t* out, cudaStream_t s);
+cudaError_t launch_gather_q8(const int8_t* codes, const uint16_t* scales, int64_t in_rows, int cols,
+                             const int32_t* src, int64_t n, uint16_t* out, cudaStream_t s);
 cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
                            cudaStream_t s);
 
 // Grouped expert product (both the gate/up and the down step): for every tile of the tile list and every 128-row
-// slice of the expert's weight matrix, OUT[row][j] = sum over K of W[e][j] . B[row], W the 2-bit weights and B the
-// q8 rows in routed-row order.
+// slice of the expert's weight matrix, OUT[row][j] = sum over K of W[e][j][i] * B[row][i], W the decoded 2-bit
+// weights and B = d q the q8 rows, given as the exact fp16 split hi + lo.
 struct ExpertsGemmArgs {
-    const uint8_t* bsl;   // q8 B rows in slice form, routed-row order, [n][K/64][80 bytes]
+    const uint16_t* bop;  // B rows in operand form: fp16 planes [2][b_rows][K] (hi, then lo), routed-row order
     int32_t* tiles;       // tile list; header[3] receives SMOE_ERR_TIMEOUT
     const uint8_t* wp;    // packed weights: per (expert, 128-row tile, 64-value slice) 2560 bytes
     int a_rows;           // weight rows per expert (2F or H)
     int K;                // contraction length (H or F)
-    float* out;           // [n][a_rows]
-    int64_t b_rows;       // rows of the q8 B matrix (n)
+    float* out;           // [b_rows][a_rows]
+    int64_t b_rows;       // n
     int n_experts;        // E
-    bool two_level;       // promote every 64-wide K slice into fp32 registers (gate/up); else one accumulator
+    bool two_level;       // add every 64-wide K slice into fp32 registers (gate/up); else one accumulator over K
 };
 cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s);
 

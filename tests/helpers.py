@@ -19,14 +19,18 @@ def i16(a):
     return np.ascontiguousarray(a).view(np.int16)
 
 
-def to_slices(codes, scales):
-    """q8 rows in the expert products' slice form: per row and per 64 values, the 64 codes, the two fp16 scales of
-    the slice's 32-value blocks (little-endian), 12 zero bytes -> uint8 [rows][cols/64][80]."""
+def to_operand(codes, scales):
+    """q8 rows [rows][cols] + fp16 scales [rows][cols/32] in the expert products' operand form: hi = fp16(d q),
+    lo = d q - hi (both exact from float64), and within each group of 16 values position 2j holds value j and 2j+1
+    value j+8 -> float16 [2][rows][cols]."""
     rows, cols = codes.shape
-    out = np.zeros((rows, cols // 64, 80), np.uint8)
-    out[:, :, :64] = np.ascontiguousarray(codes).view(np.uint8).reshape(rows, cols // 64, 64)
-    out[:, :, 64:68] = np.ascontiguousarray(scales).view(np.uint8).reshape(rows, cols // 64, 4)
-    return out
+    v = np.asarray(codes).astype(np.float64) * np.repeat(np.asarray(scales).view(np.float16).astype(np.float64), 32,
+                                                         axis=1)
+    hi = v.astype(np.float16)
+    lo = (v - hi.astype(np.float64)).astype(np.float16)
+    assert np.array_equal(hi.astype(np.float64) + lo.astype(np.float64), v), "the hi/lo split must be exact"
+    perm = lambda a: np.ascontiguousarray(a.reshape(rows, cols // 16, 2, 8).transpose(0, 1, 3, 2)).reshape(rows, cols)
+    return np.stack([perm(hi), perm(lo)])
 
 
 def packed_q2(codes, scales):

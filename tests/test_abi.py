@@ -27,7 +27,7 @@ def declared_functions():
 
 def test_header_declares_the_seven_steps():
     names = declared_functions()
-    for step in ["smoe_route_topk", "smoe_group", "smoe_quantize_q8", "smoe_gather_slices", "smoe_experts_gateup",
+    for step in ["smoe_route_topk", "smoe_group", "smoe_quantize_q8", "smoe_gather_q8", "smoe_experts_gateup",
                  "smoe_swiglu_requant", "smoe_experts_down", "smoe_combine"]:
         assert step in names
 
@@ -42,12 +42,11 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_sizing_helpers(lib):
     from quantized_routed_expert_smoe_gb300 import binding
-    assert binding.max_tiles(81920, 512) == 320 + 512
+    assert binding.max_tiles(81920, 512) == (81920 + 223) // 224 + 512
     assert binding.max_tiles(128, 16) == 1 + 16
     assert binding.max_tiles(0, 16) == 0
     assert binding.tiles_bytes(128, 16) == 16 * 18
     assert binding.group_work_bytes(81920, 512) >= 512 * 4
-    assert binding.slices_bytes(3, 256) == 3 * 4 * 80
     assert binding.pack_q2_bytes(2, 128, 64) == 2 * 128 * (16 + 4)
 
 
@@ -63,14 +62,17 @@ def test_host_side_rejections_need_no_gpu(lib):
     assert lib.smoe_route_topk(odd, 4, 16, 2, fake, fake, null) == ARG
     assert lib.smoe_route_topk(fake, 0, 16, 2, fake, fake, null) == 0  # empty chunk: nothing to do
     # q8: cols not a multiple of 32
-    assert lib.smoe_quantize_q8(fake, 4, 48, fake, fake, null, null) == ARG
-    assert lib.smoe_quantize_q8(fake, 4, 96, fake, fake, fake, null) == ARG  # slice form needs cols % 64 == 0
+    assert lib.smoe_quantize_q8(fake, 4, 48, fake, fake, null) == ARG
     # gemm shapes the kernels do not cover
     assert lib.smoe_experts_gateup(fake, fake, 10, 4, fake, 96, 64, fake, null) == UNSUP
-    # gather: cols not a multiple of 64, misaligned output
-    assert lib.smoe_gather_slices(fake, 4, 96, fake, 8, fake, null) == ARG
-    assert lib.smoe_gather_slices(fake, 4, 128, fake, 8, odd, null) == ARG
-    assert lib.smoe_gather_slices(fake, 4, 128, fake, 0, fake, null) == 0  # nothing routed: nothing to do
+    assert lib.smoe_experts_down(odd, fake, 10, 4, fake, 256, 64, fake, null) == ARG  # misaligned rows
+    # gather: cols not a multiple of 32, misaligned scales or output
+    assert lib.smoe_gather_q8(fake, fake, 4, 48, fake, 8, fake, null) == ARG
+    assert lib.smoe_gather_q8(fake, odd, 4, 128, fake, 8, fake, null) == ARG
+    assert lib.smoe_gather_q8(fake, fake, 4, 128, fake, 8, odd, null) == ARG
+    assert lib.smoe_gather_q8(fake, fake, 4, 128, fake, 0, fake, null) == 0  # nothing routed: nothing to do
+    # SwiGLU: the operand form needs F % 64 == 0
+    assert lib.smoe_swiglu_requant(fake, 4, 96, fake, fake, fake, null) == ARG
     assert lib.smoe_experts_down(fake, fake, 10, 4, fake, 256, 48, fake, null) == UNSUP
     assert lib.smoe_pack_q2(fake, fake, 2, 100, 64, fake, null) == ARG  # rows % 128
     # group: tiles buffer too small

@@ -19,7 +19,7 @@ import scipy.special
 import oracle
 from quantized_routed_expert_smoe_gb300 import synth
 
-from helpers import deq_a, deq_w, i16, packed_q2, to_slices
+from helpers import deq_a, deq_w, i16, packed_q2, to_operand
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -155,23 +155,19 @@ def test_group_edge_cases(B):
 
 
 # ------------------------------------------------------------------------------------------------ q8
-def gpu_q8(B, x, with_slices=False):
+def gpu_q8(B, x):
     rows, cols = x.shape
     codes = torch.empty(rows, cols, dtype=torch.int8, device="cuda")
     scales = torch.empty(rows, cols // 32, dtype=torch.int16, device="cuda")
-    slices = torch.full((B.slices_bytes(rows, cols),), 0xAB, dtype=torch.uint8, device="cuda") if with_slices else None
-    B.smoe_quantize_q8(dev(x), codes, scales, slices)
-    if with_slices:
-        return host(codes), host(scales).view(np.uint16), host(slices).reshape(rows, cols // 64, 80)
+    B.smoe_quantize_q8(dev(x), codes, scales)
     return host(codes), host(scales).view(np.uint16)
 
 
 def test_quantize_bit_exact_full_and_edges(B):
     x = layer_inputs("t8192")["x"]
-    c, s, sl = gpu_q8(B, x, with_slices=True)
+    c, s = gpu_q8(B, x)
     co, so = oracle.quantize_q8(x)
     assert np.array_equal(c, co) and np.array_equal(s, so)
-    assert np.array_equal(sl, to_slices(co, so))
     # edge blocks: zeros, exact .5 ties at d = 1, subnormal and zero-rounding scales, clamping, huge values
     rng = np.random.default_rng(1)
     e = rng.standard_normal((9, 64)).astype(np.float32)
@@ -196,29 +192,39 @@ def test_quantize_bit_exact_full_and_edges(B):
     assert np.array_equal(c, co) and np.array_equal(s, so)
 
 
-def test_gather_slices_routed_rows(B):
-    """Routed-row order of the q8 slice form: byte for byte the source row, for the full t8192 grouping (ragged
-    per-expert counts) and for hand-made src lists (repeats, out-of-range entries give zero rows, a single row)."""
+def test_gather_q8_operand_form(B):
+    """Routed-row order in operand form: each output row is the source row's d * q split exactly into fp16 hi + lo
+    in the pair order, for the full t8192 grouping (ragged per-expert counts) and for hand-made src lists (repeats,
+    out-of-range entries give zero rows, a single row); extreme codes (-128..127) and subnormal, zero and large
+    scales pass exactly."""
     inp = layer_inputs("t8192")
     cfg = synth.CONFIGS["t8192"]
     ids, _ = oracle.route(inp["logits"], cfg.K)
     g = oracle.group(ids, cfg.E)
     co, so = oracle.quantize_q8(inp["x"])
-    sl = to_slices(co, so)
     n = cfg.T * cfg.K
-    out = torch.full((B.slices_bytes(n, cfg.H),), 0xCD, dtype=torch.uint8, device="cuda")
-    B.smoe_gather_slices(dev(sl.reshape(-1)), cfg.T, cfg.H, dev(g["src"]), out)
-    assert np.array_equal(host(out).reshape(n, -1, 80), sl[g["src"].astype(np.int64)])
+    out = torch.full((2, n, cfg.H), float("nan"), dtype=torch.float16, device="cuda")
+    B.smoe_gather_q8(dev(co), dev(i16(so)), dev(g["src"]), out)
+    src = g["src"].astype(np.int64)
+    assert np.array_equal(host(out), to_operand(co[src], so[src]))
     rng = np.random.default_rng(5)
-    rows, cols = 7, 192
-    raw = rng.integers(0, 256, size=(rows, cols // 64, 80), dtype=np.uint8)
-    for src in (np.array([3, 3, 0, 6, -1, 7, 2, 1 << 30, 5], np.int32), np.array([4], np.int32)):
-        out = torch.full((B.slices_bytes(len(src), cols),), 0xCD, dtype=torch.uint8, device="cuda")
-        B.smoe_gather_slices(dev(raw.reshape(-1)), rows, cols, dev(src), out)
-        want = np.zeros((len(src), cols // 64, 80), np.uint8)
-        ok = (src >= 0) & (src < rows)
-        want[ok] = raw[src[ok]]
-        assert np.array_equal(host(out).reshape(len(src), cols // 64, 80), want)
+    rows, cols = 7, 96
+    raw = rng.integers(-128, 128, size=(rows, cols), dtype=np.int8)
+    raw[0, :48] = np.arange(-128, -80)
+    raw[1, :48] = np.arange(80, 128)
+    sc = rng.uniform(0.001, 0.05, size=(rows, cols // 32)).astype(np.float16)
+    sc[0, 0] = np.float16(6e-8)      # subnormal scale
+    sc[1, 1] = np.float16(0.0)
+    sc[2, 2] = np.float16(500.0)     # 127 * 500 still below the fp16 maximum
+    for s_ in (np.array([3, 3, 0, 6, -1, 7, 2, 1 << 30, 5, 1], np.int32), np.array([4], np.int32)):
+        out = torch.full((2, len(s_), cols), float("nan"), dtype=torch.float16, device="cuda")
+        B.smoe_gather_q8(dev(raw), dev(i16(sc.view(np.uint16))), dev(s_), out)
+        okr = (s_ >= 0) & (s_ < rows)
+        wc = np.zeros((len(s_), cols), np.int8)
+        ws = np.zeros((len(s_), cols // 32), np.float16)
+        wc[okr] = raw[s_[okr]]
+        ws[okr] = sc[s_[okr]]
+        assert np.array_equal(host(out), to_operand(wc, ws.view(np.uint16)))
 
 
 # ------------------------------------------------------------------------------------------------ expert products
@@ -231,15 +237,15 @@ def _tiles_dev(B, g, n, E):
 
 
 def gpu_gateup(B, xc, xs, g, wgu_c, wgu_s, n, E):
-    """gate/up through the C ABI: the oracle's q8 rows in routed-row order and slice form, the weights packed by the
-    library."""
+    """gate/up through the C ABI: the oracle's q8 codes in routed-row order and operand form with the per-token
+    scales, the weights packed by the library."""
     tiles = _tiles_dev(B, g, n, E)
     T, H = xc.shape
     F = wgu_c.shape[1] // 2
     gu = torch.full((n, 2 * F), float("nan"), dtype=torch.float32, device="cuda")
     wp = B.pack_weights(wgu_c, wgu_s)
     src = g["src"].astype(np.int64)
-    B.smoe_experts_gateup(dev(to_slices(xc[src], xs[src])), tiles, n, E, wp, H, F, gu)
+    B.smoe_experts_gateup(dev(to_operand(xc[src], xs[src])), tiles, n, E, wp, H, F, gu)
     t = host(tiles)
     assert t[3] == 0, "kernel reported a timeout"
     return gu
@@ -251,7 +257,7 @@ def gpu_down(B, hc, hs, g, wd_c, wd_s, n, E):
     F = hc.shape[1]
     dm = torch.full((n, H), float("nan"), dtype=torch.float32, device="cuda")
     wp = B.pack_weights(wd_c, wd_s)
-    B.smoe_experts_down(dev(to_slices(hc, hs)), tiles, n, E, wp, H, F, dm)
+    B.smoe_experts_down(dev(to_operand(hc, hs)), tiles, n, E, wp, H, F, dm)
     assert host(tiles)[3] == 0
     return dm
 
@@ -384,10 +390,10 @@ def test_swiglu_requant_parity(B):
     gu = synth.make_gu(n, F, seed=11, scale=2.0)
     hc = torch.empty(n, F, dtype=torch.int8, device="cuda")
     hs = torch.empty(n, F // 32, dtype=torch.int16, device="cuda")
-    hsl = torch.full((B.slices_bytes(n, F),), 0xAB, dtype=torch.uint8, device="cuda")
-    B.smoe_swiglu_requant(dev(gu), hc, hs, hsl)
+    hop = torch.full((2, n, F), float("nan"), dtype=torch.float16, device="cuda")
+    B.smoe_swiglu_requant(dev(gu), hc, hs, hop)
     c, s = host(hc), host(hs).view(np.uint16)
-    assert np.array_equal(host(hsl).reshape(n, F // 64, 80), to_slices(c, s))
+    assert np.array_equal(host(hop), to_operand(c, s))
     co, so = oracle.swiglu_requant(gu, F)
     g = gu[:, :F].astype(np.float64)
     u = gu[:, F:].astype(np.float64)
