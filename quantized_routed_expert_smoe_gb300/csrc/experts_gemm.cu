@@ -38,8 +38,9 @@
 //   warpgroups 3-4  converters: thread = (weight row, 32-value half of the slice): decode its 32 weights into the
 //                 slice's A buffer in tensor memory.
 // Tensor memory (512 columns): 2 to 8 A buffers of 32 columns (more for small tiles, so that the converters run
-// further ahead), then 1 to 4 partial buffers of N columns rounded up to 32 (two for gate/up, which promotes every
-// slice; one suffices for down); two buffers of a full tile cap the tile at 224 rows.
+// further ahead), then 1 to 4 partial buffers of N columns rounded up to 32 (2N for a tile of at most 96 rows, which
+// stacks its hi and lo rows into one MMA; two buffers for gate/up, which promotes every slice; one suffices for
+// down); two buffers of a full tile cap the tile at 224 rows.
 //
 // Synchronisation: a satisfied mbarrier wait still costs a round trip of a few hundred cycles, so each role waits
 // as little as it can per slice -- the MMA thread only on "A of slice kt decoded" (the converters arrive on it after
@@ -70,6 +71,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACols = 32;                // one slice of A: 128 lanes x 64 fp16
 constexpr int kMaxA = 8;                       // A buffers at most
 constexpr int kMaxBufs = 4;                    // partial buffers at most
+constexpr int kMaxStackN = 96;                 // tiles up to this N stack hi and lo rows into one MMA
 constexpr int kSmemBytes = 232448;             // the per-CTA maximum (227 KB): [align slack][ring][barriers]
 constexpr int kBarBytes = 512;
 constexpr int kRingBytes = kSmemBytes - 1024 - kBarBytes;
@@ -178,8 +180,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const int nk = p.K / kBK;                // slices
     const int P = p.two_level ? 1 : nk;      // slices per tensor-memory partial
     const int groups = (nk + P - 1) / P;     // partials
+    // a small tile stacks its hi and lo rows (contiguous in the slot) into one MMA of 2N columns: an MMA costs about
+    // the same for any N up to 64, so this halves the MMAs where they are cheapest per row; the partial then holds
+    // the hi product in columns [0, N) and the lo product in [N, 2N)
+    const bool stacked = N <= kMaxStackN;
+    const int ncols = stacked ? 2 * N : N;   // partial columns
     // tensor memory: na A buffers, then nbuf partial buffers of bstride columns
-    const int bstride = (N + 31) & ~31;
+    const int bstride = (ncols + 31) & ~31;
     const int need = (groups > 1 ? 2 : 1) * bstride;
     const int na = max(2, min(kMaxA, ((int)kTmemCols - need) / (int)kACols));
     const uint32_t part_base = (uint32_t)na * kACols;
@@ -237,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             // zero at its first slice
             // ring / buffer positions advance by counting (a division by a runtime value costs tens of cycles on
             // this single thread's critical path)
-            const uint32_t idesc = idesc_f16_f32(kBM, N);
+            const uint32_t idesc = idesc_f16_f32(kBM, ncols);
             int r = 0, ab = 0, b = 0, kp = 0, g = 0;
             uint32_t aph = 0, bwrap = 0;
             for (int kt = 0; kt < nk && ok; ++kt) {
@@ -251,11 +258,18 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 const uint32_t hi = ring_s + (uint32_t)(r * sbytes), lo = hi + (uint32_t)(N * 128);
                 const uint32_t d = tmem + part_base + (uint32_t)(b * bstride);
                 const uint32_t a = tmem + (uint32_t)ab * kACols;
+                if (stacked) {
 #pragma unroll
-                for (int k16 = 0; k16 < 4; ++k16) {
-                    mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
-                               (first && k16 == 0) ? 0u : 1u);
-                    mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
+                    for (int k16 = 0; k16 < 4; ++k16)
+                        mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
+                                   (first && k16 == 0) ? 0u : 1u);
+                } else {
+#pragma unroll
+                    for (int k16 = 0; k16 < 4; ++k16) {
+                        mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
+                                   (first && k16 == 0) ? 0u : 1u);
+                        mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
+                    }
                 }
                 mma_commit(&sempty[r]);
                 mma_commit(&aempty[ab]);
@@ -329,14 +343,33 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             tc_fence_after();
             const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + part_base + (uint32_t)(b * bstride);
             uint32_t v[2][16];
-            if (mine > 0) tmem_ld_32x32b_x16(base + (uint32_t)(16 * chalf), v[0]);
+            if (stacked) {
+                // hi columns c.. and lo columns N + c.. of each chunk, added in turn
 #pragma unroll
-            for (int i = 0; i < kChunks; ++i) {
-                if (i < mine) {
-                    tmem_ld_wait();
-                    if (i + 1 < mine) tmem_ld_32x32b_x16(base + (uint32_t)(16 * (chalf + 2 * (i + 1))), v[(i + 1) & 1]);
+                for (int i = 0; i < kMaxStackN / 32; ++i) {
+                    if (i < mine) {
+                        const uint32_t c = (uint32_t)(16 * (chalf + 2 * i));
+                        tmem_ld_32x32b_x16(base + c, v[0]);
+                        tmem_ld_32x32b_x16(base + (uint32_t)N + c, v[1]);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int k = 0; k < 16; k += 2) add2(acc[i][k], acc[i][k + 1], v[i & 1][k], v[i & 1][k + 1]);
+                        for (int k = 0; k < 16; k += 2) {
+                            add2(acc[i][k], acc[i][k + 1], v[0][k], v[0][k + 1]);
+                            add2(acc[i][k], acc[i][k + 1], v[1][k], v[1][k + 1]);
+                        }
+                    }
+                }
+            } else {
+                if (mine > 0) tmem_ld_32x32b_x16(base + (uint32_t)(16 * chalf), v[0]);
+#pragma unroll
+                for (int i = 0; i < kChunks; ++i) {
+                    if (i < mine) {
+                        tmem_ld_wait();
+                        if (i + 1 < mine)
+                            tmem_ld_32x32b_x16(base + (uint32_t)(16 * (chalf + 2 * (i + 1))), v[(i + 1) & 1]);
+#pragma unroll
+                        for (int k = 0; k < 16; k += 2) add2(acc[i][k], acc[i][k + 1], v[i & 1][k], v[i & 1][k + 1]);
+                    }
                 }
             }
             tc_fence_before();
