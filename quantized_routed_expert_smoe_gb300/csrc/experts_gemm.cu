@@ -72,14 +72,15 @@ constexpr uint32_t kACols = 32;                // one slice of A: 128 lanes x 64
 constexpr int kMaxA = 8;                       // A buffers at most
 constexpr int kMaxBufs = 4;                    // partial buffers at most
 constexpr int kMaxStackN = 96;                 // tiles up to this N stack hi and lo rows into one MMA
+constexpr int kClusterRows = 96;               // mean rows per expert from which CTAs of a tile form a cluster
 constexpr int kSmemBytes = 232448;             // the per-CTA maximum (227 KB): [align slack][ring][barriers]
 constexpr int kBarBytes = 512;
 constexpr int kRingBytes = kSmemBytes - 1024 - kBarBytes;
-// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 32, the converters to
-// 48 and the promoters take 176: 128 x 32 + 256 x 48 + 256 x 176 = 61,440.  Per SM sub-partition (one warp of each
-// warpgroup): 32 x (32 + 176 + 176 + 48 + 48) = 15,360 <= 16,384.
-constexpr int kRegsWg0 = 32;
-constexpr int kRegsConv = 48;
+// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 and the converters give back to 40
+// and the promoters take 176: 128 x 40 + 256 x 40 + 256 x 176 = 60,416 <= 61,440.  Per SM sub-partition (one warp
+// of each warpgroup): 32 x (40 + 176 + 176 + 40 + 40) = 15,104 <= 16,384.
+constexpr int kRegsWg0 = 40;
+constexpr int kRegsConv = 40;
 constexpr int kRegsProm = 176;
 static_assert(128 * kRegsWg0 + 256 * kRegsConv + 256 * kRegsProm <= 640 * 96, "register split exceeds the launch");
 static_assert(kMaxBN <= 224 && kMaxBN % 32 == 0, "two partial buffers and two A buffers must fit in tensor memory");
@@ -105,6 +106,33 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
+}
+
+// TMA 2D tile multicast to the CTAs of `mask` in the cluster: same shared-memory offset and mbarrier in each
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                               uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+// arrive once on `bar` in every CTA of `mask` when every tcgen05.mma issued so far by this thread has completed
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// every thread of every CTA of the cluster
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 template <uint32_t N>
@@ -192,6 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const uint32_t part_base = (uint32_t)na * kACols;
     const int nbuf = min(kMaxBufs, ((int)kTmemCols - (int)part_base) / bstride);
 
+    // the CTAs of a cluster (consecutive weight slices of the same tile) share the tile's B rows: each loads every
+    // C-th 16-row box and multicasts it to all, and each one's MMAs free a ring slot in all of them
+    const int C = p.cluster;
+    const uint32_t crank = C > 1 ? cluster_rank() : 0u;
+    const uint16_t cmask = (uint16_t)((1u << C) - 1u);
+
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t* ring = smem_raw + pad;
@@ -211,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     if (threadIdx.x == 0) {
         for (int r = 0; r < kMaxRing; ++r) {
             mbar_init(&sfull[r], 1);                 // the arrival that posts the slice's byte count
-            mbar_init(&sempty[r], 1 + kConverters);  // the MMAs' commit and every converter
+            mbar_init(&sempty[r], C + kConverters);  // the MMAs' commit of every CTA of the cluster, own converters
         }
         for (int a = 0; a < kMaxA; ++a) {
             mbar_init(&afull[a], kConverters);
@@ -231,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     }
     tc_fence_before();
     __syncthreads();
+    if (C > 1) cluster_sync();  // every CTA's barriers are initialised before any remote copy or arrival
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t ring_s = smem_u32(ring);
@@ -271,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                         mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
                     }
                 }
-                mma_commit(&sempty[r]);
+                if (C > 1) mma_commit_mc(&sempty[r], cmask);
+                else mma_commit(&sempty[r]);
                 mma_commit(&aempty[ab]);
                 if (last) mma_commit(&pfull[b]);
                 if (++r == depth) r = 0;
@@ -303,9 +339,17 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 const uint32_t slot = ring_s + (uint32_t)(r * sbytes);
                 mbar_arrive_expect_tx(&sfull[r], tx_bytes);
                 bulk_load(slot + (uint32_t)(2 * N * 128), wblocks + (int64_t)kt * kWBlock, kWBlock, &sfull[r]);
-                for (int b0 = 0; b0 < N; b0 += kRowBox) {
-                    tma_load_2d(slot + (uint32_t)(b0 * 128), &maps.hi, kt * kBK, row0 + b0, &sfull[r]);
-                    tma_load_2d(slot + (uint32_t)((N + b0) * 128), &maps.lo, kt * kBK, row0 + b0, &sfull[r]);
+                if (C > 1) {
+                    for (int b0 = kRowBox * (int)crank; b0 < N; b0 += kRowBox * C) {
+                        tma_load_2d_mc(slot + (uint32_t)(b0 * 128), &maps.hi, kt * kBK, row0 + b0, &sfull[r], cmask);
+                        tma_load_2d_mc(slot + (uint32_t)((N + b0) * 128), &maps.lo, kt * kBK, row0 + b0, &sfull[r],
+                                       cmask);
+                    }
+                } else {
+                    for (int b0 = 0; b0 < N; b0 += kRowBox) {
+                        tma_load_2d(slot + (uint32_t)(b0 * 128), &maps.hi, kt * kBK, row0 + b0, &sfull[r]);
+                        tma_load_2d(slot + (uint32_t)((N + b0) * 128), &maps.lo, kt * kBK, row0 + b0, &sfull[r]);
+                    }
                 }
                 if (++r == depth) {
                     r = 0;
@@ -434,9 +478,18 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     __syncthreads();
     if (warp == 0) {
         mbar_wait(accf, 0, nullptr);  // every MMA has completed before the tensor memory is released
+        if (C > 1 && lane == 0) {
+            // every CTA of the cluster has delivered its last slot releases here (its MMAs are done with them):
+            // nothing arrives on this CTA's barriers after it leaves
+            for (int kt = max(0, nk - depth); kt < nk; ++kt)
+                if (!mbar_wait(&sempty[kt % depth], (uint32_t)(kt / depth) & 1u, abort_flag)) break;
+        }
+        __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    // no CTA leaves while another may still copy into its shared memory or arrive on its barriers
+    if (C > 1) cluster_sync();
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -489,8 +542,26 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
         !make_map(&maps.lo, lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK, kRowBox,
                   CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)(a.a_rows / kBM), (unsigned)max_tiles);
-    experts_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(a, maps);
+    const int mt = a.a_rows / kBM;
+    ExpertsGemmArgs args = a;
+    // clusters share the row tiles through L2 once instead of once per weight slice; they pay off when tiles are
+    // large (L2 bandwidth bounds the product), not for small tiles, whose CTAs would only wait on one another
+    const bool large = a.b_rows >= (int64_t)kClusterRows * a.n_experts;
+    args.cluster = !large ? 1 : (mt % 4 == 0 ? 4 : (mt % 2 == 0 ? 2 : 1));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)mt, (unsigned)max_tiles);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)args.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, experts_gemm_kernel, args, maps);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

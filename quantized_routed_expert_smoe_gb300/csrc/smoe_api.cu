@@ -138,7 +138,7 @@ smoe_status smoe_experts_gateup(const uint16_t* xop, int32_t* tiles, int64_t n, 
     if (n == 0) return SMOE_OK;
     if (!aligned16(xop) || !aligned16(tiles) || !aligned16(wgu) || !aligned16(gu)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{xop, tiles, wgu, 2 * F, H, gu, n, E, true};
+    smoe::ExpertsGemmArgs a{xop, tiles, wgu, 2 * F, H, gu, n, E, true, 1};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 
@@ -160,7 +160,7 @@ smoe_status smoe_experts_down(const uint16_t* hop, int32_t* tiles, int64_t n, in
     if (n == 0) return SMOE_OK;
     if (!aligned16(hop) || !aligned16(tiles) || !aligned16(wd) || !aligned16(dm)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{hop, tiles, wd, H, F, dm, n, E, false};
+    smoe::ExpertsGemmArgs a{hop, tiles, wd, H, F, dm, n, E, false, 1};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 

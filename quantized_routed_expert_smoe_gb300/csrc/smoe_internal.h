@@ -37,6 +37,7 @@ struct ExpertsGemmArgs {
     int64_t b_rows;       // n
     int n_experts;        // E
     bool two_level;       // add every 64-wide K slice into fp32 registers (gate/up); else one accumulator over K
+    int cluster;          // CTAs per cluster sharing a tile's rows (set by the launcher)
 };
 cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s);
 
