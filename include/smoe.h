@@ -33,7 +33,7 @@
  *                    per (expert, 128-row tile, 64-value slice) a 2560-byte block = the tile's 128 rows x 16 code
  *                    bytes, then its 128 rows x 2 fp16 scales; blocks ordered by expert, tile, slice.
  *   tiles            int32 [4 + 4 * smoe_max_tiles(n, E)]: header {n_tiles, group_status, n, kernel_status}, then
- *                    per tile {expert, first row, rows, 0}; each expert's c rows split into ceil(c/224) near-equal
+ *                    per tile {expert, first row, rows, 0}; each expert's c rows split into ceil(c/192) near-equal
  *                    tiles [floor(i*c/nt), floor((i+1)*c/nt)), experts in id order.
  *
  * CONVENTIONS
@@ -69,7 +69,7 @@ typedef int smoe_status;
 /* Largest supported sizes. */
 #define SMOE_MAX_EXPERTS 1024
 #define SMOE_MAX_TOPK 32
-#define SMOE_TILE_ROWS 224
+#define SMOE_TILE_ROWS 192
 
 /* Human-readable name of a status code (static storage). */
 const char* smoe_status_string(smoe_status s);
@@ -80,7 +80,7 @@ const char* smoe_last_error_string(void);
 /* SMOE_OK when the current CUDA device is an sm_103 part the kernels were built for. */
 smoe_status smoe_device_check(void);
 
-/* Most tiles smoe_group can emit for n pairs over E experts: ceil(n / 224) + min(E, n). */
+/* Most tiles smoe_group can emit for n pairs over E experts: ceil(n / 192) + min(E, n). */
 int64_t smoe_max_tiles(int64_t n, int E);
 /* Bytes of the tiles buffer: 16 * (1 + smoe_max_tiles(n, E)). */
 size_t smoe_tiles_bytes(int64_t n, int E);

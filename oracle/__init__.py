@@ -22,7 +22,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-TILE_ROWS = 224  # must equal oracle_tile_rows() in the C++ file (checked at load)
+TILE_ROWS = 192  # must equal oracle_tile_rows() in the C++ file (checked at load)
 
 
 def build(force: bool = False) -> str:

@@ -28,7 +28,7 @@
 //   R5 weights: softmax, top-K, renormalised over the K:  w_k = exp(l_k - l_1) / sum_{j in top-K} exp(l_j - l_1);
 //      the full softmax denominator cancels.
 //   R6 grouping: stable by pair index i = t*K + k (the host loop's order); the pages' 64-row tiles become tiles of at
-//      most 224 rows, each expert's c rows split into ceil(c/224) parts [floor(i*c/nt), floor((i+1)*c/nt)).
+//      most 192 rows, each expert's c rows split into ceil(c/192) parts [floor(i*c/nt), floor((i+1)*c/nt)).
 //   R7 SwiGLU: h_j = silu(g_j) * u_j, silu(g) = g / (1 + exp(-g)), gate = rows [0, F), up = rows [F, 2F); h is
 //      rounded to fp32 before the q8 rule of R3 (the rule is defined on fp32 input).
 //   R8 combine: Y[t] = sum over k (in k order) of w[t][k] * Dm[slot[t*K+k]]; no shared expert.
@@ -153,7 +153,7 @@ uint16_t oracle_f2h(float f) { return f2h_rne(f); }
 float oracle_h2f(uint16_t h) { return h2f(h); }
 
 /// Most rows in one tile of the tile list (R6).
-int64_t oracle_tile_rows() { return 224; }
+int64_t oracle_tile_rows() { return 192; }
 
 // ------------------------------------------------------------------------------------------------ step 1: route
 /// [P1] Prefill::run, MoE half, route(logits, ids, w, T, n_expert): softmax over the E router logits of each token,

@@ -19,7 +19,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsmoe.so")
 
 SMOE_OK, SMOE_ERR_ARG, SMOE_ERR_LAUNCH, SMOE_ERR_UNSUPPORTED, SMOE_ERR_RANGE, SMOE_ERR_TIMEOUT = range(6)
-TILE_ROWS = 224
+TILE_ROWS = 192
 
 
 class SmoeError(RuntimeError):

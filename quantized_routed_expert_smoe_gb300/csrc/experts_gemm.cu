@@ -25,27 +25,28 @@
 //   - the weight operand (A) is decoded from the packed 2-bit block by the converter warps directly into TENSOR
 //     memory (tcgen05.st; lane = weight row, 32-bit column = a pair of K values) and the MMA reads it from there.
 //
-// Tile: one CTA = one tile of the tile list (an expert and up to 224 of its routed rows, contiguous in routed-row
+// Tile: one CTA = one tile of the tile list (an expert and up to 192 of its routed rows, contiguous in routed-row
 // order; the MMA's N, a multiple of 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB:
 // weights are the M operand so that a small expert wastes little).  Five warpgroups, registers rebalanced with
 // setmaxnreg:
-//   warpgroup 0   warp 0: tensor-memory allocation and, on one lane, the MMAs (four K16 steps x two parts a slice);
+//   warpgroup 0   warps 0 and 2, one lane each: the MMAs of alternate slices (four K16 steps x two parts a slice;
+//                 one thread's waits overlap the other's MMAs); warp 0 also allocates the tensor memory;
 //                 warp 1, one lane: the producer -- per 64-wide K slice, TMA tile loads of the tile's rows of both
 //                 parts (16 rows x 128 bytes a load, 128-byte swizzle) and one bulk copy of the packed weight
 //                 block, into a ring slot;
-//   warpgroups 1-2  promoters: add each finished partial into fp32 registers (a TMEM lane a thread, alternate
-//                 16-column chunks a warpgroup), then write the fp32 rows;
-//   warpgroups 3-4  converters: thread = (weight row, 32-value half of the slice): decode its 32 weights into the
-//                 slice's A buffer in tensor memory.
+//   warpgroups 1-3  promoters: add each finished partial into fp32 registers (a TMEM lane a thread, every third
+//                 32-column chunk a warpgroup), then write the fp32 rows;
+//   warpgroup 4   converters: thread = weight row: decode its 64 weights of the slice into the slice's A buffer in
+//                 tensor memory.
 // Tensor memory (512 columns): 2 to 8 A buffers of 32 columns (more for small tiles, so that the converters run
 // further ahead), then 1 to 4 partial buffers of N columns rounded up to 32 (2N for a tile of at most 96 rows, which
 // stacks its hi and lo rows into one MMA; two buffers for gate/up, which promotes every slice; one suffices for
-// down); two buffers of a full tile cap the tile at 224 rows.
+// down).  A tile has at most 192 rows: a promoter thread then holds its 64 accumulators and two 32-column loads.
 //
-// Synchronisation: a satisfied mbarrier wait still costs a round trip of a few hundred cycles, so each role waits
-// as little as it can per slice -- the MMA thread only on "A of slice kt decoded" (the converters arrive on it after
-// they have seen the slice's copies land, so it also orders the TMA-written B tiles before the MMAs) and on a free
-// partial buffer when a partial starts.
+// Synchronisation: a satisfied mbarrier wait still costs a round trip of a few hundred cycles, so the MMA thread
+// waits once per slice, on "A of slice kt decoded": the converters arrive on it after they have seen the slice's
+// copies land (so it also orders the TMA-written B tiles before the MMAs) and, for a slice that starts a partial,
+// after one of them has seen the promoters free that partial's buffer.
 //
 // K order: within each group of 16 K values, operand position 2m holds value m and position 2m+1 value m+8
 // (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so the contraction is unchanged
@@ -64,8 +65,8 @@ constexpr int kBM = 128;                       // weight rows per CTA (MMA M)
 constexpr int kBK = 64;                        // K values per slice: one 128-byte swizzle row of fp16
 constexpr int kMaxBN = SMOE_TILE_ROWS;         // routed rows per tile (MMA N <= 224)
 constexpr int kThreads = 640;                  // five warpgroups
-constexpr int kPromoters = 256;                // warpgroups 1-2
-constexpr int kConverters = 256;               // warpgroups 3-4
+constexpr int kPromoters = 384;                // warpgroups 1-3
+constexpr int kConverters = 128;               // warpgroup 4
 constexpr int kMaxRing = 16;                   // slices in flight at most
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACols = 32;                // one slice of A: 128 lanes x 64 fp16
@@ -76,14 +77,16 @@ constexpr int kClusterRows = 96;               // mean rows per expert from whic
 constexpr int kSmemBytes = 232448;             // the per-CTA maximum (227 KB): [align slack][ring][barriers]
 constexpr int kBarBytes = 512;
 constexpr int kRingBytes = kSmemBytes - 1024 - kBarBytes;
-// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 and the converters give back to 40
-// and the promoters take 176: 128 x 40 + 256 x 40 + 256 x 176 = 60,416 <= 61,440.  Per SM sub-partition (one warp
-// of each warpgroup): 32 x (40 + 176 + 176 + 40 + 40) = 15,104 <= 16,384.
+// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 40, the converters
+// to 64 and the promoters take 120: 128 x 40 + 384 x 120 + 128 x 64 = 59,392 <= 61,440.  Per SM sub-partition (one
+// warp of each warpgroup): 32 x (40 + 3 x 120 + 64) = 14,848 <= 16,384.
 constexpr int kRegsWg0 = 40;
-constexpr int kRegsConv = 40;
-constexpr int kRegsProm = 176;
-static_assert(128 * kRegsWg0 + 256 * kRegsConv + 256 * kRegsProm <= 640 * 96, "register split exceeds the launch");
+constexpr int kRegsConv = 64;
+constexpr int kRegsProm = 120;
+static_assert(128 * kRegsWg0 + kConverters * kRegsConv + kPromoters * kRegsProm <= kThreads * 96,
+              "register split exceeds the launch");
 static_assert(kMaxBN <= 224 && kMaxBN % 32 == 0, "two partial buffers and two A buffers must fit in tensor memory");
+static_assert(kMaxBN % 96 == 0, "the promoter warpgroups take whole 32-column chunks in turn");
 
 // Ring slot (one 64-wide K slice of the tile): the tile's N rows of the hi part, then of the lo part (N x 128 bytes
 // each, 128-byte swizzle, 1024-aligned), then the packed weight block (codes [128][16 B], scales [128][4 B]); slots
@@ -159,6 +162,16 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
           "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // D[tmem] (+)= A[tmem] * B[smem desc]^T, fp16 operands, fp32 accumulate; issued by one thread.
@@ -206,8 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const int N = (rows + 15) & ~15;
     const int m0 = blockIdx.x * kBM;
     const int nk = p.K / kBK;                // slices
-    const int P = p.two_level ? 1 : nk;      // slices per tensor-memory partial
-    const int groups = (nk + P - 1) / P;     // partials
+    // two MMA threads take alternate slices (stream kt mod 2).  Two-level: a partial per slice, buffer kt mod nbuf;
+    // else one partial per stream over all its slices, in buffer 0 or 1, summed by the promoters
+    const int P = p.two_level ? 1 : nk;      // 1, or nk for one accumulator a stream
+    const int groups = p.two_level ? nk : min(2, nk);  // partials the promoters add
     // a small tile stacks its hi and lo rows (contiguous in the slot) into one MMA of 2N columns: an MMA costs about
     // the same for any N up to 64, so this halves the MMAs where they are cheapest per row; the partial then holds
     // the hi product in columns [0, N) and the lo product in [N, 2N)
@@ -215,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const int ncols = stacked ? 2 * N : N;   // partial columns
     // tensor memory: na A buffers, then nbuf partial buffers of bstride columns
     const int bstride = (ncols + 31) & ~31;
-    const int need = (groups > 1 ? 2 : 1) * bstride;
+    const int need = 2 * bstride;             // two partials in flight (a slice each, or one per stream of slices)
     const int na = max(2, min(kMaxA, ((int)kTmemCols - need) / (int)kACols));
     const uint32_t part_base = (uint32_t)na * kACols;
     const int nbuf = min(kMaxBufs, ((int)kTmemCols - (int)part_base) / bstride);
@@ -255,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             mbar_init(&pfull[b], 1);
             mbar_init(&pempty[b], kPromoters);
         }
-        mbar_init(accf, 1);
+        mbar_init(accf, 2);  // one final commit of each MMA thread
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -273,19 +288,18 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
 
     if (warp < 4) {
         setmaxnreg_dec<kRegsWg0>();
-        if (warp == 0 && lane == 0) {
-            // ------------------------------------------------------------------ MMA issue (one thread)
-            // slice kt: A buffer kt mod na, the slot's hi and lo tiles; partial g = kt / P in buffer g mod nbuf, from
-            // zero at its first slice
-            // ring / buffer positions advance by counting (a division by a runtime value costs tens of cycles on
-            // this single thread's critical path)
+        if ((warp == 0 || warp == 2) && lane == 0) {
+            // ------------------------------------------------------------------ MMA issue (two threads)
+            // stream st = warp / 2 issues slices kt = st, st + 2, ...: A buffer kt mod na, the slot's hi and lo
+            // tiles, the partial buffer above; the other thread's waits overlap this one's MMAs.  Ring, buffer and
+            // phase positions advance by counting (a division by a runtime value costs tens of cycles here).
+            const int st = warp >> 1;
             const uint32_t idesc = idesc_f16_f32(kBM, ncols);
-            int r = 0, ab = 0, b = 0, kp = 0, g = 0;
-            uint32_t aph = 0, bwrap = 0;
-            for (int kt = 0; kt < nk && ok; ++kt) {
-                const bool first = kp == 0, last = kp == P - 1 || kt == nk - 1;
-                if (!mbar_wait(&afull[ab], aph, abort_flag) ||
-                    (first && g >= nbuf && !mbar_wait(&pempty[b], (bwrap - 1u) & 1u, abort_flag))) {
+            int r = st % depth, ab = st % na, b = p.two_level ? st % nbuf : st;
+            uint32_t aph = (uint32_t)(st / na) & 1u;
+            for (int kt = st; kt < nk && ok; kt += 2) {
+                const bool first = p.two_level || kt < 2, last = p.two_level || kt + 2 >= nk;
+                if (!mbar_wait(&afull[ab], aph, abort_flag)) {  // implies the partial buffer is free
                     ok = false;
                     break;
                 }
@@ -310,19 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 else mma_commit(&sempty[r]);
                 mma_commit(&aempty[ab]);
                 if (last) mma_commit(&pfull[b]);
-                if (++r == depth) r = 0;
-                if (++ab == na) {
-                    ab = 0;
+                if ((r += 2) >= depth) r -= depth;
+                if ((ab += 2) >= na) {
+                    ab -= na;
                     aph ^= 1u;
                 }
-                if (++kp == P) {
-                    kp = 0;
-                    ++g;
-                    if (++b == nbuf) {
-                        b = 0;
-                        ++bwrap;
-                    }
-                }
+                if (p.two_level && (b += 2) >= nbuf) b -= nbuf;
             }
             mma_commit(accf);  // completes once every MMA issued above has completed (abort path included)
         } else if (warp == 1 && lane == 0) {
@@ -362,21 +369,22 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 mbar_wait(&sfull[kt % depth], (uint32_t)(kt / depth) & 1u, nullptr);
         }
         __syncwarp();
-    } else if (warp < 12) {
+    } else if (warp < 16) {
         setmaxnreg_inc<kRegsProm>();
-        // ------------------------------------------------------------------ promoters (256 threads)
-        // this thread owns TMEM lane 32*q + lane (weight row mrow) and the 16-column chunks chalf + 2 i of the tile;
-        // the next chunk's load is in flight while the current one is added
+        // ------------------------------------------------------------------ promoters (384 threads)
+        // this thread owns TMEM lane 32*q + lane (weight row mrow) and the 32-column chunks cg + 3 i of the tile
+        // (16-column chunks for a stacked tile); three warps a sub-partition hide each other's load latency
         const int q = warp & 3;
-        const int chalf = (warp - 4) >> 2;  // warpgroup 1: even chunks; warpgroup 2: odd chunks
+        const int cg = (warp - 4) >> 2;  // promoter warpgroup 0..2
         const int mrow = 32 * q + lane;
-        const int mine = (N / 16 - chalf + 1) / 2;  // chunks of this thread
-        constexpr int kChunks = kMaxBN / 32;        // most chunks of a thread
-        float acc[kChunks][16];
+        constexpr int kChunks = kMaxBN / 96;           // most 32-column chunks of a thread
+        const int mine = (N / 32 - cg + 2) / 3;        // whole 32-column chunks of this thread
+        const bool half = !stacked && (N & 16) && cg == (N / 32) % 3;  // a last 16-column chunk is this thread's
+        float acc[kChunks][32];
 #pragma unroll
         for (int i = 0; i < kChunks; ++i)
 #pragma unroll
-            for (int k = 0; k < 16; ++k) acc[i][k] = 0.0f;
+            for (int k = 0; k < 32; ++k) acc[i][k] = 0.0f;
         int b = 0;
         uint32_t bph = 0;
         for (int g = 0; g < groups && ok; ++g) {
@@ -386,34 +394,46 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             }
             tc_fence_after();
             const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + part_base + (uint32_t)(b * bstride);
-            uint32_t v[2][16];
+            uint32_t v[1][32];
             if (stacked) {
-                // hi columns c.. and lo columns N + c.. of each chunk, added in turn
+                // 16-column chunks cg + 3 i: hi columns c.. and lo columns N + c.., added in turn
+                uint32_t(&h)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0][0]);
+                uint32_t(&l)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0][16]);
 #pragma unroll
-                for (int i = 0; i < kMaxStackN / 32; ++i) {
-                    if (i < mine) {
-                        const uint32_t c = (uint32_t)(16 * (chalf + 2 * i));
-                        tmem_ld_32x32b_x16(base + c, v[0]);
-                        tmem_ld_32x32b_x16(base + (uint32_t)N + c, v[1]);
+                for (int i = 0; i < kMaxStackN / 48; ++i) {
+                    const int c = 16 * (cg + 3 * i);
+                    if (c < N) {
+                        tmem_ld_32x32b_x16(base + (uint32_t)c, h);
+                        tmem_ld_32x32b_x16(base + (uint32_t)(N + c), l);
                         tmem_ld_wait();
+                        float* a = &acc[i >> 1][16 * (i & 1)];
 #pragma unroll
                         for (int k = 0; k < 16; k += 2) {
-                            add2(acc[i][k], acc[i][k + 1], v[0][k], v[0][k + 1]);
-                            add2(acc[i][k], acc[i][k + 1], v[1][k], v[1][k + 1]);
+                            add2(a[k], a[k + 1], h[k], h[k + 1]);
+                            add2(a[k], a[k + 1], l[k], l[k + 1]);
                         }
                     }
                 }
             } else {
-                if (mine > 0) tmem_ld_32x32b_x16(base + (uint32_t)(16 * chalf), v[0]);
 #pragma unroll
                 for (int i = 0; i < kChunks; ++i) {
                     if (i < mine) {
+                        tmem_ld_32x32b_x32(base + (uint32_t)(32 * (cg + 3 * i)), v[0]);
                         tmem_ld_wait();
-                        if (i + 1 < mine)
-                            tmem_ld_32x32b_x16(base + (uint32_t)(16 * (chalf + 2 * (i + 1))), v[(i + 1) & 1]);
 #pragma unroll
-                        for (int k = 0; k < 16; k += 2) add2(acc[i][k], acc[i][k + 1], v[i & 1][k], v[i & 1][k + 1]);
+                        for (int k = 0; k < 32; k += 2) add2(acc[i][k], acc[i][k + 1], v[0][k], v[0][k + 1]);
                     }
+                }
+                if (half) {  // the tile's last 16 columns (N = 32 m + 16) into the first half of chunk `mine`
+                    uint32_t(&h)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0][0]);
+                    tmem_ld_32x32b_x16(base + (uint32_t)(N - 16), h);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < kChunks; ++i)
+                        if (i == mine) {
+#pragma unroll
+                            for (int k = 0; k < 16; k += 2) add2(acc[i][k], acc[i][k + 1], h[k], h[k + 1]);
+                        }
                 }
             }
             tc_fence_before();
@@ -429,35 +449,50 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
 #pragma unroll
             for (int i = 0; i < kChunks; ++i) {
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const int col = 16 * (chalf + 2 * i) + k;
-                    if (col < rows) outcol[(int64_t)(row0 + col) * p.a_rows] = acc[i][k];
+                for (int k = 0; k < 32; ++k) {
+                    // a stacked tile's 16-column chunk j = cg + 3 i' sits at acc[i' / 2][16 (i' % 2) ..]
+                    const int col = stacked ? 16 * (cg + 3 * (2 * i + (k >> 4))) + (k & 15)
+                                            : ((i < mine || !half) ? 32 * (cg + 3 * i) + k : (N - 16) + k);
+                    const bool mine_k = stacked ? (2 * i + (k >> 4)) < kMaxStackN / 48
+                                                : (i < mine || (half && i == mine && k < 16));
+                    if (mine_k && col < rows) outcol[(int64_t)(row0 + col) * p.a_rows] = acc[i][k];
                 }
             }
         }
     } else {
         setmaxnreg_dec<kRegsConv>();
-        // ------------------------------------------------------------------ converters (256 threads)
-        // thread = (row ct % 128 = TMEM lane of its warp, half h = ct / 128 of each slice): 32 weights a slice
-        const int ct = threadIdx.x - 384;
-        const int row = ct & 127, h = ct >> 7;
-        const uint32_t lane_base = (uint32_t)(row & ~31) << 16;
-        int r = 0, ab = 0;
-        uint32_t rph = 0, aph = 0;  // sfull phase parity; aempty parity of the previous use of buffer ab
+        // ------------------------------------------------------------------ converters (128 threads)
+        // thread = weight row ct = TMEM lane of its warp: 64 weights a slice into the 32 columns of A buffer ab
+        const int ct = threadIdx.x - 512;
+        const uint32_t lane_base = (uint32_t)(ct & ~31) << 16;
+        int r = 0, ab = 0, b = 0;
+        uint32_t rph = 0, aph = 0, bph = 0;  // sfull phase parity; aempty parity of the previous use of buffer ab;
+                                             // pempty parity of the previous use of partial buffer b
         for (int kt = 0; kt < nk && ok; ++kt) {
             if (!mbar_wait(&sfull[r], rph, abort_flag) || (kt >= na && !mbar_wait(&aempty[ab], aph, abort_flag))) {
                 ok = false;
                 break;
             }
             const uint8_t* wb = ring + r * sbytes + 2 * N * 128;
-            const uint2 codes = *reinterpret_cast<const uint2*>(wb + row * 16 + h * 8);
-            const __half2 d2 = __half2half2(*reinterpret_cast<const __half*>(wb + 2048 + row * 4 + h * 2));
-            uint32_t col[16];
-            decode_weights16(codes.x, d2, col);
-            decode_weights16(codes.y, d2, col + 8);
-            tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols + 16u * (uint32_t)h, col);
+            const uint4 codes = *reinterpret_cast<const uint4*>(wb + ct * 16);
+            const __half2 sc = *reinterpret_cast<const __half2*>(wb + 2048 + ct * 4);
+            uint32_t col[32];
+            decode_weights16(codes.x, __low2half2(sc), col);
+            decode_weights16(codes.y, __low2half2(sc), col + 8);
+            decode_weights16(codes.z, __high2half2(sc), col + 16);
+            decode_weights16(codes.w, __high2half2(sc), col + 24);
+            tmem_st_32x32b_x32(tmem + lane_base + (uint32_t)ab * kACols, col);
             tmem_st_wait();
             tc_fence_before();
+            // a slice that starts a partial may be multiplied only once the promoters have freed its buffer (a
+            // partial per slice when two-level; one per stream, never reused, otherwise)
+            if (P == 1) {
+                if (ct == 0 && kt >= nbuf && !mbar_wait(&pempty[b], bph, abort_flag)) ok = false;
+                if (++b == nbuf) {
+                    b = 0;
+                    if (kt >= nbuf) bph ^= 1u;
+                }
+            }
             mbar_arrive(&afull[ab]);
             mbar_arrive(&sempty[r]);
             if (++r == depth) {

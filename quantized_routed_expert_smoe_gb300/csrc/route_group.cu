@@ -128,7 +128,7 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 }
 
 // pass 2 (one block, thread e = expert e): counts, offsets, each chunk's first row for each expert, and the tile
-// list (each expert's c rows in ceil(c / 224) near-equal tiles, experts in id order).  The [chunks][E] counts are
+// list (each expert's c rows in ceil(c / 192) near-equal tiles, experts in id order).  The [chunks][E] counts are
 // staged in shared memory by one coalesced sweep.
 __global__ void __launch_bounds__(kGroupThreads) group_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E,
                                                                    int64_t n, int32_t* __restrict__ counts,

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_sizing_helpers(lib):
     from quantized_routed_expert_smoe_gb300 import binding
-    assert binding.max_tiles(81920, 512) == (81920 + 223) // 224 + 512
+    assert binding.max_tiles(81920, 512) == (81920 + 191) // 192 + 512
     assert binding.max_tiles(128, 16) == 1 + 16
     assert binding.max_tiles(0, 16) == 0
     assert binding.tiles_bytes(128, 16) == 16 * 18
