@@ -78,10 +78,10 @@ constexpr int kSmemBytes = 232448;             // the per-CTA maximum (227 KB): 
 constexpr int kBarBytes = 512;
 constexpr int kRingBytes = kSmemBytes - 1024 - kBarBytes;
 // registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 40, the converters
-// to 64 and the promoters take 120: 128 x 40 + 384 x 120 + 128 x 64 = 59,392 <= 61,440.  Per SM sub-partition (one
-// warp of each warpgroup): 32 x (40 + 3 x 120 + 64) = 14,848 <= 16,384.
+// to 56 and the promoters take 120: 128 x 40 + 384 x 120 + 128 x 56 = 58,368 <= 61,440.  Per SM sub-partition (one
+// warp of each warpgroup): 32 x (40 + 3 x 120 + 56) = 14,592 <= 16,384.
 constexpr int kRegsWg0 = 40;
-constexpr int kRegsConv = 64;
+constexpr int kRegsConv = 56;
 constexpr int kRegsProm = 120;
 static_assert(128 * kRegsWg0 + kConverters * kRegsConv + kPromoters * kRegsProm <= kThreads * 96,
               "register split exceeds the launch");
@@ -207,45 +207,61 @@ struct GemmMaps {
     CUtensorMap hi, lo;  // the two parts of the B rows: fp16 [b_rows][K] each, box 64 x 16, 128-byte swizzle
 };
 
+// One work item: a tile of the tile list x one group of C consecutive 128-row weight slices (one per CTA of the
+// cluster).  Every role of every CTA walks the same item sequence and skips the same invalid items.
+struct Item {
+    int e, row0, rows, N, m0;
+    bool stacked;  // N <= kMaxStackN: hi and lo rows in one MMA of 2N columns
+    int ncols;     // partial columns
+};
+__device__ __forceinline__ bool load_item(const int32_t* tiles, int item, int mgroups, int C, uint32_t crank,
+                                          const ExpertsGemmArgs& p, Item& t) {
+    const int ti = item / mgroups, mg = item - ti * mgroups;
+    const int4 te = reinterpret_cast<const int4*>(tiles)[1 + ti];
+    t.e = te.x;
+    t.row0 = te.y;
+    t.rows = te.z;
+    // a tile the grouping cannot have written (a bad expert id or row range): nothing is read or written for it
+    if (t.rows <= 0 || t.rows > kMaxBN || t.e < 0 || t.e >= p.n_experts || t.row0 < 0 ||
+        t.row0 + (int64_t)t.rows > p.b_rows)
+        return false;
+    t.N = (t.rows + 15) & ~15;
+    t.m0 = (mg * C + (int)crank) * kBM;
+    t.stacked = t.N <= kMaxStackN;
+    t.ncols = t.stacked ? 2 * t.N : t.N;
+    return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const ExpertsGemmArgs p,
                                                                    const __grid_constant__ GemmMaps maps) {
     int32_t* tiles = p.tiles;
-    const int ti = blockIdx.y;
-    if (ti >= tiles[0] || tiles[1] != 0) return;  // no such tile, or the grouping failed: nothing to do
-    const int4 tile = reinterpret_cast<const int4*>(tiles)[1 + ti];
-    const int e = tile.x, row0 = tile.y, rows = tile.z;
-    // a tile the grouping cannot have written (a bad expert id or row range): nothing is read or written for it
-    if (rows <= 0 || rows > kMaxBN || e < 0 || e >= p.n_experts || row0 < 0 || row0 + (int64_t)rows > p.b_rows) return;
-    const int N = (rows + 15) & ~15;
-    const int m0 = blockIdx.x * kBM;
-    const int nk = p.K / kBK;                // slices
-    // two MMA threads take alternate slices (stream kt mod 2).  Two-level: a partial per slice, buffer kt mod nbuf;
-    // else one partial per stream over all its slices, in buffer 0 or 1, summed by the promoters
-    const int P = p.two_level ? 1 : nk;      // 1, or nk for one accumulator a stream
-    const int groups = p.two_level ? nk : min(2, nk);  // partials the promoters add
-    // a small tile stacks its hi and lo rows (contiguous in the slot) into one MMA of 2N columns: an MMA costs about
-    // the same for any N up to 64, so this halves the MMAs where they are cheapest per row; the partial then holds
-    // the hi product in columns [0, N) and the lo product in [N, 2N)
-    const bool stacked = N <= kMaxStackN;
-    const int ncols = stacked ? 2 * N : N;   // partial columns
-    // tensor memory: na A buffers, then nbuf partial buffers of bstride columns
-    const int bstride = (ncols + 31) & ~31;
-    const int need = 2 * bstride;             // two partials in flight (a slice each, or one per stream of slices)
-    const int na = max(2, min(kMaxA, ((int)kTmemCols - need) / (int)kACols));
-    const uint32_t part_base = (uint32_t)na * kACols;
-    const int nbuf = min(kMaxBufs, ((int)kTmemCols - (int)part_base) / bstride);
+    if (tiles[1] != 0) return;  // the grouping failed: nothing to do (the same answer in every CTA)
+    const int n_tiles = tiles[0];
+    const int nk = p.K / kBK;  // slices of an item
+    // two MMA threads take alternate slices (stream = global slice index mod 2).  Two-level: a partial per slice;
+    // else one partial per stream of an item (slices kt and kt + 2 ... of the same parity), summed by the promoters
+    const int pitem = p.two_level ? nk : min(2, nk);  // partials an item
 
-    // the CTAs of a cluster (consecutive weight slices of the same tile) share the tile's B rows: each loads every
-    // C-th 16-row box and multicasts it to all, and each one's MMAs free a ring slot in all of them
+    // persistent: cluster cid of NC takes items cid, cid + NC, ...; its CTAs take the C weight slices of an item
     const int C = p.cluster;
     const uint32_t crank = C > 1 ? cluster_rank() : 0u;
     const uint16_t cmask = (uint16_t)((1u << C) - 1u);
+    const int mgroups = p.a_rows / kBM / C;
+    const int n_items = n_tiles * mgroups;
+    const int cid = blockIdx.x / C, NC = gridDim.x / C;
+
+    // fixed geometry for every item (tiles of up to kMaxBN rows): a ring of `depth` slots, na A buffers and nbuf
+    // partial buffers of kMaxBN columns in tensor memory
+    const int sbytes = slot_bytes(kMaxBN);
+    const int depth = min(kMaxRing, kRingBytes / sbytes);
+    constexpr int na = ((int)kTmemCols - 2 * kMaxBN) / (int)kACols;
+    constexpr uint32_t part_base = (uint32_t)na * kACols;
+    constexpr int nbuf = ((int)kTmemCols - (int)part_base) / kMaxBN;
+    static_assert(na >= 2 && na <= kMaxA && nbuf >= 2 && nbuf <= kMaxBufs, "tensor-memory split");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t* ring = smem_raw + pad;
-    const int sbytes = slot_bytes(N);
-    const int depth = min(kMaxRing, kRingBytes / sbytes);
     uint64_t* sfull = reinterpret_cast<uint64_t*>(smem_raw + kSmemBytes - kBarBytes);  // slot r holds slice [kMaxRing]
     uint64_t* sempty = sfull + kMaxRing;    // the MMAs and the converters are done with slot r [kMaxRing]
     uint64_t* afull = sempty + kMaxRing;    // A buffer a decoded (and its slot's copies landed) [kMaxA]
@@ -285,167 +301,191 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const uint32_t tmem = *tmem_slot;
     const uint32_t ring_s = smem_u32(ring);
     bool ok = true;
+    int total = 0;  // slices this CTA ran (warp 0 lane 0 uses it at the end)
 
     if (warp < 4) {
         setmaxnreg_dec<kRegsWg0>();
         if ((warp == 0 || warp == 2) && lane == 0) {
             // ------------------------------------------------------------------ MMA issue (two threads)
-            // stream st = warp / 2 issues slices kt = st, st + 2, ...: A buffer kt mod na, the slot's hi and lo
-            // tiles, the partial buffer above; the other thread's waits overlap this one's MMAs.  Ring, buffer and
-            // phase positions advance by counting (a division by a runtime value costs tens of cycles here).
+            // stream st issues the global slices gs = st, st + 2, ...: A buffer gs mod na, the slot's hi and lo tiles,
+            // the slice's partial buffer; the other thread's waits overlap this one's MMAs.  Positions advance by
+            // counting (a division by a runtime value costs tens of cycles on this thread's critical path).
             const int st = warp >> 1;
-            const uint32_t idesc = idesc_f16_f32(kBM, ncols);
-            int r = st % depth, ab = st % na, b = p.two_level ? st % nbuf : st;
+            int gs = st, base = 0, seq = 0;  // this thread's next global slice; the item's first; items done
+            int r = st % depth, ab = st % na;
             uint32_t aph = (uint32_t)(st / na) & 1u;
-            for (int kt = st; kt < nk && ok; kt += 2) {
-                const bool first = p.two_level || kt < 2, last = p.two_level || kt + 2 >= nk;
-                if (!mbar_wait(&afull[ab], aph, abort_flag)) {  // implies the partial buffer is free
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t hi = ring_s + (uint32_t)(r * sbytes), lo = hi + (uint32_t)(N * 128);
-                const uint32_t d = tmem + part_base + (uint32_t)(b * bstride);
-                const uint32_t a = tmem + (uint32_t)ab * kACols;
-                if (stacked) {
+            Item t;
+            for (int item = cid; item < n_items && ok; item += NC) {
+                if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
+                const uint32_t idesc = idesc_f16_f32(kBM, t.ncols);
+                for (; gs < base + nk && ok; gs += 2) {
+                    const int kt = gs - base;
+                    // the slice's partial: a partial per slice (two-level), else the item's partial kt mod 2
+                    const int gp = seq * pitem + (p.two_level ? kt : (pitem == 2 ? (kt & 1) : 0));
+                    const int b = gp % nbuf;
+                    const bool first = p.two_level || kt < 2, last = p.two_level || kt + 2 >= nk;
+                    if (!mbar_wait(&afull[ab], aph, abort_flag)) {  // implies the partial buffer is free
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t hi = ring_s + (uint32_t)(r * sbytes), lo = hi + (uint32_t)(t.N * 128);
+                    const uint32_t d = tmem + part_base + (uint32_t)(b * kMaxBN);
+                    const uint32_t a = tmem + (uint32_t)ab * kACols;
+                    if (t.stacked) {
 #pragma unroll
-                    for (int k16 = 0; k16 < 4; ++k16)
-                        mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
-                                   (first && k16 == 0) ? 0u : 1u);
-                } else {
+                        for (int k16 = 0; k16 < 4; ++k16)
+                            mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
+                                       (first && k16 == 0) ? 0u : 1u);
+                    } else {
 #pragma unroll
-                    for (int k16 = 0; k16 < 4; ++k16) {
-                        mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
-                                   (first && k16 == 0) ? 0u : 1u);
-                        mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
+                        for (int k16 = 0; k16 < 4; ++k16) {
+                            mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
+                                       (first && k16 == 0) ? 0u : 1u);
+                            mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
+                        }
+                    }
+                    if (C > 1) mma_commit_mc(&sempty[r], cmask);
+                    else mma_commit(&sempty[r]);
+                    mma_commit(&aempty[ab]);
+                    if (last) mma_commit(&pfull[b]);
+                    if ((r += 2) >= depth) r -= depth;
+                    if ((ab += 2) >= na) {
+                        ab -= na;
+                        aph ^= 1u;
                     }
                 }
-                if (C > 1) mma_commit_mc(&sempty[r], cmask);
-                else mma_commit(&sempty[r]);
-                mma_commit(&aempty[ab]);
-                if (last) mma_commit(&pfull[b]);
-                if ((r += 2) >= depth) r -= depth;
-                if ((ab += 2) >= na) {
-                    ab -= na;
-                    aph ^= 1u;
-                }
-                if (p.two_level && (b += 2) >= nbuf) b -= nbuf;
+                base += nk;
+                ++seq;
             }
+            total = base;
             mma_commit(accf);  // completes once every MMA issued above has completed (abort path included)
         } else if (warp == 1 && lane == 0) {
             // ------------------------------------------------------------------ producer (one thread)
-            const uint8_t* wblocks = p.wp + ((int64_t)e * (p.a_rows / kBM) + blockIdx.x) * nk * (int64_t)kWBlock;
-            const uint32_t tx_bytes = 2u * (uint32_t)N * 128u + (uint32_t)kWBlock;
-            int issued = 0, r = 0;
+            int gs = 0, r = 0;
             uint32_t eph = 0;  // parity of the sempty phase the next wrap waits for
-            for (int kt = 0; kt < nk; ++kt, ++issued) {
-                if (kt >= depth && !mbar_wait(&sempty[r], eph, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t slot = ring_s + (uint32_t)(r * sbytes);
-                mbar_arrive_expect_tx(&sfull[r], tx_bytes);
-                bulk_load(slot + (uint32_t)(2 * N * 128), wblocks + (int64_t)kt * kWBlock, kWBlock, &sfull[r]);
-                if (C > 1) {
-                    for (int b0 = kRowBox * (int)crank; b0 < N; b0 += kRowBox * C) {
-                        tma_load_2d_mc(slot + (uint32_t)(b0 * 128), &maps.hi, kt * kBK, row0 + b0, &sfull[r], cmask);
-                        tma_load_2d_mc(slot + (uint32_t)((N + b0) * 128), &maps.lo, kt * kBK, row0 + b0, &sfull[r],
-                                       cmask);
+            Item t;
+            for (int item = cid; item < n_items && ok; item += NC) {
+                if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
+                const uint8_t* wblocks =
+                    p.wp + ((int64_t)t.e * (p.a_rows / kBM) + t.m0 / kBM) * nk * (int64_t)kWBlock;
+                const uint32_t tx_bytes = 2u * (uint32_t)t.N * 128u + (uint32_t)kWBlock;
+                for (int kt = 0; kt < nk; ++kt, ++gs) {
+                    if (gs >= depth && !mbar_wait(&sempty[r], eph, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                } else {
-                    for (int b0 = 0; b0 < N; b0 += kRowBox) {
-                        tma_load_2d(slot + (uint32_t)(b0 * 128), &maps.hi, kt * kBK, row0 + b0, &sfull[r]);
-                        tma_load_2d(slot + (uint32_t)((N + b0) * 128), &maps.lo, kt * kBK, row0 + b0, &sfull[r]);
+                    const uint32_t slot = ring_s + (uint32_t)(r * sbytes);
+                    mbar_arrive_expect_tx(&sfull[r], tx_bytes);
+                    bulk_load(slot + (uint32_t)(2 * t.N * 128), wblocks + (int64_t)kt * kWBlock, kWBlock, &sfull[r]);
+                    if (C > 1) {
+                        for (int b0 = kRowBox * (int)crank; b0 < t.N; b0 += kRowBox * C) {
+                            tma_load_2d_mc(slot + (uint32_t)(b0 * 128), &maps.hi, kt * kBK, t.row0 + b0, &sfull[r],
+                                           cmask);
+                            tma_load_2d_mc(slot + (uint32_t)((t.N + b0) * 128), &maps.lo, kt * kBK, t.row0 + b0,
+                                           &sfull[r], cmask);
+                        }
+                    } else {
+                        for (int b0 = 0; b0 < t.N; b0 += kRowBox) {
+                            tma_load_2d(slot + (uint32_t)(b0 * 128), &maps.hi, kt * kBK, t.row0 + b0, &sfull[r]);
+                            tma_load_2d(slot + (uint32_t)((t.N + b0) * 128), &maps.lo, kt * kBK, t.row0 + b0,
+                                        &sfull[r]);
+                        }
                     }
-                }
-                if (++r == depth) {
-                    r = 0;
-                    if (kt >= depth) eph ^= 1u;
+                    if (++r == depth) {
+                        r = 0;
+                        if (gs >= depth) eph ^= 1u;
+                    }
                 }
             }
             // no copy may still be writing shared memory when the CTA exits (on the abort path nobody has waited
             // for the last slices): wait, bounded, for the last `depth` slices issued
-            for (int kt = max(0, issued - depth); kt < issued; ++kt)
-                mbar_wait(&sfull[kt % depth], (uint32_t)(kt / depth) & 1u, nullptr);
+            for (int k = max(0, gs - depth); k < gs; ++k) mbar_wait(&sfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
         }
         __syncwarp();
     } else if (warp < 16) {
         setmaxnreg_inc<kRegsProm>();
         // ------------------------------------------------------------------ promoters (384 threads)
-        // this thread owns TMEM lane 32*q + lane (weight row mrow) and the 32-column chunks cg + 3 i of the tile
-        // (16-column chunks for a stacked tile); three warps a sub-partition hide each other's load latency
+        // this thread owns TMEM lane 32*q + lane (weight row mrow of the item's slice) and the 32-column chunks
+        // cg + 3 i of the tile (16-column chunks for a stacked tile); three warps a sub-partition hide each other's
+        // load latency
         const int q = warp & 3;
         const int cg = (warp - 4) >> 2;  // promoter warpgroup 0..2
         const int mrow = 32 * q + lane;
-        constexpr int kChunks = kMaxBN / 96;           // most 32-column chunks of a thread
-        const int mine = (N / 32 - cg + 2) / 3;        // whole 32-column chunks of this thread
-        const bool half = !stacked && (N & 16) && cg == (N / 32) % 3;  // a last 16-column chunk is this thread's
-        float acc[kChunks][32];
-#pragma unroll
-        for (int i = 0; i < kChunks; ++i)
-#pragma unroll
-            for (int k = 0; k < 32; ++k) acc[i][k] = 0.0f;
+        constexpr int kChunks = kMaxBN / 96;  // most 32-column chunks of a thread
         int b = 0;
         uint32_t bph = 0;
-        for (int g = 0; g < groups && ok; ++g) {
-            if (!mbar_wait(&pfull[b], bph, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + part_base + (uint32_t)(b * bstride);
-            uint32_t v[1][32];
-            if (stacked) {
-                // 16-column chunks cg + 3 i: hi columns c.. and lo columns N + c.., added in turn
-                uint32_t(&h)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0][0]);
-                uint32_t(&l)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0][16]);
+        Item t;
+        for (int item = cid; item < n_items && ok; item += NC) {
+            if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
+            const int N = t.N;
+            const bool stacked = t.stacked;
+            const int mine = (N / 32 - cg + 2) / 3;                         // whole 32-column chunks of this thread
+            const bool half = !stacked && (N & 16) && cg == (N / 32) % 3;  // a last 16-column chunk is this thread's
+            float acc[kChunks][32];
 #pragma unroll
-                for (int i = 0; i < kMaxStackN / 48; ++i) {
-                    const int c = 16 * (cg + 3 * i);
-                    if (c < N) {
-                        tmem_ld_32x32b_x16(base + (uint32_t)c, h);
-                        tmem_ld_32x32b_x16(base + (uint32_t)(N + c), l);
-                        tmem_ld_wait();
-                        float* a = &acc[i >> 1][16 * (i & 1)];
+            for (int i = 0; i < kChunks; ++i)
 #pragma unroll
-                        for (int k = 0; k < 16; k += 2) {
-                            add2(a[k], a[k + 1], h[k], h[k + 1]);
-                            add2(a[k], a[k + 1], l[k], l[k + 1]);
+                for (int k = 0; k < 32; ++k) acc[i][k] = 0.0f;
+            for (int g = 0; g < pitem && ok; ++g) {
+                if (!mbar_wait(&pfull[b], bph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + part_base + (uint32_t)(b * kMaxBN);
+                uint32_t v[32];
+                if (stacked) {
+                    // 16-column chunks cg + 3 i: hi columns c.. and lo columns N + c.., added in turn
+                    uint32_t(&h)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0]);
+                    uint32_t(&l)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[16]);
+#pragma unroll
+                    for (int i = 0; i < kMaxStackN / 48; ++i) {
+                        const int c = 16 * (cg + 3 * i);
+                        if (c < N) {
+                            tmem_ld_32x32b_x16(base + (uint32_t)c, h);
+                            tmem_ld_32x32b_x16(base + (uint32_t)(N + c), l);
+                            tmem_ld_wait();
+                            float* a = &acc[i >> 1][16 * (i & 1)];
+#pragma unroll
+                            for (int k = 0; k < 16; k += 2) {
+                                add2(a[k], a[k + 1], h[k], h[k + 1]);
+                                add2(a[k], a[k + 1], l[k], l[k + 1]);
+                            }
                         }
                     }
-                }
-            } else {
+                } else {
 #pragma unroll
-                for (int i = 0; i < kChunks; ++i) {
-                    if (i < mine) {
-                        tmem_ld_32x32b_x32(base + (uint32_t)(32 * (cg + 3 * i)), v[0]);
+                    for (int i = 0; i < kChunks; ++i) {
+                        if (i < mine) {
+                            tmem_ld_32x32b_x32(base + (uint32_t)(32 * (cg + 3 * i)), v);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int k = 0; k < 32; k += 2) add2(acc[i][k], acc[i][k + 1], v[k], v[k + 1]);
+                        }
+                    }
+                    if (half) {  // the tile's last 16 columns (N = 32 m + 16) into the first half of chunk `mine`
+                        uint32_t(&h)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0]);
+                        tmem_ld_32x32b_x16(base + (uint32_t)(N - 16), h);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int k = 0; k < 32; k += 2) add2(acc[i][k], acc[i][k + 1], v[0][k], v[0][k + 1]);
+                        for (int i = 0; i < kChunks; ++i)
+                            if (i == mine) {
+#pragma unroll
+                                for (int k = 0; k < 16; k += 2) add2(acc[i][k], acc[i][k + 1], h[k], h[k + 1]);
+                            }
                     }
                 }
-                if (half) {  // the tile's last 16 columns (N = 32 m + 16) into the first half of chunk `mine`
-                    uint32_t(&h)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0][0]);
-                    tmem_ld_32x32b_x16(base + (uint32_t)(N - 16), h);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < kChunks; ++i)
-                        if (i == mine) {
-#pragma unroll
-                            for (int k = 0; k < 16; k += 2) add2(acc[i][k], acc[i][k + 1], h[k], h[k + 1]);
-                        }
+                tc_fence_before();
+                mbar_arrive(&pempty[b]);
+                if (++b == nbuf) {
+                    b = 0;
+                    bph ^= 1u;
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&pempty[b]);
-            if (++b == nbuf) {
-                b = 0;
-                bph ^= 1u;
-            }
-        }
-        if (ok) {
-            // ------------------------------------------------------------------ epilogue: fp32 rows out
-            float* outcol = p.out + (m0 + mrow);
+            if (!ok) break;
+            // ---------------------------------------------------------------- epilogue: the item's fp32 rows out
+            float* outcol = p.out + (t.m0 + mrow);
 #pragma unroll
             for (int i = 0; i < kChunks; ++i) {
 #pragma unroll
@@ -455,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                                             : ((i < mine || !half) ? 32 * (cg + 3 * i) + k : (N - 16) + k);
                     const bool mine_k = stacked ? (2 * i + (k >> 4)) < kMaxStackN / 48
                                                 : (i < mine || (half && i == mine && k < 16));
-                    if (mine_k && col < rows) outcol[(int64_t)(row0 + col) * p.a_rows] = acc[i][k];
+                    if (mine_k && col < t.rows) outcol[(int64_t)(t.row0 + col) * p.a_rows] = acc[i][k];
                 }
             }
         }
@@ -465,43 +505,48 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         // thread = weight row ct = TMEM lane of its warp: 64 weights a slice into the 32 columns of A buffer ab
         const int ct = threadIdx.x - 512;
         const uint32_t lane_base = (uint32_t)(ct & ~31) << 16;
-        int r = 0, ab = 0, b = 0;
-        uint32_t rph = 0, aph = 0, bph = 0;  // sfull phase parity; aempty parity of the previous use of buffer ab;
-                                             // pempty parity of the previous use of partial buffer b
-        for (int kt = 0; kt < nk && ok; ++kt) {
-            if (!mbar_wait(&sfull[r], rph, abort_flag) || (kt >= na && !mbar_wait(&aempty[ab], aph, abort_flag))) {
-                ok = false;
-                break;
-            }
-            const uint8_t* wb = ring + r * sbytes + 2 * N * 128;
-            const uint4 codes = *reinterpret_cast<const uint4*>(wb + ct * 16);
-            const __half2 sc = *reinterpret_cast<const __half2*>(wb + 2048 + ct * 4);
-            uint32_t col[32];
-            decode_weights16(codes.x, __low2half2(sc), col);
-            decode_weights16(codes.y, __low2half2(sc), col + 8);
-            decode_weights16(codes.z, __high2half2(sc), col + 16);
-            decode_weights16(codes.w, __high2half2(sc), col + 24);
-            tmem_st_32x32b_x32(tmem + lane_base + (uint32_t)ab * kACols, col);
-            tmem_st_wait();
-            tc_fence_before();
-            // a slice that starts a partial may be multiplied only once the promoters have freed its buffer (a
-            // partial per slice when two-level; one per stream, never reused, otherwise)
-            if (P == 1) {
-                if (ct == 0 && kt >= nbuf && !mbar_wait(&pempty[b], bph, abort_flag)) ok = false;
-                if (++b == nbuf) {
-                    b = 0;
-                    if (kt >= nbuf) bph ^= 1u;
+        int gs = 0, r = 0, ab = 0, pc = 0, pb = 0;  // global slice; ring slot; A buffer; partials started, buffer
+        uint32_t rph = 0, aph = 0, pph = 0;  // sfull parity; aempty parity of the previous use of ab; pempty parity
+        Item t;
+        for (int item = cid; item < n_items && ok; item += NC) {
+            if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
+            for (int kt = 0; kt < nk && ok; ++kt, ++gs) {
+                if (!mbar_wait(&sfull[r], rph, abort_flag) || (gs >= na && !mbar_wait(&aempty[ab], aph, abort_flag))) {
+                    ok = false;
+                    break;
                 }
-            }
-            mbar_arrive(&afull[ab]);
-            mbar_arrive(&sempty[r]);
-            if (++r == depth) {
-                r = 0;
-                rph ^= 1u;
-            }
-            if (++ab == na) {
-                ab = 0;
-                if (kt >= na) aph ^= 1u;
+                const uint8_t* wb = ring + r * sbytes + 2 * t.N * 128;
+                const uint4 codes = *reinterpret_cast<const uint4*>(wb + ct * 16);
+                const __half2 sc = *reinterpret_cast<const __half2*>(wb + 2048 + ct * 4);
+                uint32_t col[16];  // one 32-value block at a time
+                decode_weights16(codes.x, __low2half2(sc), col);
+                decode_weights16(codes.y, __low2half2(sc), col + 8);
+                tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols, col);
+                decode_weights16(codes.z, __high2half2(sc), col);
+                decode_weights16(codes.w, __high2half2(sc), col + 8);
+                tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols + 16u, col);
+                tmem_st_wait();
+                tc_fence_before();
+                // a slice that starts a partial may be multiplied only once the promoters have freed the partial's
+                // buffer (partials start at every slice when two-level, else at the item's first pitem slices)
+                if (p.two_level || kt < pitem) {
+                    if (ct == 0 && pc >= nbuf && !mbar_wait(&pempty[pb], pph, abort_flag)) ok = false;
+                    ++pc;
+                    if (++pb == nbuf) {
+                        pb = 0;
+                        if (pc > nbuf) pph ^= 1u;
+                    }
+                }
+                mbar_arrive(&afull[ab]);
+                mbar_arrive(&sempty[r]);
+                if (++r == depth) {
+                    r = 0;
+                    rph ^= 1u;
+                }
+                if (++ab == na) {
+                    ab = 0;
+                    if (gs >= na) aph ^= 1u;
+                }
             }
         }
     }
@@ -516,8 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         if (C > 1 && lane == 0) {
             // every CTA of the cluster has delivered its last slot releases here (its MMAs are done with them):
             // nothing arrives on this CTA's barriers after it leaves
-            for (int kt = max(0, nk - depth); kt < nk; ++kt)
-                if (!mbar_wait(&sempty[kt % depth], (uint32_t)(kt / depth) & 1u, abort_flag)) break;
+            for (int k = max(0, total - depth); k < total; ++k)
+                if (!mbar_wait(&sempty[k % depth], (uint32_t)(k / depth) & 1u, abort_flag)) break;
         }
         __syncwarp();
         tc_fence_after();
@@ -557,6 +602,9 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uin
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// resident clusters of the kernel per device and cluster size (looked up once)
+int g_resident[64][5] = {};
+
 }  // namespace
 
 cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s) {
@@ -584,7 +632,6 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     const bool large = a.b_rows >= (int64_t)kClusterRows * a.n_experts;
     args.cluster = !large ? 1 : (mt % 4 == 0 ? 4 : (mt % 2 == 0 ? 2 : 1));
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)mt, (unsigned)max_tiles);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
@@ -595,6 +642,22 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // persistent: as many clusters as fit on the GPU at once (each CTA takes a whole SM), at most one per item
+    const int64_t items = max_tiles * (mt / args.cluster);
+    cfg.gridDim = dim3((unsigned)(args.cluster * 512));
+    int resident = 0;
+    if (dev < 64 && args.cluster <= 4 && g_resident[dev][args.cluster] > 0) {
+        resident = g_resident[dev][args.cluster];
+    } else {
+        cudaError_t err = cudaOccupancyMaxActiveClusters(&resident, experts_gemm_kernel, &cfg);
+        if (err != cudaSuccess || resident <= 0) {
+            cudaGetLastError();
+            return err != cudaSuccess ? err : cudaErrorInvalidConfiguration;
+        }
+        if (dev < 64 && args.cluster <= 4) g_resident[dev][args.cluster] = resident;
+    }
+    const int64_t nclusters = items < resident ? items : resident;
+    cfg.gridDim = dim3((unsigned)(nclusters * args.cluster));
     const cudaError_t err = cudaLaunchKernelEx(&cfg, experts_gemm_kernel, args, maps);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
