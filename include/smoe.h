@@ -12,6 +12,7 @@
  *   smoe_gather_q8       the q8 rows of the routed pairs in routed-row order, in operand form
  *   smoe_experts_gateup  grouped gate/up product of each routed row against its expert's 2-bit weights
  *   smoe_swiglu_requant  h = silu(gate) * up, requantised to int8 per 32 values
+ *                        (smoe_experts_gateup_swiglu runs these two steps as one pass)
  *   smoe_experts_down    grouped down product into one fp32 row per routed pair
  *   smoe_combine         Y[t] = sum_k w[t][k] * Dm[slot[t*K+k]] (gather form, no atomics)
  *
@@ -135,6 +136,14 @@ smoe_status smoe_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, in
                          void* stream);
 size_t smoe_pack_q2_bytes(int E, int rows, int cols);
 
+/* Weight preparation for the fused gate/up + SwiGLU product (smoe_experts_gateup_swiglu): the row-major Q2 gate/up
+ * matrix of E experts (codes [E][2F][H/4], scales [E][2F][H/32]; rows [0, F) gate, [F, 2F) up) packed with gate and
+ * up rows interleaved: packed 128-row tile m holds outputs j in [64m, 64m + 64), its row 32a + l being gate row
+ * 64m + 16a + l (l < 16) or up row F + 64m + 16a + l - 16 (l >= 16).  F % 64 == 0, H % 64 == 0.
+ * packed: smoe_pack_q2_bytes(E, 2F, H) bytes. */
+smoe_status smoe_pack_q2_swiglu(const uint8_t* codes, const uint16_t* scales, int E, int F, int H, uint8_t* packed,
+                                void* stream);
+
 /* Step 4a -- routed rows of the q8 activations.  moe_fused.hpp experts() reads each routed row's activations
  * "through the rows of group": this call lays them out once in routed-row order and operand form, so that every
  * tile of the expert products reads its rows as one contiguous block.
@@ -155,6 +164,16 @@ smoe_status smoe_gather_q8(const int8_t* codes, const uint16_t* scales, int64_t 
  *   H % 128 == 0, F % 64 == 0. */
 smoe_status smoe_experts_gateup(const uint16_t* xop, int32_t* tiles, int64_t n, int E, const uint8_t* wgu, int H, int F,
                                 float* gu, void* stream);
+
+/* Steps 4b + 5 fused -- gate/up, SwiGLU and requantisation in one pass (the SwiGLU runs in the product's epilogue on
+ * the fp32 gate and up values; GU is never written).  Same arguments as smoe_experts_gateup with the weights packed
+ * by smoe_pack_q2_swiglu, and the outputs of smoe_swiglu_requant:
+ *   hc int8 [n][F], hs fp16 [n][F/32], hop fp16 [2][n][F] (operand form).
+ * h_j = silu(GU_j) * GU_{F+j} in fp32 and the q8 rule with the scale computed exactly as in smoe_swiglu_requant
+ * (IEEE amax / 127); h and the codes use a reciprocal where that step divides, so a code can differ from
+ * smoe_swiglu_requant's only next to a .5 tie.  GU is the same fp32 sum as smoe_experts_gateup computes. */
+smoe_status smoe_experts_gateup_swiglu(const uint16_t* xop, int32_t* tiles, int64_t n, int E, const uint8_t* wgs, int H,
+                                       int F, int8_t* hc, uint16_t* hs, uint16_t* hop, void* stream);
 
 /* Step 5 -- SwiGLU and requantisation.  Page "src/prefill/prefill.cpp": mmq::swiglu(GU, H, rows, ...) then the
  * int8 rounding of H; moe_fused.hpp: "SwiGLU, H as int8".

@@ -51,10 +51,15 @@ _SIGS = {
     "smoe_pack_q2": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                       ctypes.c_void_p], ctypes.c_int),
     "smoe_pack_q2_bytes": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
+    "smoe_pack_q2_swiglu": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                             ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_gather_q8": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
                         ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_experts_gateup": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
                              ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_experts_gateup_swiglu": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p], ctypes.c_int),
     "smoe_swiglu_requant": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                              ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_experts_down": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
@@ -195,6 +200,20 @@ def smoe_experts_gateup(xop, tiles, n, E, wgu, H, F, gu, stream=None):
         _dev(gu, torch.float32, "gu"), _stream(stream)))
 
 
+def smoe_pack_q2_swiglu(codes, scales, packed, stream=None):
+    """Gate/up Q2 weights (codes uint8 [E][2F][H/4], scales int16 bits [E][2F][H/32]) -> packed for the fused product."""
+    E, rows, c4 = codes.shape
+    _check("smoe_pack_q2_swiglu", load_library().smoe_pack_q2_swiglu(
+        _dev(codes, torch.uint8, "codes"), _dev(scales, torch.int16, "scales"), E, rows // 2, c4 * 4,
+        _dev(packed, torch.uint8, "packed"), _stream(stream)))
+
+
+def smoe_experts_gateup_swiglu(xop, tiles, n, E, wgs, H, F, hc, hs, hop, stream=None):
+    _check("smoe_experts_gateup_swiglu", load_library().smoe_experts_gateup_swiglu(
+        _dev(xop, torch.float16, "xop"), _dev(tiles, torch.int32, "tiles"), n, E, _dev(wgs, torch.uint8, "wgs"), H, F,
+        _dev(hc, torch.int8, "hc"), _dev(hs, torch.int16, "hs"), _dev(hop, torch.float16, "hop"), _stream(stream)))
+
+
 def smoe_swiglu_requant(gu, hc, hs, hop=None, stream=None):
     n, twoF = gu.shape
     _check("smoe_swiglu_requant", load_library().smoe_swiglu_requant(
@@ -269,15 +288,15 @@ class SmoeBlock:
         return h[1], h[3]
 
 
-def pack_weights(codes, scales, device="cuda"):
+def pack_weights(codes, scales, device="cuda", swiglu=False):
     """Row-major Q2 weights (numpy or torch: codes [E][rows][cols/4], scales fp16 bits [E][rows][cols/32]) packed on
-    the device for the expert products."""
+    the device for the expert products; swiglu=True packs a gate/up matrix for the fused gate/up + SwiGLU product."""
     dev = torch.device(device)
     c = codes.to(dev).contiguous() if isinstance(codes, torch.Tensor) else torch.from_numpy(codes).to(dev).contiguous()
     s = _as_i16(scales, dev)
     E, rows, c4 = c.shape
     packed = torch.empty(pack_q2_bytes(E, rows, c4 * 4), dtype=torch.uint8, device=dev)
-    smoe_pack_q2(c, s, packed)
+    (smoe_pack_q2_swiglu if swiglu else smoe_pack_q2)(c, s, packed)
     return packed
 
 

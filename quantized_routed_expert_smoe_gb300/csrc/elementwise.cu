@@ -173,26 +173,39 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 // Q2 weights, row-major [E][rows][cols/4] codes + [E][rows][cols/32] scales, to the expert products' packed form:
 // per (expert, 128-row tile, 64-value slice) one 2560-byte block = the tile's 128 x 16 code bytes, then its 128 x 2
 // scales.  One thread per 16-byte piece of a block (128 code pieces, 32 scale pieces).
+// `half` > 0 packs a gate/up matrix for the fused SwiGLU product: tile mt holds outputs j in [64 mt, 64 mt + 64),
+// and its row 32 q + l is gate row 64 mt + 16 q + l (l < 16) or up row half + 64 mt + 16 q + l - 16 (l >= 16), so
+// that each 32-row warp of the product holds the gate and up rows of the same 16 outputs.
+__device__ __forceinline__ int64_t packed_source_row(int64_t e, int mt, int r, int rows, int half) {
+    if (half <= 0) return e * rows + (int64_t)mt * 128 + r;
+    const int q = r >> 5, l = r & 31;
+    const int j = 64 * mt + 16 * q + (l & 15);
+    return e * rows + (l < 16 ? j : half + j);
+}
+
 __global__ void __launch_bounds__(160) pack_q2_kernel(const uint8_t* __restrict__ codes,
                                                       const uint16_t* __restrict__ scales, int rows, int cols,
-                                                      uint8_t* __restrict__ packed) {
+                                                      int half, uint8_t* __restrict__ packed) {
     const int64_t blk = blockIdx.x;  // ((e * rows/128 + mt) * cols/64 + kt)
     const int nkt = cols / 64, nmt = rows / 128;
     const int kt = (int)(blk % nkt);
     const int64_t emt = blk / nkt;  // e * nmt + mt
-    const int64_t row0 = emt * 128;  // first row of the tile in [E * rows]
-    (void)nmt;
+    const int64_t e = emt / nmt;
+    const int mt = (int)(emt - e * nmt);
     uint8_t* out = packed + blk * 2560;
     const int t = threadIdx.x;
     if (t < 128) {
-        const uint4 v = *reinterpret_cast<const uint4*>(codes + (row0 + t) * (cols / 4) + kt * 16);
+        const int64_t sr = packed_source_row(e, mt, t, rows, half);
+        const uint4 v = *reinterpret_cast<const uint4*>(codes + sr * (cols / 4) + kt * 16);
         *reinterpret_cast<uint4*>(out + t * 16) = v;
     } else {
         const int r = (t - 128) * 4;  // four rows' scale pairs per piece
         uint32_t v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            v[j] = *reinterpret_cast<const uint32_t*>(scales + (row0 + r + j) * (cols / 32) + kt * 2);
+        for (int j = 0; j < 4; ++j) {
+            const int64_t sr = packed_source_row(e, mt, r + j, rows, half);
+            v[j] = *reinterpret_cast<const uint32_t*>(scales + sr * (cols / 32) + kt * 2);
+        }
         *reinterpret_cast<uint4*>(out + 2048 + r * 4) = make_uint4(v[0], v[1], v[2], v[3]);
     }
 }
@@ -204,6 +217,7 @@ __global__ void __launch_bounds__(256) gather_q8_kernel(const uint4* __restrict_
                                                         const uint16_t* __restrict__ scales, int64_t in_rows,
                                                         int groups, const int32_t* __restrict__ src, int64_t n,
                                                         uint4* __restrict__ out) {
+    constexpr int kAhead = 8;  // groups a lane loads before it converts and stores them (cols up to 4096 in one pass)
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t plane = n * groups * 2;  // uint4 words per plane
@@ -213,19 +227,35 @@ __global__ void __launch_bounds__(256) gather_q8_kernel(const uint4* __restrict_
         if (t < 0 || t >= in_rows) {
             for (int g = lane; g < groups; g += 32)
                 o[2 * g] = o[2 * g + 1] = o[plane + 2 * g] = o[plane + 2 * g + 1] = make_uint4(0u, 0u, 0u, 0u);
-        } else {
-            const uint4* i = codes + (int64_t)t * groups;
-            const uint16_t* sc = scales + (int64_t)t * (groups / 2);
-            for (int g = lane; g < groups; g += 32) {
-                const uint4 c = __ldg(i + g);  // values 0..3, 4..7, 8..11, 12..15 of the group
-                const __half2 d2 = __half2half2(__ushort_as_half(__ldg(sc + g / 2)));
-                uint4 hi, lo;
-                split_pairs(interleave_codes8(c.x, c.z), d2, hi, lo);
-                o[2 * g] = hi;
-                o[plane + 2 * g] = lo;
-                split_pairs(interleave_codes8(c.y, c.w), d2, hi, lo);
-                o[2 * g + 1] = hi;
-                o[plane + 2 * g + 1] = lo;
+            continue;
+        }
+        const uint4* i = codes + (int64_t)t * groups;
+        const uint16_t* sc = scales + (int64_t)t * (groups / 2);
+        for (int g0 = lane; g0 < groups; g0 += 32 * kAhead) {
+            // every load of this pass first (independent, in flight together), then the conversions and stores
+            uint4 c[kAhead];
+            uint16_t d[kAhead];
+#pragma unroll
+            for (int k = 0; k < kAhead; ++k) {
+                const int g = g0 + 32 * k;
+                if (g < groups) {
+                    c[k] = __ldg(i + g);  // values 0..3, 4..7, 8..11, 12..15 of the group
+                    d[k] = __ldg(sc + g / 2);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kAhead; ++k) {
+                const int g = g0 + 32 * k;
+                if (g < groups) {
+                    const __half2 d2 = __half2half2(__ushort_as_half(d[k]));
+                    uint4 hi, lo;
+                    split_pairs(interleave_codes8(c[k].x, c[k].z), d2, hi, lo);
+                    o[2 * g] = hi;
+                    o[plane + 2 * g] = lo;
+                    split_pairs(interleave_codes8(c[k].y, c[k].w), d2, hi, lo);
+                    o[2 * g + 1] = hi;
+                    o[plane + 2 * g + 1] = lo;
+                }
             }
         }
     }
@@ -257,11 +287,11 @@ cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc,
     return cudaGetLastError();
 }
 
-cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, uint8_t* packed,
-                           cudaStream_t s) {
+cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, int half,
+                           uint8_t* packed, cudaStream_t s) {
     const int64_t blocks = (int64_t)E * (rows / 128) * (cols / 64);
     if (blocks == 0) return cudaSuccess;
-    pack_q2_kernel<<<(unsigned)blocks, 160, 0, s>>>(codes, scales, rows, cols, packed);
+    pack_q2_kernel<<<(unsigned)blocks, 160, 0, s>>>(codes, scales, rows, cols, half, packed);
     return cudaGetLastError();
 }
 

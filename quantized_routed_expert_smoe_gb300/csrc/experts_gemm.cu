@@ -35,7 +35,9 @@
 //                 parts (16 rows x 128 bytes a load, 128-byte swizzle) and one bulk copy of the packed weight
 //                 block, into a ring slot;
 //   warpgroups 1-3  promoters: add each finished partial into fp32 registers (a TMEM lane a thread, every third
-//                 32-column chunk a warpgroup), then write the fp32 rows;
+//                 32-column chunk a warpgroup), then write the fp32 rows -- or, for the fused SwiGLU product (gate
+//                 and up rows interleaved in the packed weights), h = silu(g) * u requantised to q8, planar and in
+//                 operand form;
 //   warpgroup 4   converters: thread = weight row: decode its 64 weights of the slice into the slice's A buffer in
 //                 tensor memory.
 // Tensor memory (512 columns): 2 to 8 A buffers of 32 columns (more for small tiles, so that the converters run
@@ -76,13 +78,14 @@ constexpr int kMaxStackN = 96;                 // tiles up to this N stack hi an
 constexpr int kClusterRows = 96;               // mean rows per expert from which CTAs of a tile form a cluster
 constexpr int kSmemBytes = 232448;             // the per-CTA maximum (227 KB): [align slack][ring][barriers]
 constexpr int kBarBytes = 512;
-constexpr int kRingBytes = kSmemBytes - 1024 - kBarBytes;
+constexpr int kScratchBytes = SMOE_TILE_ROWS * 4 * 4;  // SwiGLU epilogue: a warp's block amax per column [col][4]
+constexpr int kRingBytes = kSmemBytes - 1024 - kBarBytes - kScratchBytes;
 // registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 40, the converters
-// to 56 and the promoters take 120: 128 x 40 + 384 x 120 + 128 x 56 = 58,368 <= 61,440.  Per SM sub-partition (one
-// warp of each warpgroup): 32 x (40 + 3 x 120 + 56) = 14,592 <= 16,384.
+// to 56 and the promoters take 128: 128 x 40 + 384 x 128 + 128 x 56 = 61,440.  Per SM sub-partition (one warp of
+// each warpgroup): 32 x (40 + 3 x 128 + 56) = 15,360 <= 16,384.
 constexpr int kRegsWg0 = 40;
 constexpr int kRegsConv = 56;
-constexpr int kRegsProm = 120;
+constexpr int kRegsProm = 128;
 static_assert(128 * kRegsWg0 + kConverters * kRegsConv + kPromoters * kRegsProm <= kThreads * 96,
               "register split exceeds the launch");
 static_assert(kMaxBN <= 224 && kMaxBN % 32 == 0, "two partial buffers and two A buffers must fit in tensor memory");
@@ -136,6 +139,22 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 // every thread of every CTA of the cluster
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// named barrier of `count` threads (whole warps)
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// named barrier that also returns whether `pred` held in every participating thread
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 template <uint32_t N>
@@ -271,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     uint64_t* accf = pempty + kMaxBufs;     // every MMA has completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* scratch = reinterpret_cast<float*>(smem_raw + kSmemBytes - kBarBytes - kScratchBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -483,19 +503,84 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     bph ^= 1u;
                 }
             }
-            if (!ok) break;
-            // ---------------------------------------------------------------- epilogue: the item's fp32 rows out
-            float* outcol = p.out + (t.m0 + mrow);
+            // the item's outputs; column col of chunk slot (i, k), as the partials were added
+            auto column = [&](int i, int k) {
+                // a stacked tile's 16-column chunk j = cg + 3 i' sits at acc[i' / 2][16 (i' % 2) ..]
+                return stacked ? 16 * (cg + 3 * (2 * i + (k >> 4))) + (k & 15)
+                               : ((i < mine || !half) ? 32 * (cg + 3 * i) + k : (N - 16) + k);
+            };
+            auto owned = [&](int i, int k) {
+                return stacked ? (2 * i + (k >> 4)) < kMaxStackN / 48 : (i < mine || (half && i == mine && k < 16));
+            };
+            if (p.hc == nullptr) {
+                if (!ok) break;
+                // ------------------------------------------------------------ epilogue: fp32 rows out
+                float* outcol = p.out + (t.m0 + mrow);
 #pragma unroll
-            for (int i = 0; i < kChunks; ++i) {
+                for (int i = 0; i < kChunks; ++i) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    // a stacked tile's 16-column chunk j = cg + 3 i' sits at acc[i' / 2][16 (i' % 2) ..]
-                    const int col = stacked ? 16 * (cg + 3 * (2 * i + (k >> 4))) + (k & 15)
-                                            : ((i < mine || !half) ? 32 * (cg + 3 * i) + k : (N - 16) + k);
-                    const bool mine_k = stacked ? (2 * i + (k >> 4)) < kMaxStackN / 48
-                                                : (i < mine || (half && i == mine && k < 16));
-                    if (mine_k && col < t.rows) outcol[(int64_t)(t.row0 + col) * p.a_rows] = acc[i][k];
+                    for (int k = 0; k < 32; ++k) {
+                        const int col = column(i, k);
+                        if (owned(i, k) && col < t.rows) outcol[(int64_t)(t.row0 + col) * p.a_rows] = acc[i][k];
+                    }
+                }
+            } else {
+                // ------------------------------------------------------------ epilogue: SwiGLU + requantisation
+                // the weights are packed interleaved: lane l < 16 holds gate output j, lane l + 16 the up output of
+                // the same j, and the 16 outputs of a warp are one operand-form group.  h = silu(g) * u and the q8
+                // rule with the scale exactly as in the SwiGLU step (IEEE amax / 127); h and the codes use a
+                // reciprocal instead of a division (a code can differ from the SwiGLU step's only next to a .5
+                // tie).  The 32-value block of h spans warps q and q ^ 1.
+                if (!bar_red_and(1 + cg, 128, ok)) {  // every thread of the warpgroup takes the same way out
+                    ok = false;
+                    break;
+                }
+                const int Fh = p.a_rows >> 1;
+                const int jl = lane & 15;
+                const bool gate = lane < 16;
+                const int j = (t.m0 >> 1) + 16 * q + jl;
+                const int pos = jl < 8 ? 2 * jl : 2 * (jl - 8) + 1;  // operand-form position within the group
+                int8_t* const hc0 = p.hc + (int64_t)t.row0 * Fh + j;
+                uint16_t* const hi0 = p.hop + (int64_t)t.row0 * Fh + (j - jl) + pos;
+                uint16_t* const lo0 = hi0 + p.b_rows * Fh;
+                uint16_t* const hs0 = p.hs + (int64_t)t.row0 * (Fh / 32) + (j >> 5);
+#pragma unroll
+                for (int i = 0; i < kChunks; ++i) {  // a chunk at a time: fewer values live at once
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int col = column(i, k);
+                        if (owned(i, k) && col < N) {  // the same in every lane of the warp
+                            const float g = acc[i][k];
+                            const float u = __shfl_down_sync(0xffffffffu, g, 16);
+                            const float h = gate ? g * u * __frcp_rn(1.0f + __expf(-g)) : 0.0f;
+                            acc[i][k] = h;
+                            // |h| compares as its bit pattern; the up lanes give 0
+                            const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
+                            if (lane == 0) scratch[col * 4 + q] = __uint_as_float(m);
+                        }
+                    }
+                    bar_sync(1 + cg, 128);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int col = column(i, k);
+                        if (owned(i, k) && col < t.rows) {
+                            const float amax = fmaxf(scratch[col * 4 + q], scratch[col * 4 + (q ^ 1)]);
+                            const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
+                            const float d = __half2float(dh);
+                            const int off = col * Fh;
+                            if (gate) {
+                                float qf = 0.0f;
+                                if (d != 0.0f) qf = fminf(fmaxf(roundf(acc[i][k] * __frcp_rn(d)), -127.0f), 127.0f);
+                                hc0[off] = (int8_t)(int)qf;
+                                const __half qh = __float2half_rn(qf);
+                                const __half hi = __hmul(qh, dh);
+                                hi0[off] = __half_as_ushort(hi);
+                                lo0[off] = __half_as_ushort(__hfma(qh, dh, __hneg(hi)));
+                            }
+                            if (lane == 0 && (q & 1) == 0) hs0[col * (Fh / 32)] = __half_as_ushort(dh);
+                        }
+                    }
+                    bar_sync(1 + cg, 128);  // the scratch is reused by the next chunk
                 }
             }
         }

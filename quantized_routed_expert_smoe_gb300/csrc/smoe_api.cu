@@ -110,7 +110,16 @@ smoe_status smoe_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, in
     if (!aligned16(codes) || !aligned16(scales) || !aligned16(packed)) return SMOE_ERR_ARG;
     if ((int64_t)E * (rows / 128) * (cols / 64) > INT32_MAX) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    return launch_status(smoe::launch_pack_q2(codes, scales, E, rows, cols, packed, (cudaStream_t)stream));
+    return launch_status(smoe::launch_pack_q2(codes, scales, E, rows, cols, 0, packed, (cudaStream_t)stream));
+}
+
+smoe_status smoe_pack_q2_swiglu(const uint8_t* codes, const uint16_t* scales, int E, int F, int H, uint8_t* packed,
+                                void* stream) {
+    if (E < 1 || F < 64 || H < 64 || F % 64 != 0 || H % 64 != 0) return SMOE_ERR_ARG;
+    if (!aligned16(codes) || !aligned16(scales) || !aligned16(packed)) return SMOE_ERR_ARG;
+    if ((int64_t)E * (2 * F / 128) * (H / 64) > INT32_MAX) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_pack_q2(codes, scales, E, 2 * F, H, F, packed, (cudaStream_t)stream));
 }
 
 static smoe_status check_gemm_shape(int64_t n, int E, int H, int F) {
@@ -138,7 +147,20 @@ smoe_status smoe_experts_gateup(const uint16_t* xop, int32_t* tiles, int64_t n, 
     if (n == 0) return SMOE_OK;
     if (!aligned16(xop) || !aligned16(tiles) || !aligned16(wgu) || !aligned16(gu)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{xop, tiles, wgu, 2 * F, H, gu, n, E, true, 1};
+    smoe::ExpertsGemmArgs a{xop, tiles, wgu, 2 * F, H, gu, n, E, true, 1, nullptr, nullptr, nullptr};
+    return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
+}
+
+smoe_status smoe_experts_gateup_swiglu(const uint16_t* xop, int32_t* tiles, int64_t n, int E, const uint8_t* wgs, int H,
+                                       int F, int8_t* hc, uint16_t* hs, uint16_t* hop, void* stream) {
+    const smoe_status st = check_gemm_shape(n, E, H, F);
+    if (st != SMOE_OK) return st;
+    if (n == 0) return SMOE_OK;
+    if (!aligned16(xop) || !aligned16(tiles) || !aligned16(wgs) || !aligned16(hc) || !aligned16(hs) ||
+        !aligned16(hop))
+        return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    smoe::ExpertsGemmArgs a{xop, tiles, wgs, 2 * F, H, nullptr, n, E, true, 1, hc, hs, hop};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 
@@ -160,7 +182,7 @@ smoe_status smoe_experts_down(const uint16_t* hop, int32_t* tiles, int64_t n, in
     if (n == 0) return SMOE_OK;
     if (!aligned16(hop) || !aligned16(tiles) || !aligned16(wd) || !aligned16(dm)) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    smoe::ExpertsGemmArgs a{hop, tiles, wd, H, F, dm, n, E, false, 1};
+    smoe::ExpertsGemmArgs a{hop, tiles, wd, H, F, dm, n, E, false, 1, nullptr, nullptr, nullptr};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 

@@ -17,8 +17,8 @@ cudaError_t launch_quantize_q8(const float* x, int64_t rows, int cols, int8_t* c
                                cudaStream_t s);
 cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint16_t* hop,
                                   cudaStream_t s);
-cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, uint8_t* packed,
-                           cudaStream_t s);
+cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, int half,
+                           uint8_t* packed, cudaStream_t s);
 cudaError_t launch_gather_q8(const int8_t* codes, const uint16_t* scales, int64_t in_rows, int cols,
                              const int32_t* src, int64_t n, uint16_t* out, cudaStream_t s);
 cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
@@ -33,11 +33,15 @@ struct ExpertsGemmArgs {
     const uint8_t* wp;    // packed weights: per (expert, 128-row tile, 64-value slice) 2560 bytes
     int a_rows;           // weight rows per expert (2F or H)
     int K;                // contraction length (H or F)
-    float* out;           // [b_rows][a_rows]
+    float* out;           // [b_rows][a_rows] (null in SwiGLU mode)
     int64_t b_rows;       // n
     int n_experts;        // E
     bool two_level;       // add every 64-wide K slice into fp32 registers (gate/up); else one accumulator over K
     int cluster;          // CTAs per cluster sharing a tile's rows (set by the launcher)
+    // SwiGLU mode (gate/up with weights packed interleaved): h = silu(gate) * up requantised in the epilogue
+    int8_t* hc;           // [b_rows][a_rows / 2] q8 codes of h, or null: fp32 rows to `out`
+    uint16_t* hs;         // [b_rows][a_rows / 64] fp16 scales
+    uint16_t* hop;        // [2][b_rows][a_rows / 2] h in operand form
 };
 cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s);
 

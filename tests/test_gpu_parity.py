@@ -269,6 +269,72 @@ def test_pack_q2_layout(B):
         assert np.array_equal(got, packed_q2(c, s))
 
 
+def swiglu_rows(F):
+    """Source row of each packed row for the fused gate/up + SwiGLU product (gate and up rows interleaved)."""
+    out = []
+    for m in range(2 * F // 128):
+        for r in range(128):
+            q, l = r >> 5, r & 31
+            j = 64 * m + 16 * q + (l & 15)
+            out.append(j if l < 16 else F + j)
+    return np.array(out)
+
+
+def test_pack_q2_swiglu_layout(B):
+    inp = synth.make_custom(T=4, H=256, E=3, K=1, F=128, seed=19)
+    perm = swiglu_rows(128)
+    got = host(B.pack_weights(inp["wgu_c"], inp["wgu_s"], swiglu=True))
+    want = packed_q2(np.ascontiguousarray(inp["wgu_c"][:, perm]), np.ascontiguousarray(inp["wgu_s"][:, perm]))
+    assert np.array_equal(got, want)
+
+
+def check_requant(c, s, co, so, h, what):
+    """q8 of h from two computations of the same values: scales equal or amax/127 within 1e-5 of an fp16 midpoint;
+    codes equal in equal-scale blocks except at most 1e-4 of them, each by 1 and within 1e-3 of a .5 tie."""
+    n, F = c.shape
+    d = so.view(np.float16).astype(np.float64)
+    sbad = s != so
+    if sbad.any():
+        amax = np.abs(h.reshape(n, F // 32, 32)).max(axis=2)[sbad] / 127.0
+        lo = np.minimum(s[sbad], so[sbad]).view(np.float16).astype(np.float64)
+        hi = np.maximum(s[sbad], so[sbad]).view(np.float16).astype(np.float64)
+        assert np.all(np.abs(amax - 0.5 * (lo + hi)) <= 1e-5 * amax), what
+    same_blocks = np.repeat(~sbad, 32, axis=1)
+    cbad = (c != co) & same_blocks
+    assert cbad.sum() <= 1e-4 * c.size, what
+    if cbad.any():
+        ratio = h / np.repeat(d, 32, axis=1)
+        assert np.all(np.abs(c[cbad].astype(int) - co[cbad].astype(int)) == 1), what
+        assert np.all(np.abs(np.abs(ratio[cbad]) % 1.0 - 0.5) <= 1e-3), what
+
+
+@pytest.mark.parametrize("shape", [(256, 512, 8, 4, 256), (192, 256, 64, 2, 128), (61, 384, 5, 3, 192)])
+def test_gateup_swiglu_fused(B, shape):
+    """The fused gate/up + SwiGLU + requant product against the oracle's gate/up (double) and the oracle's SwiGLU +
+    requant of it: large tiles in clusters of 4 (128 rows an expert), small stacked tiles, and a ragged shape
+    (F = 192: three 64-output tiles, a 3-slice K)."""
+    T, H, E, K, F = shape
+    inp = synth.make_custom(T=T, H=H, E=E, K=K, F=F, seed=23 + T)
+    ids, _ = oracle.route(inp["logits"], K)
+    g = oracle.group(ids, E)
+    n = T * K
+    xc, xs = oracle.quantize_q8(inp["x"])
+    src = g["src"].astype(np.int64)
+    tiles = _tiles_dev(B, g, n, E)
+    wp = B.pack_weights(inp["wgu_c"], inp["wgu_s"], swiglu=True)
+    hc = torch.full((n, F), 99, dtype=torch.int8, device="cuda")
+    hs = torch.zeros((n, F // 32), dtype=torch.int16, device="cuda")
+    hop = torch.full((2, n, F), float("nan"), dtype=torch.float16, device="cuda")
+    B.smoe_experts_gateup_swiglu(dev(to_operand(xc[src], xs[src])), tiles, n, E, wp, H, F, hc, hs, hop)
+    assert host(tiles)[3] == 0
+    c, s = host(hc), host(hs).view(np.uint16)
+    assert np.array_equal(host(hop), to_operand(c, s))
+    gu = oracle.gateup(xc, xs, g["src"], g["offsets"], inp["wgu_c"], inp["wgu_s"], H, F).astype(np.float32)
+    co, so = oracle.swiglu_requant(gu, F)
+    gg, uu = gu[:, :F].astype(np.float64), gu[:, F:].astype(np.float64)
+    check_requant(c, s, co, so, gg * scipy.special.expit(gg) * uu, f"fused {shape}")
+
+
 def rows_of(t, rows):
     return host(t[torch.from_numpy(np.ascontiguousarray(rows, dtype=np.int64)).cuda()])
 
@@ -397,22 +463,7 @@ def test_swiglu_requant_parity(B):
     co, so = oracle.swiglu_requant(gu, F)
     g = gu[:, :F].astype(np.float64)
     u = gu[:, F:].astype(np.float64)
-    h = g * scipy.special.expit(g) * u
-    d = so.view(np.float16).astype(np.float64)
-    # scales: equal, or amax/127 within 1e-5 of an fp16 rounding midpoint
-    sbad = s != so
-    if sbad.any():
-        amax = np.abs(h.reshape(n, F // 32, 32)).max(axis=2)[sbad] / 127.0
-        lo = np.minimum(s[sbad], so[sbad]).view(np.float16).astype(np.float64)
-        hi = np.maximum(s[sbad], so[sbad]).view(np.float16).astype(np.float64)
-        assert np.all(np.abs(amax - 0.5 * (lo + hi)) <= 1e-5 * amax)
-    same_blocks = np.repeat(~sbad, 32, axis=1)
-    cbad = (c != co) & same_blocks
-    assert cbad.sum() <= 1e-4 * c.size
-    if cbad.any():
-        ratio = h / np.repeat(d, 32, axis=1)
-        assert np.all(np.abs(c[cbad].astype(int) - co[cbad].astype(int)) == 1)
-        assert np.all(np.abs(np.abs(ratio[cbad]) % 1.0 - 0.5) <= 1e-3)
+    check_requant(c, s, co, so, g * scipy.special.expit(g) * u, "swiglu")
 
 
 # ------------------------------------------------------------------------------------------------ combine
