@@ -31,9 +31,9 @@
 // setmaxnreg:
 //   warpgroup 0   warps 0 and 2, one lane each: the MMAs of alternate slices (four K16 steps x two parts a slice;
 //                 one thread's waits overlap the other's MMAs); warp 0 also allocates the tensor memory;
-//                 warp 1, one lane: the producer -- per 64-wide K slice, TMA tile loads of the tile's rows of both
-//                 parts (16 rows x 128 bytes a load, 128-byte swizzle) and one bulk copy of the packed weight
-//                 block, into a ring slot;
+//                 warp 1: the producer -- per 64-wide K slice, TMA tile loads of the tile's rows of both parts (16
+//                 rows x 128 bytes a load, 128-byte swizzle) and one bulk copy of the packed weight block into a
+//                 ring slot, a copy per lane;
 //   warpgroups 1-3  promoters: add each finished partial into fp32 registers (a TMEM lane a thread, every third
 //                 32-column chunk a warpgroup), then write the fp32 rows -- or, for the fused SwiGLU product (gate
 //                 and up rows interleaved in the packed weights), h = silu(g) * u requantised to q8, planar and in
@@ -91,13 +91,17 @@ static_assert(128 * kRegsWg0 + kConverters * kRegsConv + kPromoters * kRegsProm 
 static_assert(kMaxBN <= 224 && kMaxBN % 32 == 0, "two partial buffers and two A buffers must fit in tensor memory");
 static_assert(kMaxBN % 96 == 0, "the promoter warpgroups take whole 32-column chunks in turn");
 
-// Ring slot (one 64-wide K slice of the tile): the tile's N rows of the hi part, then of the lo part (N x 128 bytes
-// each, 128-byte swizzle, 1024-aligned), then the packed weight block (codes [128][16 B], scales [128][4 B]); slots
-// are 1024-byte multiples.
+// Ring slot (one 64-wide K slice of the tile): the rows of the hi part, then of the lo part (128 bytes a row,
+// 128-byte swizzle, 1024-aligned), then the packed weight block (codes [128][16 B], scales [128][4 B]); slots are
+// 1024-byte multiples.  A stacked tile's lo rows follow its N hi rows (one MMA reads both); a larger tile's parts
+// take fixed regions of kMaxBN rows each, filled by 64-row boxes (rows past N are loaded and never read).
 constexpr int kWBlock = 2560;
-constexpr int kRowBox = 16;                    // B rows per TMA load
+constexpr int kRowBox = 16;                    // B rows per TMA load of a stacked tile
+constexpr int kBigBox = 64;                    // B rows per TMA load of a larger tile (the TMA unit takes a copy per
+                                               // ~100 cycles whatever its size, so larger tiles use fewer, larger ones)
 __host__ __device__ constexpr int slot_bytes(int N) { return (2 * N * 128 + kWBlock + 1023) & ~1023; }
 static_assert(kRingBytes / slot_bytes(kMaxBN) >= 3, "the ring must hold three slices of a full tile");
+static_assert(kMaxBN % kBigBox == 0 && kMaxStackN % kRowBox == 0, "boxes fill a part's region exactly");
 
 // bulk copy (no tensor map) of `bytes` (a multiple of 16) into shared memory, completing on `bar`
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -223,7 +227,8 @@ __device__ __forceinline__ void decode_weights16(uint32_t codes, __half2 d2, uin
 }
 
 struct GemmMaps {
-    CUtensorMap hi, lo;  // the two parts of the B rows: fp16 [b_rows][K] each, box 64 x 16, 128-byte swizzle
+    // the two parts of the B rows: fp16 [b_rows][K] each, 128-byte swizzle; boxes of 64 values x 16 or 64 rows
+    CUtensorMap hi, lo, hi64, lo64;
 };
 
 // One work item: a tile of the tile list x one group of C consecutive 128-row weight slices (one per CTA of the
@@ -232,6 +237,9 @@ struct Item {
     int e, row0, rows, N, m0;
     bool stacked;  // N <= kMaxStackN: hi and lo rows in one MMA of 2N columns
     int ncols;     // partial columns
+    int lo_rows;   // slot row where the lo part starts (N stacked, kMaxBN otherwise)
+    int box;       // rows per TMA box
+    int nbox;      // boxes per part
 };
 __device__ __forceinline__ bool load_item(const int32_t* tiles, int item, int mgroups, int C, uint32_t crank,
                                           const ExpertsGemmArgs& p, Item& t) {
@@ -248,6 +256,9 @@ __device__ __forceinline__ bool load_item(const int32_t* tiles, int item, int mg
     t.m0 = (mg * C + (int)crank) * kBM;
     t.stacked = t.N <= kMaxStackN;
     t.ncols = t.stacked ? 2 * t.N : t.N;
+    t.lo_rows = t.stacked ? t.N : kMaxBN;
+    t.box = t.stacked ? kRowBox : kBigBox;
+    t.nbox = (t.N + t.box - 1) / t.box;
     return true;
 }
 
@@ -349,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t hi = ring_s + (uint32_t)(r * sbytes), lo = hi + (uint32_t)(t.N * 128);
+                    const uint32_t hi = ring_s + (uint32_t)(r * sbytes), lo = hi + (uint32_t)(t.lo_rows * 128);
                     const uint32_t d = tmem + part_base + (uint32_t)(b * kMaxBN);
                     const uint32_t a = tmem + (uint32_t)ab * kACols;
                     if (t.stacked) {
@@ -380,8 +391,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             }
             total = base;
             mma_commit(accf);  // completes once every MMA issued above has completed (abort path included)
-        } else if (warp == 1 && lane == 0) {
-            // ------------------------------------------------------------------ producer (one thread)
+        } else if (warp == 1) {
+            // ------------------------------------------------------------------ producer (one warp)
+            // lane 0 waits for the slot and posts its byte count; then every lane issues one or two of the slice's
+            // copies (a TMA instruction costs its issuing thread ~100 cycles, so one thread could not keep up)
+            if (lane < 4) {
+                const CUtensorMap* m = lane == 0 ? &maps.hi : (lane == 1 ? &maps.lo : (lane == 2 ? &maps.hi64 : &maps.lo64));
+                asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
+            }
             int gs = 0, r = 0;
             uint32_t eph = 0;  // parity of the sempty phase the next wrap waits for
             Item t;
@@ -389,28 +406,32 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
                 const uint8_t* wblocks =
                     p.wp + ((int64_t)t.e * (p.a_rows / kBM) + t.m0 / kBM) * nk * (int64_t)kWBlock;
-                const uint32_t tx_bytes = 2u * (uint32_t)t.N * 128u + (uint32_t)kWBlock;
+                const uint32_t tx_bytes = 2u * (uint32_t)(t.nbox * t.box) * 128u + (uint32_t)kWBlock;
+                // this CTA's boxes of a part: every C-th from box crank (all of them without a cluster)
+                const int nbox = (t.nbox - (int)crank + C - 1) / C;
+                const CUtensorMap* const mhi = t.stacked ? &maps.hi : &maps.hi64;
+                const CUtensorMap* const mlo = t.stacked ? &maps.lo : &maps.lo64;
                 for (int kt = 0; kt < nk; ++kt, ++gs) {
-                    if (gs >= depth && !mbar_wait(&sempty[r], eph, abort_flag)) {
+                    bool go = true;
+                    if (lane == 0) {
+                        if (gs >= depth && !mbar_wait(&sempty[r], eph, abort_flag)) go = false;
+                        else mbar_arrive_expect_tx(&sfull[r], tx_bytes);
+                    }
+                    if (!__shfl_sync(0xffffffffu, go, 0)) {
                         ok = false;
                         break;
                     }
                     const uint32_t slot = ring_s + (uint32_t)(r * sbytes);
-                    mbar_arrive_expect_tx(&sfull[r], tx_bytes);
-                    bulk_load(slot + (uint32_t)(2 * t.N * 128), wblocks + (int64_t)kt * kWBlock, kWBlock, &sfull[r]);
-                    if (C > 1) {
-                        for (int b0 = kRowBox * (int)crank; b0 < t.N; b0 += kRowBox * C) {
-                            tma_load_2d_mc(slot + (uint32_t)(b0 * 128), &maps.hi, kt * kBK, t.row0 + b0, &sfull[r],
-                                           cmask);
-                            tma_load_2d_mc(slot + (uint32_t)((t.N + b0) * 128), &maps.lo, kt * kBK, t.row0 + b0,
-                                           &sfull[r], cmask);
-                        }
-                    } else {
-                        for (int b0 = 0; b0 < t.N; b0 += kRowBox) {
-                            tma_load_2d(slot + (uint32_t)(b0 * 128), &maps.hi, kt * kBK, t.row0 + b0, &sfull[r]);
-                            tma_load_2d(slot + (uint32_t)((t.N + b0) * 128), &maps.lo, kt * kBK, t.row0 + b0,
-                                        &sfull[r]);
-                        }
+                    if (lane == 31)
+                        bulk_load(slot + (uint32_t)(2 * t.lo_rows * 128), wblocks + (int64_t)kt * kWBlock, kWBlock,
+                                  &sfull[r]);
+                    for (int f = lane; f < 2 * nbox; f += 32) {  // box f: part f / nbox, box f % nbox of this CTA
+                        const int part = f >= nbox, i = part ? f - nbox : f;
+                        const int b0 = t.box * ((int)crank + C * i);
+                        const uint32_t dst = slot + (uint32_t)((part ? t.lo_rows + b0 : b0) * 128);
+                        const CUtensorMap* map = part ? mlo : mhi;
+                        if (C > 1) tma_load_2d_mc(dst, map, kt * kBK, t.row0 + b0, &sfull[r], cmask);
+                        else tma_load_2d(dst, map, kt * kBK, t.row0 + b0, &sfull[r]);
                     }
                     if (++r == depth) {
                         r = 0;
@@ -420,7 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             }
             // no copy may still be writing shared memory when the CTA exits (on the abort path nobody has waited
             // for the last slices): wait, bounded, for the last `depth` slices issued
-            for (int k = max(0, gs - depth); k < gs; ++k) mbar_wait(&sfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
+            if (lane == 0)
+                for (int k = max(0, gs - depth); k < gs; ++k)
+                    mbar_wait(&sfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
         }
         __syncwarp();
     } else if (warp < 16) {
@@ -600,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     ok = false;
                     break;
                 }
-                const uint8_t* wb = ring + r * sbytes + 2 * t.N * 128;
+                const uint8_t* wb = ring + r * sbytes + 2 * t.lo_rows * 128;
                 const uint4 codes = *reinterpret_cast<const uint4*>(wb + ct * 16);
                 const __half2 sc = *reinterpret_cast<const __half2*>(wb + 2048 + ct * 4);
                 uint32_t col[16];  // one 32-value block at a time
@@ -708,7 +731,11 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     if (!make_map(&maps.hi, a.bop, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
                   kRowBox, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.lo, lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK, kRowBox,
-                  CU_TENSOR_MAP_SWIZZLE_128B))
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&maps.hi64, a.bop, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
+                  kBigBox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&maps.lo64, lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
+                  kBigBox, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int mt = a.a_rows / kBM;
     ExpertsGemmArgs args = a;
