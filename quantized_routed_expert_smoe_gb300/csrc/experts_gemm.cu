@@ -31,9 +31,9 @@
 // setmaxnreg:
 //   warpgroup 0   warps 0 and 2, one lane each: the MMAs of alternate slices (four K16 steps x two parts a slice;
 //                 one thread's waits overlap the other's MMAs); warp 0 also allocates the tensor memory;
-//                 warp 1: the producer -- per 64-wide K slice, TMA tile loads of the tile's rows of both parts (16
-//                 rows x 128 bytes a load, 128-byte swizzle) and one bulk copy of the packed weight block into a
-//                 ring slot, a copy per lane;
+//                 warp 1: the producer -- per 64-wide K slice, one TMA tile load of the tile's rows of each part
+//                 (128-byte swizzle; in a cluster, multicast by one CTA to all) and one bulk copy of the packed
+//                 weight block into a ring slot;
 //   warpgroups 1-3  promoters: add each finished partial into fp32 registers (a TMEM lane a thread, every third
 //                 32-column chunk a warpgroup), then write the fp32 rows -- or, for the fused SwiGLU product (gate
 //                 and up rows interleaved in the packed weights), h = silu(g) * u requantised to q8, planar and in
@@ -94,14 +94,15 @@ static_assert(kMaxBN % 96 == 0, "the promoter warpgroups take whole 32-column ch
 // Ring slot (one 64-wide K slice of the tile): the rows of the hi part, then of the lo part (128 bytes a row,
 // 128-byte swizzle, 1024-aligned), then the packed weight block (codes [128][16 B], scales [128][4 B]); slots are
 // 1024-byte multiples.  A stacked tile's lo rows follow its N hi rows (one MMA reads both); a larger tile's parts
-// take fixed regions of kMaxBN rows each, filled by 64-row boxes (rows past N are loaded and never read).
+// take fixed regions of kMaxBN rows each (rows past N are loaded and never read).
 constexpr int kWBlock = 2560;
-constexpr int kRowBox = 16;                    // B rows per TMA load of a stacked tile
-constexpr int kBigBox = 64;                    // B rows per TMA load of a larger tile (the TMA unit takes a copy per
-                                               // ~100 cycles whatever its size, so larger tiles use fewer, larger ones)
+// One TMA copy per part and slice (the TMA unit takes a copy per ~100 cycles whatever its size): a stacked tile of
+// N = 16 m rows uses the map whose box is N rows; a larger tile a box of kMaxBN rows into its part's fixed region.
+constexpr int kRowBox = 16;                    // box-height step of the stacked maps
+constexpr int kNumMaps = kMaxStackN / kRowBox + 1;
 __host__ __device__ constexpr int slot_bytes(int N) { return (2 * N * 128 + kWBlock + 1023) & ~1023; }
 static_assert(kRingBytes / slot_bytes(kMaxBN) >= 3, "the ring must hold three slices of a full tile");
-static_assert(kMaxBN % kBigBox == 0 && kMaxStackN % kRowBox == 0, "boxes fill a part's region exactly");
+static_assert(kMaxStackN % kRowBox == 0 && kMaxBN <= 256, "box heights");
 
 // bulk copy (no tensor map) of `bytes` (a multiple of 16) into shared memory, completing on `bar`
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -227,8 +228,9 @@ __device__ __forceinline__ void decode_weights16(uint32_t codes, __half2 d2, uin
 }
 
 struct GemmMaps {
-    // the two parts of the B rows: fp16 [b_rows][K] each, 128-byte swizzle; boxes of 64 values x 16 or 64 rows
-    CUtensorMap hi, lo, hi64, lo64;
+    // the two parts of the B rows: fp16 [b_rows][K] each, 128-byte swizzle, boxes of 64 values x 16 (m + 1) rows
+    // (m < kNumMaps - 1) or x kMaxBN rows (m = kNumMaps - 1)
+    CUtensorMap hi[kNumMaps], lo[kNumMaps];
 };
 
 // One work item: a tile of the tile list x one group of C consecutive 128-row weight slices (one per CTA of the
@@ -238,8 +240,7 @@ struct Item {
     bool stacked;  // N <= kMaxStackN: hi and lo rows in one MMA of 2N columns
     int ncols;     // partial columns
     int lo_rows;   // slot row where the lo part starts (N stacked, kMaxBN otherwise)
-    int box;       // rows per TMA box
-    int nbox;      // boxes per part
+    int map;       // tensor maps of its parts (one box per part)
 };
 __device__ __forceinline__ bool load_item(const int32_t* tiles, int item, int mgroups, int C, uint32_t crank,
                                           const ExpertsGemmArgs& p, Item& t) {
@@ -257,8 +258,7 @@ __device__ __forceinline__ bool load_item(const int32_t* tiles, int item, int mg
     t.stacked = t.N <= kMaxStackN;
     t.ncols = t.stacked ? 2 * t.N : t.N;
     t.lo_rows = t.stacked ? t.N : kMaxBN;
-    t.box = t.stacked ? kRowBox : kBigBox;
-    t.nbox = (t.N + t.box - 1) / t.box;
+    t.map = t.stacked ? t.N / kRowBox - 1 : kNumMaps - 1;
     return true;
 }
 
@@ -395,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             // ------------------------------------------------------------------ producer (one warp)
             // lane 0 waits for the slot and posts its byte count; then every lane issues one or two of the slice's
             // copies (a TMA instruction costs its issuing thread ~100 cycles, so one thread could not keep up)
-            if (lane < 4) {
-                const CUtensorMap* m = lane == 0 ? &maps.hi : (lane == 1 ? &maps.lo : (lane == 2 ? &maps.hi64 : &maps.lo64));
+            if (lane < 2 * kNumMaps) {
+                const CUtensorMap* m = lane < kNumMaps ? &maps.hi[lane] : &maps.lo[lane - kNumMaps];
                 asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
             }
             int gs = 0, r = 0;
@@ -406,11 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
                 const uint8_t* wblocks =
                     p.wp + ((int64_t)t.e * (p.a_rows / kBM) + t.m0 / kBM) * nk * (int64_t)kWBlock;
-                const uint32_t tx_bytes = 2u * (uint32_t)(t.nbox * t.box) * 128u + (uint32_t)kWBlock;
-                // this CTA's boxes of a part: every C-th from box crank (all of them without a cluster)
-                const int nbox = (t.nbox - (int)crank + C - 1) / C;
-                const CUtensorMap* const mhi = t.stacked ? &maps.hi : &maps.hi64;
-                const CUtensorMap* const mlo = t.stacked ? &maps.lo : &maps.lo64;
+                const uint32_t tx_bytes = 2u * (uint32_t)t.lo_rows * 128u + (uint32_t)kWBlock;
+                const CUtensorMap* const mhi = &maps.hi[t.map];
+                const CUtensorMap* const mlo = &maps.lo[t.map];
                 for (int kt = 0; kt < nk; ++kt, ++gs) {
                     bool go = true;
                     if (lane == 0) {
@@ -422,16 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                         break;
                     }
                     const uint32_t slot = ring_s + (uint32_t)(r * sbytes);
-                    if (lane == 31)
+                    // lane 0 the weights, lanes 1 and 2 the hi and lo boxes; in a cluster, CTA 0 copies hi and CTA 1
+                    // lo for all (C = 2 or 4), the others only their weights
+                    if (lane == 0)
                         bulk_load(slot + (uint32_t)(2 * t.lo_rows * 128), wblocks + (int64_t)kt * kWBlock, kWBlock,
                                   &sfull[r]);
-                    for (int f = lane; f < 2 * nbox; f += 32) {  // box f: part f / nbox, box f % nbox of this CTA
-                        const int part = f >= nbox, i = part ? f - nbox : f;
-                        const int b0 = t.box * ((int)crank + C * i);
-                        const uint32_t dst = slot + (uint32_t)((part ? t.lo_rows + b0 : b0) * 128);
+                    const int part = lane - 1;
+                    if (part == 0 || part == 1) {
+                        const uint32_t dst = slot + (uint32_t)(part ? t.lo_rows * 128 : 0);
                         const CUtensorMap* map = part ? mlo : mhi;
-                        if (C > 1) tma_load_2d_mc(dst, map, kt * kBK, t.row0 + b0, &sfull[r], cmask);
-                        else tma_load_2d(dst, map, kt * kBK, t.row0 + b0, &sfull[r]);
+                        if (C == 1) tma_load_2d(dst, map, kt * kBK, t.row0, &sfull[r]);
+                        else if ((int)crank == part) tma_load_2d_mc(dst, map, kt * kBK, t.row0, &sfull[r], cmask);
                     }
                     if (++r == depth) {
                         r = 0;
@@ -728,15 +727,14 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     if (max_tiles <= 0) return cudaSuccess;
     GemmMaps maps;
     const uint16_t* lo = a.bop + a.b_rows * (int64_t)a.K;
-    if (!make_map(&maps.hi, a.bop, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
-                  kRowBox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&maps.lo, lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK, kRowBox,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&maps.hi64, a.bop, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
-                  kBigBox, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&maps.lo64, lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
-                  kBigBox, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+    for (int m = 0; m < kNumMaps; ++m) {
+        const uint32_t box = m < kNumMaps - 1 ? (uint32_t)(kRowBox * (m + 1)) : (uint32_t)kMaxBN;
+        if (!make_map(&maps.hi[m], a.bop, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
+                      box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&maps.lo[m], lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
+                      box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
     const int mt = a.a_rows / kBM;
     ExpertsGemmArgs args = a;
     // clusters share the row tiles through L2 once instead of once per weight slice; they pay off when tiles are
