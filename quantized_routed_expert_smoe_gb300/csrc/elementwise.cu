@@ -249,12 +249,13 @@ __global__ void __launch_bounds__(256) gather_q8_kernel(const uint4* __restrict_
                 if (g < groups) {
                     const __half2 d2 = __half2half2(__ushort_as_half(d[k]));
                     uint4 hi, lo;
+                    // streaming stores: the rows are read once, by the gate/up product
                     split_pairs(interleave_codes8(c[k].x, c[k].z), d2, hi, lo);
-                    o[2 * g] = hi;
-                    o[plane + 2 * g] = lo;
+                    __stcs(o + 2 * g, hi);
+                    __stcs(o + plane + 2 * g, lo);
                     split_pairs(interleave_codes8(c[k].y, c[k].w), d2, hi, lo);
-                    o[2 * g + 1] = hi;
-                    o[plane + 2 * g + 1] = lo;
+                    __stcs(o + 2 * g + 1, hi);
+                    __stcs(o + plane + 2 * g + 1, lo);
                 }
             }
         }
