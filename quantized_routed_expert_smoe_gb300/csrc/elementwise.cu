@@ -211,51 +211,54 @@ __global__ void __launch_bounds__(160) pack_q2_kernel(const uint8_t* __restrict_
 }
 
 // Routed rows of the q8 activations in operand form: out row r = codes row src[r] scaled by its scales and split
-// into the hi and lo planes, in operand order.  One warp per output row, its lanes striding over the row's groups of
-// 16 codes (16 bytes of codes and one scale in, 2 x 32 bytes out); an src entry outside [0, in_rows) gives zero rows.
-__global__ void __launch_bounds__(256) gather_q8_kernel(const uint4* __restrict__ codes,
+// into the hi and lo planes, in operand order.  One warp per output row.  Lane l makes the output words (8 fp16
+// each) l, l + 32, ... of both planes, so every store instruction writes 512 contiguous bytes: word w is half w % 2
+// of group w / 2, i.e. values 4h..4h+3 and 8+4h..8+4h+3 of the group (h = w % 2).  An src entry outside
+// [0, in_rows) gives zero rows.
+__global__ void __launch_bounds__(256) gather_q8_kernel(const uint32_t* __restrict__ codes,
                                                         const uint16_t* __restrict__ scales, int64_t in_rows,
                                                         int groups, const int32_t* __restrict__ src, int64_t n,
                                                         uint4* __restrict__ out) {
-    constexpr int kAhead = 8;  // groups a lane loads before it converts and stores them (cols up to 4096 in one pass)
+    constexpr int kAhead = 16;  // words a lane loads before it converts and stores them (cols up to 4096 a pass)
     const int lane = threadIdx.x & 31;
+    const int words = 2 * groups;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    const int64_t plane = n * groups * 2;  // uint4 words per plane
+    const int64_t plane = n * words;  // uint4 words per plane
     for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n; r += warps) {
         const int32_t t = __ldg(src + r);
-        uint4* o = out + r * groups * 2;
+        uint4* o = out + r * words;
         if (t < 0 || t >= in_rows) {
-            for (int g = lane; g < groups; g += 32)
-                o[2 * g] = o[2 * g + 1] = o[plane + 2 * g] = o[plane + 2 * g + 1] = make_uint4(0u, 0u, 0u, 0u);
+            for (int w = lane; w < words; w += 32) {
+                __stcs(o + w, make_uint4(0u, 0u, 0u, 0u));
+                __stcs(o + plane + w, make_uint4(0u, 0u, 0u, 0u));
+            }
             continue;
         }
-        const uint4* i = codes + (int64_t)t * groups;
+        const uint32_t* i = codes + (int64_t)t * groups * 4;  // 4 code words (16 codes) a group
         const uint16_t* sc = scales + (int64_t)t * (groups / 2);
-        for (int g0 = lane; g0 < groups; g0 += 32 * kAhead) {
+        for (int w0 = lane; w0 < words; w0 += 32 * kAhead) {
             // every load of this pass first (independent, in flight together), then the conversions and stores
-            uint4 c[kAhead];
+            uint32_t a[kAhead], b[kAhead];
             uint16_t d[kAhead];
 #pragma unroll
             for (int k = 0; k < kAhead; ++k) {
-                const int g = g0 + 32 * k;
-                if (g < groups) {
-                    c[k] = __ldg(i + g);  // values 0..3, 4..7, 8..11, 12..15 of the group
+                const int w = w0 + 32 * k;
+                if (w < words) {
+                    const int g = w >> 1, h = w & 1;
+                    a[k] = __ldg(i + 4 * g + h);      // values 4h .. 4h+3 of the group
+                    b[k] = __ldg(i + 4 * g + 2 + h);  // values 8+4h .. 8+4h+3
                     d[k] = __ldg(sc + g / 2);
                 }
             }
 #pragma unroll
             for (int k = 0; k < kAhead; ++k) {
-                const int g = g0 + 32 * k;
-                if (g < groups) {
-                    const __half2 d2 = __half2half2(__ushort_as_half(d[k]));
+                const int w = w0 + 32 * k;
+                if (w < words) {
                     uint4 hi, lo;
+                    split_pairs(interleave_codes8(a[k], b[k]), __half2half2(__ushort_as_half(d[k])), hi, lo);
                     // streaming stores: the rows are read once, by the gate/up product
-                    split_pairs(interleave_codes8(c[k].x, c[k].z), d2, hi, lo);
-                    __stcs(o + 2 * g, hi);
-                    __stcs(o + plane + 2 * g, lo);
-                    split_pairs(interleave_codes8(c[k].y, c[k].w), d2, hi, lo);
-                    __stcs(o + 2 * g + 1, hi);
-                    __stcs(o + plane + 2 * g + 1, lo);
+                    __stcs(o + w, hi);
+                    __stcs(o + plane + w, lo);
                 }
             }
         }
@@ -299,7 +302,7 @@ cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, 
 cudaError_t launch_gather_q8(const int8_t* codes, const uint16_t* scales, int64_t in_rows, int cols,
                              const int32_t* src, int64_t n, uint16_t* out, cudaStream_t s) {
     if (n == 0) return cudaSuccess;
-    gather_q8_kernel<<<grid_for(n * 32, 256), 256, 0, s>>>(reinterpret_cast<const uint4*>(codes), scales, in_rows,
+    gather_q8_kernel<<<grid_for(n * 32, 256), 256, 0, s>>>(reinterpret_cast<const uint32_t*>(codes), scales, in_rows,
                                                            cols / 16, src, n, reinterpret_cast<uint4*>(out));
     return cudaGetLastError();
 }
