@@ -40,15 +40,18 @@
 //                 operand form;
 //   warpgroup 4   converters: thread = weight row: decode its 64 weights of the slice into the slice's A buffer in
 //                 tensor memory.
-// Tensor memory (512 columns): 2 to 8 A buffers of 32 columns (more for small tiles, so that the converters run
-// further ahead), then 1 to 4 partial buffers of N columns rounded up to 32 (2N for a tile of at most 96 rows, which
-// stacks its hi and lo rows into one MMA; two buffers for gate/up, which promotes every slice; one suffices for
-// down).  A tile has at most 192 rows: a promoter thread then holds its 64 accumulators and two 32-column loads.
+// Tensor memory (512 columns): 4 A buffers of 32 columns, then 2 partial buffers of 192 columns (a tile's partial
+// takes N of them, or 2N for a tile of at most 96 rows, which stacks its hi and lo rows into one MMA; gate/up
+// promotes every slice's partial, down one partial per MMA thread at the item's end).  A tile has at most 192 rows:
+// a promoter thread then holds its 64 accumulators and two 32-column loads.
 //
-// Synchronisation: a satisfied mbarrier wait still costs a round trip of a few hundred cycles, so the MMA thread
-// waits once per slice, on "A of slice kt decoded": the converters arrive on it after they have seen the slice's
-// copies land (so it also orders the TMA-written B tiles before the MMAs) and, for a slice that starts a partial,
-// after one of them has seen the promoters free that partial's buffer.
+// Synchronisation: a satisfied mbarrier wait still costs a round trip of a few hundred cycles, so every role waits
+// as little as it can.  The MMA thread waits once per slice on "A of slice gs decoded" (the converters arrive after
+// they have seen the slice's copies land, so it also orders the TMA-written B tiles before the MMAs) and, for a slice
+// that starts a partial in a buffer used before, in the same round trip on "the promoters have taken that buffer's
+// previous partial".  The converters wait only on "slot full" -- the ring has as many slots as A buffers, so a full
+// slot also means that the MMAs of the slice that last used its A buffer have completed -- and test the next slot's
+// barrier while a slice's stores complete, so that a slice already landed costs them no wait.
 //
 // K order: within each group of 16 K values, operand position 2m holds value m and position 2m+1 value m+8
 // (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so the contraction is unchanged
@@ -80,11 +83,11 @@ constexpr int kSmemBytes = 232448;             // the per-CTA maximum (227 KB): 
 constexpr int kBarBytes = 512;
 constexpr int kScratchBytes = SMOE_TILE_ROWS * 4 * 4;  // SwiGLU epilogue: a warp's block amax per column [col][4]
 constexpr int kRingBytes = kSmemBytes - 1024 - kBarBytes - kScratchBytes;
-// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 40, the converters
-// to 56 and the promoters take 128: 128 x 40 + 384 x 128 + 128 x 56 = 61,440.  Per SM sub-partition (one warp of
-// each warpgroup): 32 x (40 + 3 x 128 + 56) = 15,360 <= 16,384.
-constexpr int kRegsWg0 = 40;
-constexpr int kRegsConv = 56;
+// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 32, the converters
+// to 64 and the promoters take 128: 128 x 32 + 384 x 128 + 128 x 64 = 61,440.  Per SM sub-partition (one warp of
+// each warpgroup): 32 x (32 + 3 x 128 + 64) = 15,360 <= 16,384.
+constexpr int kRegsWg0 = 32;
+constexpr int kRegsConv = 64;
 constexpr int kRegsProm = 128;
 static_assert(128 * kRegsWg0 + kConverters * kRegsConv + kPromoters * kRegsProm <= kThreads * 96,
               "register split exceeds the launch");
@@ -282,12 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
 
     // fixed geometry for every item (tiles of up to kMaxBN rows): a ring of `depth` slots, na A buffers and nbuf
     // partial buffers of kMaxBN columns in tensor memory
-    const int sbytes = slot_bytes(kMaxBN);
-    const int depth = min(kMaxRing, kRingBytes / sbytes);
+    constexpr int sbytes = slot_bytes(kMaxBN);
+    constexpr int depth = kRingBytes / sbytes < kMaxRing ? kRingBytes / sbytes : kMaxRing;
     constexpr int na = ((int)kTmemCols - 2 * kMaxBN) / (int)kACols;
     constexpr uint32_t part_base = (uint32_t)na * kACols;
     constexpr int nbuf = ((int)kTmemCols - (int)part_base) / kMaxBN;
     static_assert(na >= 2 && na <= kMaxA && nbuf >= 2 && nbuf <= kMaxBufs, "tensor-memory split");
+    // slice gs uses ring slot and A buffer gs mod depth.  Its copies can land only after the producer has seen the
+    // slot's previous slice (gs - depth) released by this CTA's MMA commit, which follows that slice's MMAs, the last
+    // readers of the A buffer: "slot full" also means "A buffer free", so the converters wait for nothing else
+    static_assert(depth == na, "ring slots and A buffers advance together");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -295,8 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     uint64_t* sfull = reinterpret_cast<uint64_t*>(smem_raw + kSmemBytes - kBarBytes);  // slot r holds slice [kMaxRing]
     uint64_t* sempty = sfull + kMaxRing;    // the MMAs and the converters are done with slot r [kMaxRing]
     uint64_t* afull = sempty + kMaxRing;    // A buffer a decoded (and its slot's copies landed) [kMaxA]
-    uint64_t* aempty = afull + kMaxA;       // the MMAs are done with A buffer a [kMaxA]
-    uint64_t* pfull = aempty + kMaxA;       // partial in tensor-memory buffer b is complete [kMaxBufs]
+    uint64_t* pfull = afull + kMaxA;        // partial in tensor-memory buffer b is complete [kMaxBufs]
     uint64_t* pempty = pfull + kMaxBufs;    // the promoters have added buffer b into their registers [kMaxBufs]
     uint64_t* accf = pempty + kMaxBufs;     // every MMA has completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
@@ -309,10 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             mbar_init(&sfull[r], 1);                 // the arrival that posts the slice's byte count
             mbar_init(&sempty[r], C + kConverters);  // the MMAs' commit of every CTA of the cluster, own converters
         }
-        for (int a = 0; a < kMaxA; ++a) {
-            mbar_init(&afull[a], kConverters);
-            mbar_init(&aempty[a], 1);
-        }
+        for (int a = 0; a < kMaxA; ++a) mbar_init(&afull[a], kConverters);
         for (int b = 0; b < kMaxBufs; ++b) {
             mbar_init(&pfull[b], 1);
             mbar_init(&pempty[b], kPromoters);
@@ -355,7 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     const int gp = seq * pitem + (p.two_level ? kt : (pitem == 2 ? (kt & 1) : 0));
                     const int b = gp % nbuf;
                     const bool first = p.two_level || kt < 2, last = p.two_level || kt + 2 >= nk;
-                    if (!mbar_wait(&afull[ab], aph, abort_flag)) {  // implies the partial buffer is free
+                    // A decoded (which implies the slot's copies landed); a slice that starts a partial in a buffer
+                    // used before also needs the promoters to have taken the previous partial there (partial
+                    // gp - nbuf: phase gp / nbuf - 1 of its pempty).  Both waits overlap.
+                    const bool reuse = first && gp >= nbuf;
+                    if (!(reuse ? mbar_wait2(&afull[ab], aph, &pempty[b], (uint32_t)(gp / nbuf - 1) & 1u, abort_flag)
+                                : mbar_wait(&afull[ab], aph, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -378,7 +386,6 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     }
                     if (C > 1) mma_commit_mc(&sempty[r], cmask);
                     else mma_commit(&sempty[r]);
-                    mma_commit(&aempty[ab]);
                     if (last) mma_commit(&pfull[b]);
                     if ((r += 2) >= depth) r -= depth;
                     if ((ab += 2) >= na) {
@@ -612,48 +619,40 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         // thread = weight row ct = TMEM lane of its warp: 64 weights a slice into the 32 columns of A buffer ab
         const int ct = threadIdx.x - 512;
         const uint32_t lane_base = (uint32_t)(ct & ~31) << 16;
-        int gs = 0, r = 0, ab = 0, pc = 0, pb = 0;  // global slice; ring slot; A buffer; partials started, buffer
-        uint32_t rph = 0, aph = 0, pph = 0;  // sfull parity; aempty parity of the previous use of ab; pempty parity
+        int r = 0;           // the slice's ring slot = its A buffer
+        uint32_t rph = 0;    // that slot's sfull parity
+        bool ready = false;  // its copies are known to have landed (tested while the previous slice was stored)
         Item t;
         for (int item = cid; item < n_items && ok; item += NC) {
             if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
-            for (int kt = 0; kt < nk && ok; ++kt, ++gs) {
-                if (!mbar_wait(&sfull[r], rph, abort_flag) || (gs >= na && !mbar_wait(&aempty[ab], aph, abort_flag))) {
+            const int wofs = 2 * t.lo_rows * 128;  // the packed weight block within a slot
+            for (int kt = 0; kt < nk && ok; ++kt) {
+                if (!ready && !mbar_wait(&sfull[r], rph, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint8_t* wb = ring + r * sbytes + 2 * t.lo_rows * 128;
+                tc_fence_after();
+                const uint8_t* wb = ring + r * sbytes + wofs;
                 const uint4 codes = *reinterpret_cast<const uint4*>(wb + ct * 16);
                 const __half2 sc = *reinterpret_cast<const __half2*>(wb + 2048 + ct * 4);
                 uint32_t col[16];  // one 32-value block at a time
                 decode_weights16(codes.x, __low2half2(sc), col);
                 decode_weights16(codes.y, __low2half2(sc), col + 8);
-                tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols, col);
+                tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)r * kACols, col);
                 decode_weights16(codes.z, __high2half2(sc), col);
                 decode_weights16(codes.w, __high2half2(sc), col + 8);
-                tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols + 16u, col);
+                tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)r * kACols + 16u, col);
+                const int rn = r + 1 == depth ? 0 : r + 1;
+                const uint32_t rphn = r + 1 == depth ? rph ^ 1u : rph;
+                // the next global slice (of this item or the next) uses slot rn: test its barrier while the stores
+                // complete, so that a slice whose copies have landed costs no wait round trip
+                ready = mbar_test(smem_u32(&sfull[rn]), rphn);
                 tmem_st_wait();
                 tc_fence_before();
-                // a slice that starts a partial may be multiplied only once the promoters have freed the partial's
-                // buffer (partials start at every slice when two-level, else at the item's first pitem slices)
-                if (p.two_level || kt < pitem) {
-                    if (ct == 0 && pc >= nbuf && !mbar_wait(&pempty[pb], pph, abort_flag)) ok = false;
-                    ++pc;
-                    if (++pb == nbuf) {
-                        pb = 0;
-                        if (pc > nbuf) pph ^= 1u;
-                    }
-                }
-                mbar_arrive(&afull[ab]);
+                mbar_arrive(&afull[r]);
                 mbar_arrive(&sempty[r]);
-                if (++r == depth) {
-                    r = 0;
-                    rph ^= 1u;
-                }
-                if (++ab == na) {
-                    ab = 0;
-                    if (gs >= na) aph ^= 1u;
-                }
+                r = rn;
+                rph = rphn;
             }
         }
     }

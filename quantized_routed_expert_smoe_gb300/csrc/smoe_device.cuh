@@ -38,6 +38,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Has the phase of `parity` completed?  One non-blocking test (acquire on success).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Both phases complete?  One non-blocking test of each barrier, issued back to back (their round trips overlap).
+__device__ __forceinline__ bool mbar_test2(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+        "and.pred p, p, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(b0), "r"(p0), "r"(b1), "r"(p1)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase of `parity` to complete.  Returns false when *abort is set by another role of the CTA or when
 // kWaitLimitNs have passed; never spins forever.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -46,6 +69,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     const uint64_t t0 = global_ns();
     for (;;) {
         if (mbar_try_wait(a, parity)) return true;
+        if (abort != nullptr && *abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Wait for the phases of two barriers (`parity0` of bar0, `parity1` of bar1), with mbar_wait's limits.  When both
+// have completed already this costs one round trip instead of two.
+__device__ __forceinline__ bool mbar_wait2(uint64_t* bar0, uint32_t parity0, uint64_t* bar1, uint32_t parity1,
+                                           volatile int* abort) {
+    const uint32_t a0 = smem_u32(bar0), a1 = smem_u32(bar1);
+    if (mbar_test2(a0, parity0, a1, parity1)) return true;
+    bool d0 = false, d1 = false;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (!d0) d0 = mbar_try_wait(a0, parity0);
+        if (!d1) d1 = mbar_try_wait(a1, parity1);
+        if (d0 && d1) return true;
         if (abort != nullptr && *abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) return false;
     }
