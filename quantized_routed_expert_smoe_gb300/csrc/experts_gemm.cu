@@ -45,13 +45,14 @@
 // promotes every slice's partial, down one partial per MMA thread at the item's end).  A tile has at most 192 rows:
 // a promoter thread then holds its 64 accumulators and two 32-column loads.
 //
-// Synchronisation: a satisfied mbarrier wait still costs a round trip of a few hundred cycles, so every role waits
-// as little as it can.  The MMA thread waits once per slice on "A of slice gs decoded" (the converters arrive after
-// they have seen the slice's copies land, so it also orders the TMA-written B tiles before the MMAs) and, for a slice
-// that starts a partial in a buffer used before, in the same round trip on "the promoters have taken that buffer's
-// previous partial".  The converters wait only on "slot full" -- the ring has as many slots as A buffers, so a full
-// slot also means that the MMAs of the slice that last used its A buffer have completed -- and test the next slot's
-// barrier while a slice's stores complete, so that a slice already landed costs them no wait.
+// Synchronisation: a satisfied mbarrier wait still costs a round trip of a few hundred cycles, and the ring's slots
+// circulate through a chain of latencies (slot released -> copies issued -> landed -> A decoded -> MMAs -> released),
+// so each role waits as little as it can and nothing waits on what it does not need.  A slot's packed weights land
+// on their own barrier, so the converters decode while the B tiles are still in flight; they wait on nothing else
+// -- the ring has as many slots as A buffers, so a slot's new contents also mean that the MMAs of the slice that
+// last used its A buffer have completed -- and test the next slot's barrier while a slice's stores complete.  The
+// MMA thread waits once per slice, in one round trip, on "A decoded", "B tiles landed" and, for a slice that starts
+// a partial in a buffer used before, "the promoters have taken that buffer's previous partial".
 //
 // K order: within each group of 16 K values, operand position 2m holds value m and position 2m+1 value m+8
 // (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so the contraction is unchanged
@@ -72,7 +73,7 @@ constexpr int kMaxBN = SMOE_TILE_ROWS;         // routed rows per tile (MMA N <=
 constexpr int kThreads = 640;                  // five warpgroups
 constexpr int kPromoters = 384;                // warpgroups 1-3
 constexpr int kConverters = 128;               // warpgroup 4
-constexpr int kMaxRing = 16;                   // slices in flight at most
+constexpr int kMaxRing = 8;                    // slices in flight at most
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACols = 32;                // one slice of A: 128 lanes x 64 fp16
 constexpr int kMaxA = 8;                       // A buffers at most
@@ -83,11 +84,11 @@ constexpr int kSmemBytes = 232448;             // the per-CTA maximum (227 KB): 
 constexpr int kBarBytes = 512;
 constexpr int kScratchBytes = SMOE_TILE_ROWS * 4 * 4;  // SwiGLU epilogue: a warp's block amax per column [col][4]
 constexpr int kRingBytes = kSmemBytes - 1024 - kBarBytes - kScratchBytes;
-// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 32, the converters
-// to 64 and the promoters take 128: 128 x 32 + 384 x 128 + 128 x 64 = 61,440.  Per SM sub-partition (one warp of
-// each warpgroup): 32 x (32 + 3 x 128 + 64) = 15,360 <= 16,384.
-constexpr int kRegsWg0 = 32;
-constexpr int kRegsConv = 64;
+// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 40, the converters
+// to 56 and the promoters take 128: 128 x 40 + 384 x 128 + 128 x 56 = 61,440.  Per SM sub-partition (one warp of
+// each warpgroup): 32 x (40 + 3 x 128 + 56) = 15,360 <= 16,384.
+constexpr int kRegsWg0 = 40;
+constexpr int kRegsConv = 56;
 constexpr int kRegsProm = 128;
 static_assert(128 * kRegsWg0 + kConverters * kRegsConv + kPromoters * kRegsProm <= kThreads * 96,
               "register split exceeds the launch");
@@ -293,15 +294,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     static_assert(na >= 2 && na <= kMaxA && nbuf >= 2 && nbuf <= kMaxBufs, "tensor-memory split");
     // slice gs uses ring slot and A buffer gs mod depth.  Its copies can land only after the producer has seen the
     // slot's previous slice (gs - depth) released by this CTA's MMA commit, which follows that slice's MMAs, the last
-    // readers of the A buffer: "slot full" also means "A buffer free", so the converters wait for nothing else
+    // readers of the A buffer: "weights landed" also means "A buffer free", so the converters wait for nothing else
     static_assert(depth == na, "ring slots and A buffers advance together");
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t* ring = smem_raw + pad;
-    uint64_t* sfull = reinterpret_cast<uint64_t*>(smem_raw + kSmemBytes - kBarBytes);  // slot r holds slice [kMaxRing]
-    uint64_t* sempty = sfull + kMaxRing;    // the MMAs and the converters are done with slot r [kMaxRing]
-    uint64_t* afull = sempty + kMaxRing;    // A buffer a decoded (and its slot's copies landed) [kMaxA]
+    uint64_t* sfull = reinterpret_cast<uint64_t*>(smem_raw + kSmemBytes - kBarBytes);  // slot r's B tiles [kMaxRing]
+    uint64_t* wfull = sfull + kMaxRing;     // slot r's packed weight block landed [kMaxRing]
+    uint64_t* sempty = wfull + kMaxRing;    // the MMAs and the converters are done with slot r [kMaxRing]
+    uint64_t* afull = sempty + kMaxRing;    // A buffer a decoded [kMaxA]
     uint64_t* pfull = afull + kMaxA;        // partial in tensor-memory buffer b is complete [kMaxBufs]
     uint64_t* pempty = pfull + kMaxBufs;    // the promoters have added buffer b into their registers [kMaxBufs]
     uint64_t* accf = pempty + kMaxBufs;     // every MMA has completed
@@ -312,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int r = 0; r < kMaxRing; ++r) {
-            mbar_init(&sfull[r], 1);                 // the arrival that posts the slice's byte count
+            mbar_init(&sfull[r], 1);                 // the arrival that posts the B tiles' byte count
+            mbar_init(&wfull[r], 1);                 // the arrival that posts the weight block's
             mbar_init(&sempty[r], C + kConverters);  // the MMAs' commit of every CTA of the cluster, own converters
         }
         for (int a = 0; a < kMaxA; ++a) mbar_init(&afull[a], kConverters);
@@ -358,12 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     const int gp = seq * pitem + (p.two_level ? kt : (pitem == 2 ? (kt & 1) : 0));
                     const int b = gp % nbuf;
                     const bool first = p.two_level || kt < 2, last = p.two_level || kt + 2 >= nk;
-                    // A decoded (which implies the slot's copies landed); a slice that starts a partial in a buffer
-                    // used before also needs the promoters to have taken the previous partial there (partial
-                    // gp - nbuf: phase gp / nbuf - 1 of its pempty).  Both waits overlap.
+                    // A decoded and the slot's B tiles landed (slot r = A buffer ab: the same phase); a slice that
+                    // starts a partial in a buffer used before also needs the promoters to have taken the previous
+                    // partial there (partial gp - nbuf: phase gp / nbuf - 1 of its pempty).  The waits overlap.
                     const bool reuse = first && gp >= nbuf;
-                    if (!(reuse ? mbar_wait2(&afull[ab], aph, &pempty[b], (uint32_t)(gp / nbuf - 1) & 1u, abort_flag)
-                                : mbar_wait(&afull[ab], aph, abort_flag))) {
+                    if (!mbar_wait3(&afull[ab], aph, &sfull[r], aph, reuse ? &pempty[b] : &afull[ab],
+                                    reuse ? (uint32_t)(gp / nbuf - 1) & 1u : aph, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -413,25 +416,29 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
                 const uint8_t* wblocks =
                     p.wp + ((int64_t)t.e * (p.a_rows / kBM) + t.m0 / kBM) * nk * (int64_t)kWBlock;
-                const uint32_t tx_bytes = 2u * (uint32_t)t.lo_rows * 128u + (uint32_t)kWBlock;
+                const uint32_t b_bytes = 2u * (uint32_t)t.lo_rows * 128u;
                 const CUtensorMap* const mhi = &maps.hi[t.map];
                 const CUtensorMap* const mlo = &maps.lo[t.map];
                 for (int kt = 0; kt < nk; ++kt, ++gs) {
                     bool go = true;
                     if (lane == 0) {
                         if (gs >= depth && !mbar_wait(&sempty[r], eph, abort_flag)) go = false;
-                        else mbar_arrive_expect_tx(&sfull[r], tx_bytes);
+                        else {
+                            mbar_arrive_expect_tx(&wfull[r], (uint32_t)kWBlock);
+                            mbar_arrive_expect_tx(&sfull[r], b_bytes);
+                        }
                     }
                     if (!__shfl_sync(0xffffffffu, go, 0)) {
                         ok = false;
                         break;
                     }
                     const uint32_t slot = ring_s + (uint32_t)(r * sbytes);
-                    // lane 0 the weights, lanes 1 and 2 the hi and lo boxes; in a cluster, CTA 0 copies hi and CTA 1
-                    // lo for all (C = 2 or 4), the others only their weights
+                    // lane 0 the weights (on their own barrier: the converters need nothing else), lanes 1 and 2 the
+                    // hi and lo boxes; in a cluster, CTA 0 copies hi and CTA 1 lo for all (C = 2 or 4), the others only
+                    // their weights
                     if (lane == 0)
                         bulk_load(slot + (uint32_t)(2 * t.lo_rows * 128), wblocks + (int64_t)kt * kWBlock, kWBlock,
-                                  &sfull[r]);
+                                  &wfull[r]);
                     const int part = lane - 1;
                     if (part == 0 || part == 1) {
                         const uint32_t dst = slot + (uint32_t)(part ? t.lo_rows * 128 : 0);
@@ -448,8 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             // no copy may still be writing shared memory when the CTA exits (on the abort path nobody has waited
             // for the last slices): wait, bounded, for the last `depth` slices issued
             if (lane == 0)
-                for (int k = max(0, gs - depth); k < gs; ++k)
+                for (int k = max(0, gs - depth); k < gs; ++k) {
+                    mbar_wait(&wfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
                     mbar_wait(&sfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
+                }
         }
         __syncwarp();
     } else if (warp < 16) {
@@ -620,14 +629,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         const int ct = threadIdx.x - 512;
         const uint32_t lane_base = (uint32_t)(ct & ~31) << 16;
         int r = 0;           // the slice's ring slot = its A buffer
-        uint32_t rph = 0;    // that slot's sfull parity
+        uint32_t rph = 0;    // that slot's wfull parity
         bool ready = false;  // its copies are known to have landed (tested while the previous slice was stored)
         Item t;
         for (int item = cid; item < n_items && ok; item += NC) {
             if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
             const int wofs = 2 * t.lo_rows * 128;  // the packed weight block within a slot
             for (int kt = 0; kt < nk && ok; ++kt) {
-                if (!ready && !mbar_wait(&sfull[r], rph, abort_flag)) {
+                if (!ready && !mbar_wait(&wfull[r], rph, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -645,8 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 const int rn = r + 1 == depth ? 0 : r + 1;
                 const uint32_t rphn = r + 1 == depth ? rph ^ 1u : rph;
                 // the next global slice (of this item or the next) uses slot rn: test its barrier while the stores
-                // complete, so that a slice whose copies have landed costs no wait round trip
-                ready = mbar_test(smem_u32(&sfull[rn]), rphn);
+                // complete, so that a slice whose weights have landed costs no wait round trip
+                ready = mbar_test(smem_u32(&wfull[rn]), rphn);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(&afull[r]);

@@ -61,6 +61,21 @@ __device__ __forceinline__ bool mbar_test2(uint32_t b0, uint32_t p0, uint32_t b1
         : "memory");
     return ok != 0;
 }
+// All three phases complete?  (A barrier may be passed twice.)
+__device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2,
+                                           uint32_t p2) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p, q, r;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 r, [%5], %6;\n\t"
+        "and.pred p, p, q;\n\tand.pred p, p, r;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+        : "memory");
+    return ok != 0;
+}
 // Wait for the phase of `parity` to complete.  Returns false when *abort is set by another role of the CTA or when
 // kWaitLimitNs have passed; never spins forever.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -86,6 +101,23 @@ __device__ __forceinline__ bool mbar_wait2(uint64_t* bar0, uint32_t parity0, uin
         if (!d0) d0 = mbar_try_wait(a0, parity0);
         if (!d1) d1 = mbar_try_wait(a1, parity1);
         if (d0 && d1) return true;
+        if (abort != nullptr && *abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Wait for the phases of three barriers, with mbar_wait's limits (one round trip when all have completed already).
+__device__ __forceinline__ bool mbar_wait3(uint64_t* bar0, uint32_t parity0, uint64_t* bar1, uint32_t parity1,
+                                           uint64_t* bar2, uint32_t parity2, volatile int* abort) {
+    const uint32_t a0 = smem_u32(bar0), a1 = smem_u32(bar1), a2 = smem_u32(bar2);
+    if (mbar_test3(a0, parity0, a1, parity1, a2, parity2)) return true;
+    bool d0 = false, d1 = false, d2 = false;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (!d0) d0 = mbar_try_wait(a0, parity0);
+        if (!d1) d1 = mbar_try_wait(a1, parity1);
+        if (!d2) d2 = mbar_try_wait(a2, parity2);
+        if (d0 && d1 && d2) return true;
         if (abort != nullptr && *abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) return false;
     }
