@@ -98,15 +98,16 @@ static_assert(kMaxBN % 96 == 0, "the promoter warpgroups take whole 32-column ch
 // Ring slot (one 64-wide K slice of the tile): the rows of the hi part, then of the lo part (128 bytes a row,
 // 128-byte swizzle, 1024-aligned), then the packed weight block (codes [128][16 B], scales [128][4 B]); slots are
 // 1024-byte multiples.  A stacked tile's lo rows follow its N hi rows (one MMA reads both); a larger tile's parts
-// take fixed regions of kMaxBN rows each (rows past N are loaded and never read).
+// take fixed regions of kMaxBN rows each.
 constexpr int kWBlock = 2560;
-// One TMA copy per part and slice (the TMA unit takes a copy per ~100 cycles whatever its size): a stacked tile of
-// N = 16 m rows uses the map whose box is N rows; a larger tile a box of kMaxBN rows into its part's fixed region.
-constexpr int kRowBox = 16;                    // box-height step of the stacked maps
-constexpr int kNumMaps = kMaxStackN / kRowBox + 1;
+// One TMA copy per part and slice, of exactly the tile's N rows: the map whose box is N = 16 (m + 1) rows (the
+// SM's TMA unit, which every copy of the CTA shares, is on the ring's critical path; rows that are never read are
+// not loaded).
+constexpr int kRowBox = 16;                    // box-height step of the maps
+constexpr int kNumMaps = kMaxBN / kRowBox;
 __host__ __device__ constexpr int slot_bytes(int N) { return (2 * N * 128 + kWBlock + 1023) & ~1023; }
 static_assert(kRingBytes / slot_bytes(kMaxBN) >= 3, "the ring must hold three slices of a full tile");
-static_assert(kMaxStackN % kRowBox == 0 && kMaxBN <= 256, "box heights");
+static_assert(kMaxStackN % kRowBox == 0 && kMaxBN % kRowBox == 0 && kMaxBN <= 256, "box heights");
 
 // bulk copy (no tensor map) of `bytes` (a multiple of 16) into shared memory, completing on `bar`
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -233,7 +234,6 @@ __device__ __forceinline__ void decode_weights16(uint32_t codes, __half2 d2, uin
 
 struct GemmMaps {
     // the two parts of the B rows: fp16 [b_rows][K] each, 128-byte swizzle, boxes of 64 values x 16 (m + 1) rows
-    // (m < kNumMaps - 1) or x kMaxBN rows (m = kNumMaps - 1)
     CUtensorMap hi[kNumMaps], lo[kNumMaps];
 };
 
@@ -262,7 +262,7 @@ __device__ __forceinline__ bool load_item(const int32_t* tiles, int item, int mg
     t.stacked = t.N <= kMaxStackN;
     t.ncols = t.stacked ? 2 * t.N : t.N;
     t.lo_rows = t.stacked ? t.N : kMaxBN;
-    t.map = t.stacked ? t.N / kRowBox - 1 : kNumMaps - 1;
+    t.map = t.N / kRowBox - 1;
     return true;
 }
 
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
                 const uint8_t* wblocks =
                     p.wp + ((int64_t)t.e * (p.a_rows / kBM) + t.m0 / kBM) * nk * (int64_t)kWBlock;
-                const uint32_t b_bytes = 2u * (uint32_t)t.lo_rows * 128u;
+                const uint32_t b_bytes = 2u * (uint32_t)t.N * 128u;
                 const CUtensorMap* const mhi = &maps.hi[t.map];
                 const CUtensorMap* const mlo = &maps.lo[t.map];
                 for (int kt = 0; kt < nk; ++kt, ++gs) {
@@ -736,7 +736,7 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     GemmMaps maps;
     const uint16_t* lo = a.bop + a.b_rows * (int64_t)a.K;
     for (int m = 0; m < kNumMaps; ++m) {
-        const uint32_t box = m < kNumMaps - 1 ? (uint32_t)(kRowBox * (m + 1)) : (uint32_t)kMaxBN;
+        const uint32_t box = (uint32_t)(kRowBox * (m + 1));
         if (!make_map(&maps.hi[m], a.bop, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
                       box, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_map(&maps.lo[m], lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
