@@ -16,6 +16,11 @@
  *   smoe_experts_down    grouped down product into one fp32 row per routed pair
  *   smoe_combine         Y[t] = sum_k w[t][k] * Dm[slot[t*K+k]] (gather form, no atomics)
  *
+ * With the shared expert (the same page's "shared expert and its scalar gate"): one more expert in the routed
+ * experts' form that every token takes -- grouped by smoe_group with E = 1, K = 1 and all ids 0, gathered by
+ * smoe_gather_q8, multiplied by smoe_experts_gateup / smoe_swiglu_requant / smoe_experts_down with E = 1 --, its
+ * scalar gate from smoe_shared_gate, and smoe_combine_shared in place of smoe_combine.
+ *
  * FORMATS (all row-major, little-endian):
  *   q8 activations   codes int8 [rows][cols] and scales fp16 (as uint16 bits) [rows][cols/32].  A block of 32 values
  *                    x has amax = max|x|, d = fp16_rne(amax / 127.0f) (IEEE fp32 division) and codes
@@ -197,6 +202,19 @@ smoe_status smoe_experts_down(const uint16_t* hop, int32_t* tiles, int64_t n, in
  *   dm fp32 [n][H], slot int32 [T*K], w fp32 [T][K] -> y fp32 [T][H].   H % 4 == 0. */
 smoe_status smoe_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
                          void* stream);
+
+/* Shared expert, scalar gate.  Page "src/prefill/prefill.cpp", Prefill::run, MoE half ("the shared expert and its
+ * scalar gate": a projection of each token onto one row); the gate's nonlinearity is not given there and is read as
+ * the logistic sigmoid:  sg[t] = 1 / (1 + exp(-(x[t] . w_sg))), the dot product in fp32.
+ *   x fp32 [T][H], w_sg fp32 [H] -> sg fp32 [T].   H % 4 == 0; x, w_sg, sg 16-byte aligned. */
+smoe_status smoe_shared_gate(const float* x, const float* wsg, int64_t T, int H, float* sg, void* stream);
+
+/* Step 7 with the shared expert: smoe_combine's sum, then + sg[t] * ds[t][o] (fp32):
+ *   Y[t][o] = sum_{k=0}^{K-1} w[t][k] * dm[slot[t*K+k]][o]  +  sg[t] * ds[t][o].
+ *   ds fp32 [T][H] (the shared expert's down rows, row t = token t), sg fp32 [T] (smoe_shared_gate); the other
+ *   arguments and rules as smoe_combine. */
+smoe_status smoe_combine_shared(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,
+                                const float* ds, const float* sg, float* y, void* stream);
 
 #ifdef __cplusplus
 }

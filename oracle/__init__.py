@@ -67,6 +67,12 @@ def lib():
             L.oracle_layer_tokens.argtypes = [vp, vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp,
                                               vp, c_int]
             L.oracle_layer_bruteforce.argtypes = [vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, c_int]
+            L.oracle_shared_gate.argtypes = [vp, vp, i64, c_int, vp, c_int]
+            L.oracle_shared_expert.argtypes = [vp, i64, c_int, c_int, vp, vp, vp, vp, vp, c_int]
+            L.oracle_combine_shared.argtypes = [vp, vp, vp, vp, vp, i64, c_int, c_int, vp, c_int]
+            L.oracle_layer_shared.argtypes = [vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              vp, vp, c_int]
+            L.oracle_layer_shared.restype = c_int
             assert L.oracle_tile_rows() == TILE_ROWS
             _lib = L
     return _lib
@@ -216,3 +222,61 @@ def layer_bruteforce(inp: dict, nthreads: int = 0) -> np.ndarray:
     lib().oracle_layer_bruteforce(_ptr(logits), _ptr(x), T, H, E, K, F, _ptr(a), _ptr(b), _ptr(c), _ptr(d), _ptr(y),
                                   nthreads)
     return y
+
+
+# ----------------------------------------------------------------------------------------------- shared expert
+def _shared_weights(inp):
+    return (_c(inp["sgu_c"], np.uint8), _c(inp["sgu_s"], np.uint16), _c(inp["sd_c"], np.uint8),
+            _c(inp["sd_s"], np.uint16))
+
+
+def shared_gate(x: np.ndarray, wsg: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    """sg [T] = sigmoid(x . w_sg) per token, in double."""
+    x, wsg = _c(x, np.float32), _c(wsg, np.float32)
+    T, H = x.shape
+    sg = np.empty(T, np.float64)
+    lib().oracle_shared_gate(_ptr(x), _ptr(wsg), T, H, _ptr(sg), nthreads)
+    return sg
+
+
+def shared_expert(x: np.ndarray, sgu_c, sgu_s, sd_c, sd_s, F: int, nthreads: int = 0) -> np.ndarray:
+    """The shared expert's rows S [T][H] (every token through the one shared expert)."""
+    x = _c(x, np.float32)
+    T, H = x.shape
+    a, b, c, d = _c(sgu_c, np.uint8), _c(sgu_s, np.uint16), _c(sd_c, np.uint8), _c(sd_s, np.uint16)
+    out = np.empty((T, H), np.float64)
+    lib().oracle_shared_expert(_ptr(x), T, H, F, _ptr(a), _ptr(b), _ptr(c), _ptr(d), _ptr(out), nthreads)
+    return out
+
+
+def combine_shared(dm, slot, w, shared, sg, T: int, K: int, H: int, nthreads: int = 0) -> np.ndarray:
+    dm, slot, w = _c(dm, np.float64), _c(slot, np.int32), _c(w, np.float64)
+    shared, sg = _c(shared, np.float64), _c(sg, np.float64)
+    y = np.empty((T, H), np.float64)
+    lib().oracle_combine_shared(_ptr(dm), _ptr(slot), _ptr(w), _ptr(shared), _ptr(sg), T, K, H, _ptr(y), nthreads)
+    return y
+
+
+def layer_shared(inp: dict, nthreads: int = 0) -> np.ndarray:
+    """The whole block with the shared expert; `inp` also holds the shared weights and the gate row."""
+    logits, x = _c(inp["logits"], np.float32), _c(inp["x"], np.float32)
+    T, H = x.shape
+    E, K, F = inp["E"], inp["K"], inp["F"]
+    a, b, c, d = _weights(inp)
+    sa, sb, sc, sd = _shared_weights(inp)
+    wsg = _c(inp["wsg"], np.float32)
+    y = np.empty((T, H), np.float64)
+    rc = lib().oracle_layer_shared(_ptr(logits), _ptr(x), T, H, E, K, F, _ptr(a), _ptr(b), _ptr(c), _ptr(d), _ptr(sa),
+                                   _ptr(sb), _ptr(sc), _ptr(sd), _ptr(wsg), _ptr(y), nthreads)
+    if rc != 0:
+        raise ValueError("routed id out of range")
+    return y
+
+
+def layer_tokens_shared(inp: dict, tokens, nthreads: int = 0):
+    """The block with the shared expert for the listed tokens only; returns (y [ntok][H], ids, w)."""
+    y, ids, w = layer_tokens(inp, tokens, nthreads)
+    xs = _c(np.asarray(inp["x"], np.float32)[np.asarray(tokens, np.int64)], np.float32)
+    sa, sb, sc, sd = _shared_weights(inp)
+    y = y + shared_gate(xs, inp["wsg"], nthreads)[:, None] * shared_expert(xs, sa, sb, sc, sd, inp["F"], nthreads)
+    return y, ids, w

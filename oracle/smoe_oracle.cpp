@@ -31,7 +31,11 @@
 //      most 192 rows, each expert's c rows split into ceil(c/192) parts [floor(i*c/nt), floor((i+1)*c/nt)).
 //   R7 SwiGLU: h_j = silu(g_j) * u_j, silu(g) = g / (1 + exp(-g)), gate = rows [0, F), up = rows [F, 2F); h is
 //      rounded to fp32 before the q8 rule of R3 (the rule is defined on fp32 input).
-//   R8 combine: Y[t] = sum over k (in k order) of w[t][k] * Dm[slot[t*K+k]]; no shared expert.
+//   R8 combine: Y[t] = sum over k (in k order) of w[t][k] * Dm[slot[t*K+k]].
+//   R9 shared expert (the "shared expert and its scalar gate" of [P1]; its weight format, width and the gate's
+//      nonlinearity are not given): one more expert of the routed experts' form (2-bit weights, gate/up [2F][H],
+//      down [H][F]) that every token takes, on the same int8 activations; its scalar gate is
+//      sg[t] = sigmoid(x[t] . w_sg) with w_sg fp32 [H]; the combine adds sg[t] * S[t] after the routed sum.
 //
 // Arithmetic: double everywhere except the q8 rule (R3), which is defined in fp32 and emulated here in `float`.
 // Build with -ffp-contract=off so that no fused multiply-add changes a fp32 step.
@@ -320,6 +324,48 @@ void oracle_combine(const double* dm, const int32_t* slot, const double* w, int6
     });
 }
 
+// ------------------------------------------------------------------------------------------------ shared expert
+/// [P1] Prefill::run, MoE half, "the shared expert and its scalar gate": the gate is a projection of the token onto
+/// one row, read as sg[t] = sigmoid(sum_h x[t][h] * w_sg[h]) in double (R9).  x fp32 [T][H], wsg fp32 [H].
+void oracle_shared_gate(const float* x, const float* wsg, int64_t T, int H, double* sg, int nthreads) {
+    parallel_for(T, nthreads, [&](int64_t t0, int64_t t1) {
+        for (int64_t t = t0; t < t1; ++t) {
+            double z = 0.0;
+            for (int64_t h = 0; h < H; ++h) z += (double)x[t * H + h] * (double)wsg[h];
+            sg[t] = 1.0 / (1.0 + std::exp(-z));
+        }
+    });
+}
+
+/// [P1] the shared expert's gate and up projections, SwiGLU, and down projection of every token (R9): the steps
+/// 3-6 above with one expert that all T tokens take (row r = token r).  s double [T][H].
+void oracle_shared_expert(const float* x, int64_t T, int H, int F, const uint8_t* wgu_c, const uint16_t* wgu_s,
+                          const uint8_t* wd_c, const uint16_t* wd_s, double* s, int nthreads) {
+    std::vector<int8_t> xc((size_t)(T * H));
+    std::vector<uint16_t> xs((size_t)(T * H / 32));
+    oracle_quantize_q8(x, T, H, xc.data(), xs.data(), nthreads);
+    std::vector<int32_t> src((size_t)T);
+    for (int64_t t = 0; t < T; ++t) src[(size_t)t] = (int32_t)t;
+    const int32_t offsets[2] = {0, (int32_t)T};
+    std::vector<double> gu((size_t)(T * 2 * F));
+    oracle_gateup(xc.data(), xs.data(), src.data(), offsets, 1, wgu_c, wgu_s, H, F, gu.data(), nthreads);
+    std::vector<int8_t> hc((size_t)(T * F));
+    std::vector<uint16_t> hs((size_t)(T * F / 32));
+    oracle_swiglu_requant(gu.data(), T, F, hc.data(), hs.data(), nthreads);
+    oracle_down(hc.data(), hs.data(), offsets, 1, wd_c, wd_s, H, F, s, nthreads);
+}
+
+/// The combine with the shared expert (R8, R9): Y[t][o] = sum_{k=0}^{K-1} w[t][k] * Dm[slot[t*K+k]][o], then
+/// + sg[t] * S[t][o].
+void oracle_combine_shared(const double* dm, const int32_t* slot, const double* w, const double* s, const double* sg,
+                           int64_t T, int K, int H, double* y, int nthreads) {
+    oracle_combine(dm, slot, w, T, K, H, y, nthreads);
+    parallel_for(T, nthreads, [&](int64_t t0, int64_t t1) {
+        for (int64_t t = t0; t < t1; ++t)
+            for (int64_t o = 0; o < H; ++o) y[t * H + o] += sg[t] * s[t * H + o];
+    });
+}
+
 // ------------------------------------------------------------------------------------------------ whole block
 /// The seven steps in the pages' order on one prompt chunk; y double [T][H].  Returns oracle_group's status.
 int oracle_layer(const float* logits, const float* x, int64_t T, int H, int E, int K, int F, const uint8_t* wgu_c,
@@ -342,6 +388,22 @@ int oracle_layer(const float* logits, const float* x, int64_t T, int H, int E, i
     std::vector<double> dm((size_t)(n * H));
     oracle_down(hc.data(), hs.data(), offsets.data(), E, wd_c, wd_s, H, F, dm.data(), nthreads);
     oracle_combine(dm.data(), slot.data(), w.data(), T, K, H, y, nthreads);
+    return 0;
+}
+
+/// The block with the shared expert (R9): oracle_layer, then + sg[t] * S[t].  y double [T][H].
+int oracle_layer_shared(const float* logits, const float* x, int64_t T, int H, int E, int K, int F,
+                        const uint8_t* wgu_c, const uint16_t* wgu_s, const uint8_t* wd_c, const uint16_t* wd_s,
+                        const uint8_t* sgu_c, const uint16_t* sgu_s, const uint8_t* sd_c, const uint16_t* sd_s,
+                        const float* wsg, double* y, int nthreads) {
+    if (oracle_layer(logits, x, T, H, E, K, F, wgu_c, wgu_s, wd_c, wd_s, y, nthreads) != 0) return -1;
+    std::vector<double> s((size_t)(T * H)), sg((size_t)T);
+    oracle_shared_expert(x, T, H, F, sgu_c, sgu_s, sd_c, sd_s, s.data(), nthreads);
+    oracle_shared_gate(x, wsg, T, H, sg.data(), nthreads);
+    parallel_for(T, nthreads, [&](int64_t t0, int64_t t1) {
+        for (int64_t t = t0; t < t1; ++t)
+            for (int64_t o = 0; o < H; ++o) y[t * H + o] += sg[(size_t)t] * s[(size_t)(t * H + o)];
+    });
     return 0;
 }
 

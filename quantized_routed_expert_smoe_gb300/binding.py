@@ -66,6 +66,11 @@ _SIGS = {
                            ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_combine": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                       ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_shared_gate": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                          ctypes.c_void_p], ctypes.c_int),
+    "smoe_combine_shared": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                             ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+                            ctypes.c_int),
 }
 
 # every symbol include/smoe.h declares
@@ -235,12 +240,33 @@ def smoe_combine(dm, slot, w, y, stream=None):
         _dev(y, torch.float32, "y"), _stream(stream)))
 
 
+def smoe_shared_gate(x, wsg, sg, stream=None):
+    """sg [T] = sigmoid(x [T][H] . w_sg [H]) (the shared expert's scalar gate)."""
+    T, H = x.shape
+    _check("smoe_shared_gate", load_library().smoe_shared_gate(
+        _dev(x, torch.float32, "x"), _dev(wsg, torch.float32, "wsg"), T, H, _dev(sg, torch.float32, "sg"),
+        _stream(stream)))
+
+
+def smoe_combine_shared(dm, slot, w, ds, sg, y, stream=None):
+    T, K = w.shape
+    H = y.shape[1]
+    _check("smoe_combine_shared", load_library().smoe_combine_shared(
+        _dev(dm, torch.float32, "dm"), _dev(slot, torch.int32, "slot"), _dev(w, torch.float32, "w"), T, K, H,
+        _dev(ds, torch.float32, "ds"), _dev(sg, torch.float32, "sg"), _dev(y, torch.float32, "y"), _stream(stream)))
+
+
 # ------------------------------------------------------------------------------------------------ one block
 class SmoeBlock:
     """The routed-expert block for chunks of up to T tokens: weights resident on the device, every intermediate
-    buffer allocated once.  run(logits, x) issues the eight calls on the current stream and returns y [T][H]."""
+    buffer allocated once.  run(logits, x) issues the eight calls on the current stream and returns y [T][H].
 
-    def __init__(self, T: int, H: int, E: int, K: int, F: int, wgu_c, wgu_s, wd_c, wd_s, device="cuda"):
+    shared: optional dict(sgu_c, sgu_s, sd_c, sd_s, wsg) -- a shared expert (gate/up codes [2F][H/4] and scales,
+    down codes [H][F/4] and scales, in the routed experts' format) and its scalar gate row w_sg [H]; every token
+    takes it and the combine adds sigmoid(x . w_sg) times its row."""
+
+    def __init__(self, T: int, H: int, E: int, K: int, F: int, wgu_c, wgu_s, wd_c, wd_s, device="cuda",
+                 shared=None):
         load_library()
         device_check()
         self.T, self.H, self.E, self.K, self.F = T, H, E, K, F
@@ -269,6 +295,30 @@ class SmoeBlock:
         self.hop = e(2, max(n, 1), F, dt=torch.float16)
         self.dm = e(n, H, dt=torch.float32)
         self.y = e(T, H, dt=torch.float32)
+        self.shared = shared is not None
+        if self.shared:
+            lift = lambda a: a[None] if a.ndim == 2 else a  # one expert: [rows][..] -> [1][rows][..]
+            as_np = lambda a: a.cpu().numpy() if isinstance(a, torch.Tensor) else a
+            self.swgu = pack_weights(lift(as_np(shared["sgu_c"])), lift(as_np(shared["sgu_s"])), dev)
+            self.swd = pack_weights(lift(as_np(shared["sd_c"])), lift(as_np(shared["sd_s"])), dev)
+            self.wsg = as_t(shared["wsg"], torch.float32)
+            # the shared expert's grouping: E = 1, K = 1, every id 0 -> row r = token r, its tiles; fixed for T
+            zeros = torch.zeros(T, 1, dtype=torch.int32, device=dev)
+            self.s_counts = e(1 + 3, dt=torch.int32)
+            self.s_offsets = e(2 + 2, dt=torch.int32)
+            self.s_src = e(max(T, 4), dt=torch.int32)
+            self.s_slot = e(max(T, 4), dt=torch.int32)
+            self.s_tiles = e(tiles_bytes(T, 1) // 4, dt=torch.int32)
+            s_work = e(max(group_work_bytes(T, 1), 16), dt=torch.uint8)
+            smoe_group(zeros, 1, self.s_counts[:1], self.s_offsets[:2], self.s_src[:T], self.s_slot[:T],
+                       self.s_tiles, s_work)
+            self.sxop = e(2, max(T, 1), H, dt=torch.float16)
+            self.sgu = e(T, 2 * F, dt=torch.float32)
+            self.shc = e(T, F, dt=torch.int8)
+            self.shs = e(T, F // 32, dt=torch.int16)
+            self.shop = e(2, max(T, 1), F, dt=torch.float16)
+            self.ds = e(T, H, dt=torch.float32)
+            self.sg = e(max(T, 4), dt=torch.float32)
 
     def run(self, logits, x, stream=None):
         smoe_route_topk(logits, self.ids, self.w, stream)
@@ -279,7 +329,16 @@ class SmoeBlock:
         smoe_experts_gateup(self.xop, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.gu, stream)
         smoe_swiglu_requant(self.gu, self.hc, self.hs, self.hop, stream)
         smoe_experts_down(self.hop, self.tiles, self.n, self.E, self.wd, self.H, self.F, self.dm, stream)
-        smoe_combine(self.dm, self.slot, self.w, self.y, stream)
+        if not self.shared:
+            smoe_combine(self.dm, self.slot, self.w, self.y, stream)
+            return self.y
+        T = self.T
+        smoe_shared_gate(x, self.wsg, self.sg[:T], stream)
+        smoe_gather_q8(self.xc, self.xs, self.s_src[:T], self.sxop, stream)
+        smoe_experts_gateup(self.sxop, self.s_tiles, T, 1, self.swgu, self.H, self.F, self.sgu, stream)
+        smoe_swiglu_requant(self.sgu, self.shc, self.shs, self.shop, stream)
+        smoe_experts_down(self.shop, self.s_tiles, T, 1, self.swd, self.H, self.F, self.ds, stream)
+        smoe_combine_shared(self.dm, self.slot, self.w, self.ds, self.sg[:T], self.y, stream)
         return self.y
 
     def device_status(self):

@@ -148,10 +148,12 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
     }
 }
 
-// step 7: Y[t][o] = sum_k w[t][k] * dm[slot[t*K+k]][o], in k order, fp32.  Block (t, y): 128 threads, a float4 each.
-// A slot outside [0, n) (a pair dropped for an out-of-range id) contributes nothing.
+// step 7: Y[t][o] = sum_k w[t][k] * dm[slot[t*K+k]][o], in k order, fp32, then (with a shared expert) + sg[t] *
+// ds[t][o].  Block (t, y): 128 threads, a float4 each.  A slot outside [0, n) (a pair dropped for an out-of-range id)
+// contributes nothing.
 __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ dm, const int32_t* __restrict__ slot,
                                                       const float* __restrict__ w, int K, int H, int64_t n,
+                                                      const float* __restrict__ ds, const float* __restrict__ sg,
                                                       float* __restrict__ y) {
     const int64_t t = blockIdx.x;
     const int o4 = blockIdx.y * blockDim.x + threadIdx.x;
@@ -167,7 +169,37 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
         acc.z = fmaf(wk, d.z, acc.z);
         acc.w = fmaf(wk, d.w, acc.w);
     }
+    if (ds != nullptr) {
+        const float g = __ldg(sg + t);
+        const float4 d = __ldcs(reinterpret_cast<const float4*>(ds + t * H) + o4);
+        acc.x = fmaf(g, d.x, acc.x);
+        acc.y = fmaf(g, d.y, acc.y);
+        acc.z = fmaf(g, d.z, acc.z);
+        acc.w = fmaf(g, d.w, acc.w);
+    }
     reinterpret_cast<float4*>(y + t * H)[o4] = acc;
+}
+
+// The shared expert's scalar gate (page "src/prefill/prefill.cpp", Prefill::run, MoE half: "the shared expert and
+// its scalar gate", a projection of the token onto one row): sg[t] = 1 / (1 + exp(-(x[t] . w_sg))), the dot product
+// in fp32 (lane l sums the float4s l, l + 32, ... of the row, then a butterfly).  One warp per token.
+__global__ void __launch_bounds__(256) shared_gate_kernel(const float4* __restrict__ x, const float4* __restrict__ wsg,
+                                                          int64_t T, int H4, float* __restrict__ sg) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;  // the whole warp
+    const float4* xt = x + t * H4;
+    float acc = 0.0f;
+    for (int i = lane; i < H4; i += 32) {
+        const float4 a = __ldcs(xt + i), b = __ldg(wsg + i);
+        acc = fmaf(a.x, b.x, acc);
+        acc = fmaf(a.y, b.y, acc);
+        acc = fmaf(a.z, b.z, acc);
+        acc = fmaf(a.w, b.w, acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) sg[t] = __fdiv_rn(1.0f, 1.0f + expf(-acc));
 }
 
 // Q2 weights, row-major [E][rows][cols/4] codes + [E][rows][cols/32] scales, to the expert products' packed form:
@@ -307,11 +339,19 @@ cudaError_t launch_gather_q8(const int8_t* codes, const uint16_t* scales, int64_
     return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
-                           cudaStream_t s) {
+cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,
+                           const float* ds, const float* sg, float* y, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
     const dim3 grid((unsigned)T, (unsigned)((H / 4 + 127) / 128));
-    combine_kernel<<<grid, 128, 0, s>>>(dm, slot, w, K, H, T * (int64_t)K, y);
+    combine_kernel<<<grid, 128, 0, s>>>(dm, slot, w, K, H, T * (int64_t)K, ds, sg, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_shared_gate(const float* x, const float* wsg, int64_t T, int H, float* sg, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const int warps = 8;
+    shared_gate_kernel<<<(unsigned)((T + warps - 1) / warps), 32 * warps, 0, s>>>(
+        reinterpret_cast<const float4*>(x), reinterpret_cast<const float4*>(wsg), T, H / 4, sg);
     return cudaGetLastError();
 }
 

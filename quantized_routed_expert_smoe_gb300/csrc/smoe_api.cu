@@ -193,7 +193,26 @@ smoe_status smoe_combine(const float* dm, const int32_t* slot, const float* w, i
     if (!aligned16(dm) || !aligned16(slot) || !aligned16(w) || !aligned16(y)) return SMOE_ERR_ARG;
     if ((H / 4 + 127) / 128 > kMaxGridY) return SMOE_ERR_UNSUPPORTED;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    return launch_status(smoe::launch_combine(dm, slot, w, T, K, H, y, (cudaStream_t)stream));
+    return launch_status(smoe::launch_combine(dm, slot, w, T, K, H, nullptr, nullptr, y, (cudaStream_t)stream));
+}
+
+smoe_status smoe_shared_gate(const float* x, const float* wsg, int64_t T, int H, float* sg, void* stream) {
+    if (T < 0 || H < 4 || H % 4 != 0) return SMOE_ERR_ARG;
+    if (T == 0) return SMOE_OK;
+    if (!aligned16(x) || !aligned16(wsg) || !aligned16(sg)) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_shared_gate(x, wsg, T, H, sg, (cudaStream_t)stream));
+}
+
+smoe_status smoe_combine_shared(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,
+                                const float* ds, const float* sg, float* y, void* stream) {
+    if (T < 0 || K < 1 || K > SMOE_MAX_TOPK || H < 4 || H % 4 != 0) return SMOE_ERR_ARG;
+    if (T == 0) return SMOE_OK;
+    if (!aligned16(dm) || !aligned16(slot) || !aligned16(w) || !aligned16(y) || !aligned16(ds) || !aligned16(sg))
+        return SMOE_ERR_ARG;
+    if ((H / 4 + 127) / 128 > kMaxGridY) return SMOE_ERR_UNSUPPORTED;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_combine(dm, slot, w, T, K, H, ds, sg, y, (cudaStream_t)stream));
 }
 
 }  // extern "C"

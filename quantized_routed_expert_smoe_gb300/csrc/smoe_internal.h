@@ -21,8 +21,9 @@ cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, 
                            uint8_t* packed, cudaStream_t s);
 cudaError_t launch_gather_q8(const int8_t* codes, const uint16_t* scales, int64_t in_rows, int cols,
                              const int32_t* src, int64_t n, uint16_t* out, cudaStream_t s);
-cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
-                           cudaStream_t s);
+cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,
+                           const float* ds, const float* sg, float* y, cudaStream_t s);
+cudaError_t launch_shared_gate(const float* x, const float* wsg, int64_t T, int H, float* sg, cudaStream_t s);
 
 // Grouped expert product (both the gate/up and the down step): for every tile of the tile list and every 128-row
 // slice of the expert's weight matrix, OUT[row][j] = sum over K of W[e][j][i] * B[row][i], W the decoded 2-bit

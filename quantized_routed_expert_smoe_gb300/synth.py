@@ -10,6 +10,10 @@ Generator: numpy's PCG64 (``numpy.random.default_rng(seed)``), draws in a fixed 
   gate/up codes bytes [E][2F][H/4] uniform (so every 2-bit code is uniform on {0..3}); gate/up scales
   U[0.005, 0.02] -> fp16 [E][2F][H/32]; down codes [E][H][F/4]; down scales [E][H][F/32].
 
+Shared expert (``make_shared``): its own generator, PCG64 seeded with 1000 + the chunk's seed, so the routed inputs
+above do not change: gate/up codes [2F][H/4], scales, down codes [H][F/4], scales (the distributions of the routed
+experts), then the gate row w_sg [H] fp32 N(0, sigma_r).
+
 Weight format (the library's and the oracle's): a 32-weight block has one fp16 scale d and 2-bit codes q,
 w = d * (q - 2); codes are packed four to a byte, weight 4j+i in bits 2i..2i+1 of byte j; gate rows [0, F) and up
 rows [F, 2F) of an expert's gate/up matrix; every expert of a matrix contiguous, expert-major.
@@ -104,3 +108,18 @@ def make_rows(rows: int, cols: int, seed: int, scale: float = 1.0) -> np.ndarray
 def make_dm(n: int, H: int, seed: int) -> np.ndarray:
     rng = np.random.default_rng(seed)
     return rng.standard_normal((n, H), dtype=np.float32)
+
+
+def make_shared(cfg_or_inp, sigma: float | None = None) -> dict:
+    """The shared expert of a chunk: one expert's weights in the routed experts' format and the scalar gate's row.
+    Accepts a Config or an input dict made by make_layer / make_custom (uses its T, H, F and seed)."""
+    if isinstance(cfg_or_inp, Config):
+        H, F, seed, sig = cfg_or_inp.H, cfg_or_inp.F, cfg_or_inp.seed, cfg_or_inp.router_sigma
+    else:
+        H, F, seed, sig = cfg_or_inp["H"], cfg_or_inp["F"], cfg_or_inp["seed"], 0.02
+    if sigma is not None:
+        sig = sigma
+    rng = np.random.default_rng(1000 + seed)
+    w = make_weights(rng, 1, H, F)
+    return dict(sgu_c=w["wgu_c"][0], sgu_s=w["wgu_s"][0], sd_c=w["wd_c"][0], sd_s=w["wd_s"][0],
+                wsg=(rng.standard_normal(H) * sig).astype(np.float32))

@@ -75,6 +75,12 @@ def test_host_side_rejections_need_no_gpu(lib):
     assert lib.smoe_swiglu_requant(fake, 4, 96, fake, fake, fake, null) == ARG
     assert lib.smoe_experts_down(fake, fake, 10, 4, fake, 256, 48, fake, null) == UNSUP
     assert lib.smoe_pack_q2(fake, fake, 2, 100, 64, fake, null) == ARG  # rows % 128
+    # shared expert: H % 4, misaligned gate output, misaligned shared rows in the combine
+    assert lib.smoe_shared_gate(fake, fake, 4, 30, fake, null) == ARG
+    assert lib.smoe_shared_gate(fake, fake, 4, 32, odd, null) == ARG
+    assert lib.smoe_shared_gate(fake, fake, 0, 32, fake, null) == 0  # empty chunk: nothing to do
+    assert lib.smoe_combine_shared(fake, fake, fake, 4, 2, 32, odd, fake, fake, null) == ARG
+    assert lib.smoe_combine_shared(fake, fake, fake, 4, 2, 32, fake, null, fake, null) == ARG
     # group: tiles buffer too small
     assert lib.smoe_group(fake, 8, 2, 4, fake, fake, fake, fake, fake, 16, fake, 1 << 20, null) == ARG
     # well-formed arguments on a machine without an sm_103 device: a clean error, never a fallback
