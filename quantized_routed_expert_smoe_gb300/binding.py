@@ -320,7 +320,9 @@ class SmoeBlock:
             self.ds = e(T, H, dt=torch.float32)
             self.sg = e(max(T, 4), dt=torch.float32)
 
-    def run(self, logits, x, stream=None):
+    def run(self, logits, x, stream=None, out=None):
+        """y = the block on (logits [T][E], x [T][H]); into `out` (fp32 [T][H] on the device) when given."""
+        y = self.y if out is None else out
         smoe_route_topk(logits, self.ids, self.w, stream)
         smoe_group(self.ids, self.E, self.counts, self.offsets, self.src[:self.n], self.slot[:self.n], self.tiles,
                    self.work, stream)
@@ -330,21 +332,79 @@ class SmoeBlock:
         smoe_swiglu_requant(self.gu, self.hc, self.hs, self.hop, stream)
         smoe_experts_down(self.hop, self.tiles, self.n, self.E, self.wd, self.H, self.F, self.dm, stream)
         if not self.shared:
-            smoe_combine(self.dm, self.slot, self.w, self.y, stream)
-            return self.y
+            smoe_combine(self.dm, self.slot, self.w, y, stream)
+            return y
         T = self.T
         smoe_shared_gate(x, self.wsg, self.sg[:T], stream)
         smoe_gather_q8(self.xc, self.xs, self.s_src[:T], self.sxop, stream)
         smoe_experts_gateup(self.sxop, self.s_tiles, T, 1, self.swgu, self.H, self.F, self.sgu, stream)
         smoe_swiglu_requant(self.sgu, self.shc, self.shs, self.shop, stream)
         smoe_experts_down(self.shop, self.s_tiles, T, 1, self.swd, self.H, self.F, self.ds, stream)
-        smoe_combine_shared(self.dm, self.slot, self.w, self.ds, self.sg[:T], self.y, stream)
-        return self.y
+        smoe_combine_shared(self.dm, self.slot, self.w, self.ds, self.sg[:T], y, stream)
+        return y
 
     def device_status(self):
         """(group status, kernel status) from the tiles header; reads the device (synchronises)."""
         h = self.tiles[:4].cpu().tolist()
         return h[1], h[3]
+
+
+class SmoePipeline:
+    """A SmoeBlock fed from and into pinned host memory, with the copies overlapped with the compute: step i's inputs
+    go to the device (one copy stream) while step i-1 computes, and its output comes back (another copy stream) while
+    step i+1 computes; device inputs and outputs are double-buffered.
+
+    start(event): the copies of the first step wait for `event` (e.g. recorded on the compute stream before a timed
+    region); submit(h_logits, h_x, h_y) queues one step -- h_y (pinned fp32 [T][H]) holds the result once the step's
+    copy back has completed; drain(): the compute stream waits for every queued copy back; synchronize(): the host
+    waits for all of it."""
+
+    def __init__(self, block: "SmoeBlock", stream=None):
+        self.blk = block
+        dev = block.y.device
+        T, H, E = block.T, block.H, block.E
+        e = lambda *sh: torch.empty(*sh, dtype=torch.float32, device=dev)
+        self.d_logits = [e(T, E), e(T, E)]
+        self.d_x = [e(T, H), e(T, H)]
+        self.d_y = [e(T, H), e(T, H)]
+        self.compute = stream if stream is not None else torch.cuda.current_stream(dev)
+        self.copy_in = torch.cuda.Stream(device=dev)
+        self.copy_out = torch.cuda.Stream(device=dev)
+        self.ev_in = [torch.cuda.Event(), torch.cuda.Event()]    # slot b's inputs are on the device
+        self.ev_done = [torch.cuda.Event(), torch.cuda.Event()]  # slot b's step has computed
+        self.ev_out = [torch.cuda.Event(), torch.cuda.Event()]   # slot b's output is back on the host
+        self.i = 0
+
+    def start(self, event):
+        self.copy_in.wait_event(event)
+        self.copy_out.wait_event(event)
+
+    def submit(self, h_logits, h_x, h_y):
+        b = self.i & 1
+        with torch.cuda.stream(self.copy_in):
+            if self.i >= 2:
+                self.copy_in.wait_event(self.ev_done[b])  # step i-2 has consumed slot b's inputs
+            self.d_logits[b].copy_(h_logits, non_blocking=True)
+            self.d_x[b].copy_(h_x, non_blocking=True)
+            self.ev_in[b].record(self.copy_in)
+        self.compute.wait_event(self.ev_in[b])
+        if self.i >= 2:
+            self.compute.wait_event(self.ev_out[b])  # slot b's previous output is back on the host
+        self.blk.run(self.d_logits[b], self.d_x[b], stream=self.compute, out=self.d_y[b])
+        self.ev_done[b].record(self.compute)
+        with torch.cuda.stream(self.copy_out):
+            self.copy_out.wait_event(self.ev_done[b])
+            h_y.copy_(self.d_y[b], non_blocking=True)
+            self.ev_out[b].record(self.copy_out)
+        self.i += 1
+
+    def drain(self):
+        for k in range(min(self.i, 2)):
+            self.compute.wait_event(self.ev_out[k])
+
+    def synchronize(self):
+        self.drain()
+        self.compute.synchronize()
 
 
 def pack_weights(codes, scales, device="cuda", swiglu=False):

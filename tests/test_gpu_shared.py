@@ -94,3 +94,30 @@ def test_block_with_shared_expert(B, name):
     assert np.abs(y_r - y_o).max() > 0.1 * np.sqrt((y_o ** 2).mean())
     del blk
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("with_shared", [False, True])
+def test_pipeline_matches_run(B, with_shared):
+    # SmoePipeline (host in, host out, copies overlapped with the neighbouring steps' compute) gives every step's
+    # output bit for bit as the plain run on device inputs, over more steps than it has buffers
+    cfg = synth.CONFIGS["tiny"]
+    inp = synth.make_layer(cfg)
+    shared = None
+    if with_shared:
+        inp.update(synth.make_shared(cfg))
+        shared = {k: inp[k] for k in ("sgu_c", "sgu_s", "sd_c", "sd_s", "wsg")}
+    blk = B.SmoeBlock(cfg.T, cfg.H, cfg.E, cfg.K, cfg.F, inp["wgu_c"], inp["wgu_s"], inp["wd_c"], inp["wd_s"],
+                      shared=shared)
+    steps = 5
+    xs = [synth.make_rows(cfg.T, cfg.H, seed=40 + s) for s in range(steps)]
+    lgs = [synth.make_rows(cfg.T, cfg.E, seed=50 + s, scale=0.5) for s in range(steps)]
+    want = [host(blk.run(dev(lgs[s]), dev(xs[s]))).copy() for s in range(steps)]
+    pipe = B.SmoePipeline(blk)
+    h_in = [(torch.from_numpy(lgs[s]).pin_memory(), torch.from_numpy(xs[s]).pin_memory()) for s in range(steps)]
+    h_out = [torch.empty(cfg.T, cfg.H, dtype=torch.float32).pin_memory() for _ in range(steps)]
+    for s in range(steps):
+        pipe.submit(h_in[s][0], h_in[s][1], h_out[s])
+    pipe.synchronize()
+    for s in range(steps):
+        assert np.array_equal(h_out[s].numpy(), want[s]), f"step {s}"
+    assert blk.device_status() == (0, 0)
