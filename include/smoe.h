@@ -203,6 +203,21 @@ smoe_status smoe_experts_down(const uint16_t* hop, int32_t* tiles, int64_t n, in
 smoe_status smoe_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
                          void* stream);
 
+/* Step 1 with the router projection fused in (the logits are never written).  Page "src/prefill/prefill.cpp",
+ * Prefill::run, MoE half: the router is a BF16 projection of the hidden state, with the low part of its BF16 copy,
+ * followed by route().  Here
+ *   xh = bf16_rne(x), xl = bf16_rne(x - xh);  logit[t][e] = sum_h wr[e][h] * (xh[t][h] + xl[t][h])
+ * accumulated in fp32 on the tensor cores, then the top-K and weights exactly as smoe_route_topk (ties to the lower
+ * id; weights exp(l_k - l_1) / sum_j exp(l_j - l_1) over the K).
+ *   x fp32 [T][H], wr bf16 (uint16 bits) [E][H] -> ids int32 [T][K], w fp32 [T][K].
+ *   work: caller scratch of smoe_router_work_bytes(T, H) bytes (the split activations, bf16 [2][T][H]).
+ *   H % 64 == 0; 16 <= E <= 512, E % 16 == 0 (E % 32 == 0 above 256); 1 <= K <= min(E, 16); all pointers
+ *   16-byte aligned.
+ *   If an internal wait gives up, the affected tokens get id -1, which smoe_group reports as SMOE_ERR_RANGE. */
+smoe_status smoe_router_topk(const float* x, const uint16_t* wr, int64_t T, int H, int E, int K, uint16_t* work,
+                             int32_t* ids, float* w, void* stream);
+size_t smoe_router_work_bytes(int64_t T, int H);
+
 /* Shared expert, scalar gate.  Page "src/prefill/prefill.cpp", Prefill::run, MoE half ("the shared expert and its
  * scalar gate": a projection of each token onto one row); the gate's nonlinearity is not given there and is read as
  * the logistic sigmoid:  sg[t] = 1 / (1 + exp(-(x[t] . w_sg))), the dot product in fp32.

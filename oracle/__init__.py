@@ -67,6 +67,9 @@ def lib():
             L.oracle_layer_tokens.argtypes = [vp, vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp,
                                               vp, c_int]
             L.oracle_layer_bruteforce.argtypes = [vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, c_int]
+            L.oracle_bf16_split.argtypes = [vp, i64, vp, vp]
+            L.oracle_router_logits.argtypes = [vp, vp, i64, c_int, c_int, vp, c_int]
+            L.oracle_router_route.argtypes = [vp, vp, i64, c_int, c_int, c_int, vp, vp, vp, c_int]
             L.oracle_shared_gate.argtypes = [vp, vp, i64, c_int, vp, c_int]
             L.oracle_shared_expert.argtypes = [vp, i64, c_int, c_int, vp, vp, vp, vp, vp, c_int]
             L.oracle_combine_shared.argtypes = [vp, vp, vp, vp, vp, i64, c_int, c_int, vp, c_int]
@@ -280,3 +283,35 @@ def layer_tokens_shared(inp: dict, tokens, nthreads: int = 0):
     sa, sb, sc, sd = _shared_weights(inp)
     y = y + shared_gate(xs, inp["wsg"], nthreads)[:, None] * shared_expert(xs, sa, sb, sc, sd, inp["F"], nthreads)
     return y, ids, w
+
+
+# ----------------------------------------------------------------------------------------------- router projection
+def bf16_split(x: np.ndarray):
+    """(xh, xl) bf16 bits (uint16) of fp32 x: xh = bf16_rne(x), xl = bf16_rne(x - xh)."""
+    x = _c(x, np.float32)
+    xh = np.empty(x.shape, np.uint16)
+    xl = np.empty(x.shape, np.uint16)
+    lib().oracle_bf16_split(_ptr(x), x.size, _ptr(xh), _ptr(xl))
+    return xh, xl
+
+
+def router_logits(x: np.ndarray, wr: np.ndarray, nthreads: int = 0) -> np.ndarray:
+    """logits double [T][E] = wr (bf16 bits [E][H]) . (xh + xl)."""
+    x, wr = _c(x, np.float32), _c(wr, np.uint16)
+    T, H = x.shape
+    E = wr.shape[0]
+    out = np.empty((T, E), np.float64)
+    lib().oracle_router_logits(_ptr(x), _ptr(wr), T, H, E, _ptr(out), nthreads)
+    return out
+
+
+def router_route(x: np.ndarray, wr: np.ndarray, K: int, nthreads: int = 0):
+    """Step 1 from the hidden state: (ids [T][K], w double [T][K], logits double [T][E])."""
+    x, wr = _c(x, np.float32), _c(wr, np.uint16)
+    T, H = x.shape
+    E = wr.shape[0]
+    ids = np.empty((T, K), np.int32)
+    w = np.empty((T, K), np.float64)
+    lg = np.empty((T, E), np.float64)
+    lib().oracle_router_route(_ptr(x), _ptr(wr), T, H, E, K, _ptr(ids), _ptr(w), _ptr(lg), nthreads)
+    return ids, w, lg

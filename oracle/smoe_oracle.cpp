@@ -36,6 +36,9 @@
 //      nonlinearity are not given): one more expert of the routed experts' form (2-bit weights, gate/up [2F][H],
 //      down [H][F]) that every token takes, on the same int8 activations; its scalar gate is
 //      sg[t] = sigmoid(x[t] . w_sg) with w_sg fp32 [H]; the combine adds sg[t] * S[t] after the routed sum.
+//   R10 router projection ([P1]: "bf16_proj" of the router weight on the hidden state's BF16 copy and its low part):
+//      router weights bf16 [E][H]; xh = bf16_rne(x), xl = bf16_rne(x - xh) (x - xh exact in fp32);
+//      logit[t][e] = sum_h w[e][h] * (xh + xl) in double, rounded to fp32, then step 1 (R4, R5).
 //
 // Arithmetic: double everywhere except the q8 rule (R3), which is defined in fp32 and emulated here in `float`.
 // Build with -ffp-contract=off so that no fused multiply-add changes a fp32 step.
@@ -91,6 +94,24 @@ uint16_t f2h_rne(float f) {
     const uint32_t halfv = 1u << (shift - 1);
     if (rem > halfv || (rem == halfv && (q & 1u))) q += 1;
     return (uint16_t)(sign | q);
+}
+
+// ---------------------------------------------------------------- bfloat16 (own, from the format: the top 16 bits
+// of binary32, rounded to nearest, ties to even)
+uint16_t f2bf(float f) {
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);  // NaN
+    const uint32_t keep = u >> 16, rest = u & 0xFFFFu;
+    uint32_t r = keep;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) ++r;  // carries into the exponent as the format wants
+    return (uint16_t)r;
+}
+float bf2f(uint16_t b) {
+    const uint32_t u = (uint32_t)b << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return f;
 }
 
 // ---------------------------------------------------------------- threads
@@ -182,6 +203,46 @@ void oracle_route(const float* logits, int64_t T, int E, int K, int32_t* ids, do
             }
         }
     });
+}
+
+/// [P1] the router's BF16 projection of the hidden state with its low part (R10): x fp32 [T][H] -> the two bf16
+/// parts (bits) xh, xl [T][H].
+void oracle_bf16_split(const float* x, int64_t n, uint16_t* xh, uint16_t* xl) {
+    for (int64_t i = 0; i < n; ++i) {
+        xh[i] = f2bf(x[i]);
+        const float rest = x[i] - bf2f(xh[i]);  // exact in fp32
+        xl[i] = f2bf(rest);
+    }
+}
+
+/// logit[t][e] = sum_h wr[e][h] * (xh[t][h] + xl[t][h]) in double (R10); wr bf16 bits [E][H]; logits double [T][E].
+void oracle_router_logits(const float* x, const uint16_t* wr, int64_t T, int H, int E, double* logits,
+                          int nthreads) {
+    parallel_for(T, nthreads, [&](int64_t t0, int64_t t1) {
+        std::vector<uint16_t> xh((size_t)H), xl((size_t)H);
+        std::vector<double> a((size_t)H);
+        for (int64_t t = t0; t < t1; ++t) {
+            oracle_bf16_split(x + t * H, H, xh.data(), xl.data());
+            for (int h = 0; h < H; ++h) a[(size_t)h] = (double)bf2f(xh[(size_t)h]) + (double)bf2f(xl[(size_t)h]);
+            for (int e = 0; e < E; ++e) {
+                double s = 0.0;
+                for (int h = 0; h < H; ++h) s += (double)bf2f(wr[(int64_t)e * H + h]) * a[(size_t)h];
+                logits[t * E + e] = s;
+            }
+        }
+    });
+}
+
+/// Step 1 from the hidden state (R10): the logits above rounded to fp32, then oracle_route.  logits_out (double
+/// [T][E]) may be null.
+void oracle_router_route(const float* x, const uint16_t* wr, int64_t T, int H, int E, int K, int32_t* ids, double* w,
+                         double* logits_out, int nthreads) {
+    std::vector<double> lg((size_t)(T * E));
+    oracle_router_logits(x, wr, T, H, E, lg.data(), nthreads);
+    std::vector<float> lf((size_t)(T * E));
+    for (size_t i = 0; i < lf.size(); ++i) lf[i] = (float)lg[i];
+    oracle_route(lf.data(), T, E, K, ids, w, nthreads);
+    if (logits_out) std::memcpy(logits_out, lg.data(), lg.size() * sizeof(double));
 }
 
 // ------------------------------------------------------------------------------------------------ step 2: group

@@ -66,6 +66,9 @@ _SIGS = {
                            ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_combine": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                       ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_router_topk": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_router_work_bytes": ([ctypes.c_int64, ctypes.c_int], ctypes.c_size_t),
     "smoe_shared_gate": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
                           ctypes.c_void_p], ctypes.c_int),
     "smoe_combine_shared": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -240,6 +243,21 @@ def smoe_combine(dm, slot, w, y, stream=None):
         _dev(y, torch.float32, "y"), _stream(stream)))
 
 
+def router_work_bytes(T: int, H: int) -> int:
+    return int(load_library().smoe_router_work_bytes(T, H))
+
+
+def smoe_router_topk(x, wr, ids, w, work, stream=None):
+    """Router projection (bf16 weights wr [E][H] as int16 bits, activations x fp32 [T][H] split into bf16 hi + lo)
+    fused into the top-K: ids int32 [T][K], w fp32 [T][K]; work: uint8 scratch of router_work_bytes(T, H)."""
+    T, H = x.shape
+    E = wr.shape[0]
+    K = ids.shape[1]
+    _check("smoe_router_topk", load_library().smoe_router_topk(
+        _dev(x, torch.float32, "x"), _dev(wr, torch.int16, "wr"), T, H, E, K, _dev(work, torch.uint8, "work"),
+        _dev(ids, torch.int32, "ids"), _dev(w, torch.float32, "w"), _stream(stream)))
+
+
 def smoe_shared_gate(x, wsg, sg, stream=None):
     """sg [T] = sigmoid(x [T][H] . w_sg [H]) (the shared expert's scalar gate)."""
     T, H = x.shape
@@ -263,10 +281,13 @@ class SmoeBlock:
 
     shared: optional dict(sgu_c, sgu_s, sd_c, sd_s, wsg) -- a shared expert (gate/up codes [2F][H/4] and scales,
     down codes [H][F/4] and scales, in the routed experts' format) and its scalar gate row w_sg [H]; every token
-    takes it and the combine adds sigmoid(x . w_sg) times its row."""
+    takes it and the combine adds sigmoid(x . w_sg) times its row.
+
+    router: optional bf16 router weights (uint16 / int16 bits [E][H]); the block then computes the router projection
+    itself (smoe_router_topk) and run() ignores its logits argument."""
 
     def __init__(self, T: int, H: int, E: int, K: int, F: int, wgu_c, wgu_s, wd_c, wd_s, device="cuda",
-                 shared=None):
+                 shared=None, router=None):
         load_library()
         device_check()
         self.T, self.H, self.E, self.K, self.F = T, H, E, K, F
@@ -295,6 +316,10 @@ class SmoeBlock:
         self.hop = e(2, max(n, 1), F, dt=torch.float16)
         self.dm = e(n, H, dt=torch.float32)
         self.y = e(T, H, dt=torch.float32)
+        self.router = None
+        if router is not None:
+            self.router = _as_i16(router, dev)
+            self.router_work = e(max(router_work_bytes(T, H), 16), dt=torch.uint8)
         self.shared = shared is not None
         if self.shared:
             lift = lambda a: a[None] if a.ndim == 2 else a  # one expert: [rows][..] -> [1][rows][..]
@@ -323,7 +348,10 @@ class SmoeBlock:
     def run(self, logits, x, stream=None, out=None):
         """y = the block on (logits [T][E], x [T][H]); into `out` (fp32 [T][H] on the device) when given."""
         y = self.y if out is None else out
-        smoe_route_topk(logits, self.ids, self.w, stream)
+        if self.router is not None:
+            smoe_router_topk(x, self.router, self.ids, self.w, self.router_work, stream)
+        else:
+            smoe_route_topk(logits, self.ids, self.w, stream)
         smoe_group(self.ids, self.E, self.counts, self.offsets, self.src[:self.n], self.slot[:self.n], self.tiles,
                    self.work, stream)
         smoe_quantize_q8(x, self.xc, self.xs, stream)
@@ -384,7 +412,8 @@ class SmoePipeline:
         with torch.cuda.stream(self.copy_in):
             if self.i >= 2:
                 self.copy_in.wait_event(self.ev_done[b])  # step i-2 has consumed slot b's inputs
-            self.d_logits[b].copy_(h_logits, non_blocking=True)
+            if h_logits is not None:  # a block that computes its own router projection needs none
+                self.d_logits[b].copy_(h_logits, non_blocking=True)
             self.d_x[b].copy_(h_x, non_blocking=True)
             self.ev_in[b].record(self.copy_in)
         self.compute.wait_event(self.ev_in[b])

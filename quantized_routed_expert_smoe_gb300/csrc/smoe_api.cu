@@ -196,6 +196,19 @@ smoe_status smoe_combine(const float* dm, const int32_t* slot, const float* w, i
     return launch_status(smoe::launch_combine(dm, slot, w, T, K, H, nullptr, nullptr, y, (cudaStream_t)stream));
 }
 
+smoe_status smoe_router_topk(const float* x, const uint16_t* wr, int64_t T, int H, int E, int K, uint16_t* work,
+                             int32_t* ids, float* w, void* stream) {
+    if (T < 0 || T > INT32_MAX || H < 64 || H % 64 != 0 || E < 16 || E > 512 || E % 16 != 0 ||
+        (E > 256 && E % 32 != 0) || K < 1 || K > 16 || K > E)
+        return SMOE_ERR_ARG;
+    if (T == 0) return SMOE_OK;
+    if (!aligned16(x) || !aligned16(wr) || !aligned16(work) || !aligned16(ids) || !aligned16(w)) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_router_topk(x, wr, T, H, E, K, work, ids, w, (cudaStream_t)stream));
+}
+
+size_t smoe_router_work_bytes(int64_t T, int H) { return T <= 0 || H <= 0 ? 0 : (size_t)T * (size_t)H * 4; }
+
 smoe_status smoe_shared_gate(const float* x, const float* wsg, int64_t T, int H, float* sg, void* stream) {
     if (T < 0 || H < 4 || H % 4 != 0) return SMOE_ERR_ARG;
     if (T == 0) return SMOE_OK;

@@ -186,6 +186,11 @@ __host__ __device__ __forceinline__ uint32_t idesc_f16_f32(int M, int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with A and B bf16 (1 in both type fields).
+__host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
+    return idesc_f16_f32(M, N) | (1u << 7) | (1u << 10);
+}
+
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 

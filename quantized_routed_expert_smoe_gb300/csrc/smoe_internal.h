@@ -23,6 +23,8 @@ cudaError_t launch_gather_q8(const int8_t* codes, const uint16_t* scales, int64_
                              const int32_t* src, int64_t n, uint16_t* out, cudaStream_t s);
 cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,
                            const float* ds, const float* sg, float* y, cudaStream_t s);
+cudaError_t launch_router_topk(const float* x, const uint16_t* wr, int64_t T, int H, int E, int K, uint16_t* work,
+                               int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_shared_gate(const float* x, const float* wsg, int64_t T, int H, float* sg, cudaStream_t s);
 
 // Grouped expert product (both the gate/up and the down step): for every tile of the tile list and every 128-row

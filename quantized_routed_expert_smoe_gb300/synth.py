@@ -14,6 +14,9 @@ Shared expert (``make_shared``): its own generator, PCG64 seeded with 1000 + the
 above do not change: gate/up codes [2F][H/4], scales, down codes [H][F/4], scales (the distributions of the routed
 experts), then the gate row w_sg [H] fp32 N(0, sigma_r).
 
+Router weights (``make_router``): their own generator, PCG64 seeded with 2000 + the chunk's seed: W_r [E][H]
+N(0, sigma_r), stored as bf16 (the top 16 bits of the fp32 value, rounded to nearest even).
+
 Weight format (the library's and the oracle's): a 32-weight block has one fp16 scale d and 2-bit codes q,
 w = d * (q - 2); codes are packed four to a byte, weight 4j+i in bits 2i..2i+1 of byte j; gate rows [0, F) and up
 rows [F, 2F) of an expert's gate/up matrix; every expert of a matrix contiguous, expert-major.
@@ -123,3 +126,17 @@ def make_shared(cfg_or_inp, sigma: float | None = None) -> dict:
     w = make_weights(rng, 1, H, F)
     return dict(sgu_c=w["wgu_c"][0], sgu_s=w["wgu_s"][0], sd_c=w["wd_c"][0], sd_s=w["wd_s"][0],
                 wsg=(rng.standard_normal(H) * sig).astype(np.float32))
+
+
+def make_router(cfg_or_inp, sigma: float | None = None) -> np.ndarray:
+    """Router weights bf16 bits (uint16) [E][H] for the fused router projection."""
+    if isinstance(cfg_or_inp, Config):
+        E, H, seed, sig = cfg_or_inp.E, cfg_or_inp.H, cfg_or_inp.seed, cfg_or_inp.router_sigma
+    else:
+        E, H, seed, sig = cfg_or_inp["E"], cfg_or_inp["H"], cfg_or_inp["seed"], 0.05
+    if sigma is not None:
+        sig = sigma
+    rng = np.random.default_rng(2000 + seed)
+    u = (rng.standard_normal((E, H)) * sig).astype(np.float32).view(np.uint32)
+    # storage format: keep the top 16 bits, rounded to nearest, ties to even
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
