@@ -48,19 +48,6 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Both phases complete?  One non-blocking test of each barrier, issued back to back (their round trips overlap).
-__device__ __forceinline__ bool mbar_test2(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
-        "and.pred p, p, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(b0), "r"(p0), "r"(b1), "r"(p1)
-        : "memory");
-    return ok != 0;
-}
 // All three phases complete?  (A barrier may be passed twice.)
 __device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2,
                                            uint32_t p2) {
@@ -84,23 +71,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     const uint64_t t0 = global_ns();
     for (;;) {
         if (mbar_try_wait(a, parity)) return true;
-        if (abort != nullptr && *abort) return false;
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-// Wait for the phases of two barriers (`parity0` of bar0, `parity1` of bar1), with mbar_wait's limits.  When both
-// have completed already this costs one round trip instead of two.
-__device__ __forceinline__ bool mbar_wait2(uint64_t* bar0, uint32_t parity0, uint64_t* bar1, uint32_t parity1,
-                                           volatile int* abort) {
-    const uint32_t a0 = smem_u32(bar0), a1 = smem_u32(bar1);
-    if (mbar_test2(a0, parity0, a1, parity1)) return true;
-    bool d0 = false, d1 = false;
-    const uint64_t t0 = global_ns();
-    for (;;) {
-        if (!d0) d0 = mbar_try_wait(a0, parity0);
-        if (!d1) d1 = mbar_try_wait(a1, parity1);
-        if (d0 && d1) return true;
         if (abort != nullptr && *abort) return false;
         if (global_ns() - t0 > kWaitLimitNs) return false;
     }
@@ -193,9 +163,5 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(int M, int N) {
 
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 }  // namespace smoe
