@@ -16,8 +16,8 @@
 //   [P3] same page, include/strata/kernels/qsa_select.hpp: the engine's top-k rule "ties to the lowest index".
 //
 // Readings where the pages are silent or disagree:
-//   R1 weight code offset: w = d * (q - 2) for a 2-bit code q in {0..3} (the moe_fused.hpp header's "q - 1" is not
-//      followed; the problem statement fixes q - 2).
+//   R1 weight code offset: w = d * (q - 2) for a 2-bit code q in {0..3}, i.e. d * {-2, -1, 0, 1}: the weight format
+//      of this library (the moe_fused.hpp header's "q - 1" is not followed).
 //   R2 weight blob: planar per matrix, codes uint8 [rows][cols/4] with weight 4j+i in bits 2i..2i+1 of byte j,
 //      scales fp16 [rows][cols/32]; all experts of one matrix contiguous, expert-major.  Gate rows [0, F), up rows
 //      [F, 2F) of the gate/up matrix.
