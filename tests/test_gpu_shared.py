@@ -96,8 +96,8 @@ def test_block_with_shared_expert(B, name):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("with_shared", [False, True])
-def test_pipeline_matches_run(B, with_shared):
+@pytest.mark.parametrize("with_shared,with_router", [(False, False), (True, False), (True, True)])
+def test_pipeline_matches_run(B, with_shared, with_router):
     # SmoePipeline (host in, host out, copies overlapped with the neighbouring steps' compute) gives every step's
     # output bit for bit as the plain run on device inputs, over more steps than it has buffers
     cfg = synth.CONFIGS["tiny"]
@@ -107,13 +107,15 @@ def test_pipeline_matches_run(B, with_shared):
         inp.update(synth.make_shared(cfg))
         shared = {k: inp[k] for k in ("sgu_c", "sgu_s", "sd_c", "sd_s", "wsg")}
     blk = B.SmoeBlock(cfg.T, cfg.H, cfg.E, cfg.K, cfg.F, inp["wgu_c"], inp["wgu_s"], inp["wd_c"], inp["wd_s"],
-                      shared=shared)
+                      shared=shared, router=synth.make_router(cfg) if with_router else None)
     steps = 5
     xs = [synth.make_rows(cfg.T, cfg.H, seed=40 + s) for s in range(steps)]
     lgs = [synth.make_rows(cfg.T, cfg.E, seed=50 + s, scale=0.5) for s in range(steps)]
     want = [host(blk.run(dev(lgs[s]), dev(xs[s]))).copy() for s in range(steps)]
     pipe = B.SmoePipeline(blk)
-    h_in = [(torch.from_numpy(lgs[s]).pin_memory(), torch.from_numpy(xs[s]).pin_memory()) for s in range(steps)]
+    # a block with its own router projection takes no logits: the pipeline copies none
+    h_in = [(None if with_router else torch.from_numpy(lgs[s]).pin_memory(), torch.from_numpy(xs[s]).pin_memory())
+            for s in range(steps)]
     h_out = [torch.empty(cfg.T, cfg.H, dtype=torch.float32).pin_memory() for _ in range(steps)]
     for s in range(steps):
         pipe.submit(h_in[s][0], h_in[s][1], h_out[s])
