@@ -32,11 +32,11 @@
 //   R7 SwiGLU: h_j = silu(g_j) * u_j, silu(g) = g / (1 + exp(-g)), gate = rows [0, F), up = rows [F, 2F); h is
 //      rounded to fp32 before the q8 rule of R3 (the rule is defined on fp32 input).
 //   R8 combine: Y[t] = sum over k (in k order) of w[t][k] * Dm[slot[t*K+k]].
-//   R9 shared expert (the "shared expert and its scalar gate" of [P1]; its weight format, width and the gate's
+//   R14 shared expert (the "shared expert and its scalar gate" of [P1]; its weight format, width and the gate's
 //      nonlinearity are not given): one more expert of the routed experts' form (2-bit weights, gate/up [2F][H],
 //      down [H][F]) that every token takes, on the same int8 activations; its scalar gate is
 //      sg[t] = sigmoid(x[t] . w_sg) with w_sg fp32 [H]; the combine adds sg[t] * S[t] after the routed sum.
-//   R10 router projection ([P1]: "bf16_proj" of the router weight on the hidden state's BF16 copy and its low part):
+//   R15 router projection ([P1]: "bf16_proj" of the router weight on the hidden state's BF16 copy and its low part):
 //      router weights bf16 [E][H]; xh = bf16_rne(x), xl = bf16_rne(x - xh) (x - xh exact in fp32);
 //      logit[t][e] = sum_h w[e][h] * (xh + xl) in double, rounded to fp32, then step 1 (R4, R5).
 //
@@ -205,7 +205,7 @@ void oracle_route(const float* logits, int64_t T, int E, int K, int32_t* ids, do
     });
 }
 
-/// [P1] the router's BF16 projection of the hidden state with its low part (R10): x fp32 [T][H] -> the two bf16
+/// [P1] the router's BF16 projection of the hidden state with its low part (R15): x fp32 [T][H] -> the two bf16
 /// parts (bits) xh, xl [T][H].
 void oracle_bf16_split(const float* x, int64_t n, uint16_t* xh, uint16_t* xl) {
     for (int64_t i = 0; i < n; ++i) {
@@ -215,7 +215,7 @@ void oracle_bf16_split(const float* x, int64_t n, uint16_t* xh, uint16_t* xl) {
     }
 }
 
-/// logit[t][e] = sum_h wr[e][h] * (xh[t][h] + xl[t][h]) in double (R10); wr bf16 bits [E][H]; logits double [T][E].
+/// logit[t][e] = sum_h wr[e][h] * (xh[t][h] + xl[t][h]) in double (R15); wr bf16 bits [E][H]; logits double [T][E].
 void oracle_router_logits(const float* x, const uint16_t* wr, int64_t T, int H, int E, double* logits,
                           int nthreads) {
     parallel_for(T, nthreads, [&](int64_t t0, int64_t t1) {
@@ -233,7 +233,7 @@ void oracle_router_logits(const float* x, const uint16_t* wr, int64_t T, int H, 
     });
 }
 
-/// Step 1 from the hidden state (R10): the logits above rounded to fp32, then oracle_route.  logits_out (double
+/// Step 1 from the hidden state (R15): the logits above rounded to fp32, then oracle_route.  logits_out (double
 /// [T][E]) may be null.
 void oracle_router_route(const float* x, const uint16_t* wr, int64_t T, int H, int E, int K, int32_t* ids, double* w,
                          double* logits_out, int nthreads) {
@@ -387,7 +387,7 @@ void oracle_combine(const double* dm, const int32_t* slot, const double* w, int6
 
 // ------------------------------------------------------------------------------------------------ shared expert
 /// [P1] Prefill::run, MoE half, "the shared expert and its scalar gate": the gate is a projection of the token onto
-/// one row, read as sg[t] = sigmoid(sum_h x[t][h] * w_sg[h]) in double (R9).  x fp32 [T][H], wsg fp32 [H].
+/// one row, read as sg[t] = sigmoid(sum_h x[t][h] * w_sg[h]) in double (R14).  x fp32 [T][H], wsg fp32 [H].
 void oracle_shared_gate(const float* x, const float* wsg, int64_t T, int H, double* sg, int nthreads) {
     parallel_for(T, nthreads, [&](int64_t t0, int64_t t1) {
         for (int64_t t = t0; t < t1; ++t) {
@@ -398,7 +398,7 @@ void oracle_shared_gate(const float* x, const float* wsg, int64_t T, int H, doub
     });
 }
 
-/// [P1] the shared expert's gate and up projections, SwiGLU, and down projection of every token (R9): the steps
+/// [P1] the shared expert's gate and up projections, SwiGLU, and down projection of every token (R14): the steps
 /// 3-6 above with one expert that all T tokens take (row r = token r).  s double [T][H].
 void oracle_shared_expert(const float* x, int64_t T, int H, int F, const uint8_t* wgu_c, const uint16_t* wgu_s,
                           const uint8_t* wd_c, const uint16_t* wd_s, double* s, int nthreads) {
@@ -416,7 +416,7 @@ void oracle_shared_expert(const float* x, int64_t T, int H, int F, const uint8_t
     oracle_down(hc.data(), hs.data(), offsets, 1, wd_c, wd_s, H, F, s, nthreads);
 }
 
-/// The combine with the shared expert (R8, R9): Y[t][o] = sum_{k=0}^{K-1} w[t][k] * Dm[slot[t*K+k]][o], then
+/// The combine with the shared expert (R8, R14): Y[t][o] = sum_{k=0}^{K-1} w[t][k] * Dm[slot[t*K+k]][o], then
 /// + sg[t] * S[t][o].
 void oracle_combine_shared(const double* dm, const int32_t* slot, const double* w, const double* s, const double* sg,
                            int64_t T, int K, int H, double* y, int nthreads) {
@@ -452,7 +452,7 @@ int oracle_layer(const float* logits, const float* x, int64_t T, int H, int E, i
     return 0;
 }
 
-/// The block with the shared expert (R9): oracle_layer, then + sg[t] * S[t].  y double [T][H].
+/// The block with the shared expert (R14): oracle_layer, then + sg[t] * S[t].  y double [T][H].
 int oracle_layer_shared(const float* logits, const float* x, int64_t T, int H, int E, int K, int F,
                         const uint8_t* wgu_c, const uint16_t* wgu_s, const uint8_t* wd_c, const uint16_t* wd_s,
                         const uint8_t* sgu_c, const uint16_t* sgu_s, const uint8_t* sd_c, const uint16_t* sd_s,
