@@ -48,6 +48,9 @@ def test_sizing_helpers(lib):
     assert binding.tiles_bytes(128, 16) == 16 * 18
     assert binding.group_work_bytes(81920, 512) >= 512 * 4
     assert binding.pack_q2_bytes(2, 128, 64) == 2 * 128 * (16 + 4)
+    # the router's scratch: the bf16 hi and lo planes of the activations
+    assert binding.router_work_bytes(8192, 2560) == 2 * 2 * 8192 * 2560
+    assert binding.router_work_bytes(0, 2560) == 0
 
 
 def test_host_side_rejections_need_no_gpu(lib):
@@ -81,6 +84,13 @@ def test_host_side_rejections_need_no_gpu(lib):
     assert lib.smoe_shared_gate(fake, fake, 0, 32, fake, null) == 0  # empty chunk: nothing to do
     assert lib.smoe_combine_shared(fake, fake, fake, 4, 2, 32, odd, fake, fake, null) == ARG
     assert lib.smoe_combine_shared(fake, fake, fake, 4, 2, 32, fake, null, fake, null) == ARG
+    # router: H % 64, E out of range or not a multiple of 16 (of 32 above 256), K > 16
+    assert lib.smoe_router_topk(fake, fake, 4, 96, 64, 2, fake, fake, fake, null) == ARG
+    assert lib.smoe_router_topk(fake, fake, 4, 128, 8, 2, fake, fake, fake, null) == ARG
+    assert lib.smoe_router_topk(fake, fake, 4, 128, 528, 2, fake, fake, fake, null) == ARG
+    assert lib.smoe_router_topk(fake, fake, 4, 128, 272, 2, fake, fake, fake, null) == ARG
+    assert lib.smoe_router_topk(fake, fake, 4, 128, 64, 17, fake, fake, fake, null) == ARG
+    assert lib.smoe_router_topk(fake, fake, 0, 128, 64, 2, fake, fake, fake, null) == 0  # empty chunk
     # group: tiles buffer too small
     assert lib.smoe_group(fake, 8, 2, 4, fake, fake, fake, fake, fake, 16, fake, 1 << 20, null) == ARG
     # well-formed arguments on a machine without an sm_103 device: a clean error, never a fallback
