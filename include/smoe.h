@@ -210,7 +210,8 @@ smoe_status smoe_combine(const float* dm, const int32_t* slot, const float* w, i
  * accumulated in fp32 on the tensor cores, then the top-K and weights exactly as smoe_route_topk (ties to the lower
  * id; weights exp(l_k - l_1) / sum_j exp(l_j - l_1) over the K).
  *   x fp32 [T][H], wr bf16 (uint16 bits) [E][H] -> ids int32 [T][K], w fp32 [T][K].
- *   work: caller scratch of smoe_router_work_bytes(T, H) bytes (the split activations, bf16 [2][T][H]).
+ *   work: caller scratch of smoe_router_work_bytes(T, H) bytes (the split activations, bf16 [2][T][H], then the
+ *   top-K candidates of the two halves of E when E > 256).
  *   H % 64 == 0; 16 <= E <= 512, E % 16 == 0 (E % 32 == 0 above 256); 1 <= K <= min(E, 16); all pointers
  *   16-byte aligned.
  *   If an internal wait gives up, the affected tokens get id -1, which smoe_group reports as SMOE_ERR_RANGE. */

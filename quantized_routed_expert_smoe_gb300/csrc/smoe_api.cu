@@ -207,7 +207,10 @@ smoe_status smoe_router_topk(const float* x, const uint16_t* wr, int64_t T, int 
     return launch_status(smoe::launch_router_topk(x, wr, T, H, E, K, work, ids, w, (cudaStream_t)stream));
 }
 
-size_t smoe_router_work_bytes(int64_t T, int H) { return T <= 0 || H <= 0 ? 0 : (size_t)T * (size_t)H * 4; }
+size_t smoe_router_work_bytes(int64_t T, int H) {
+    // the bf16 hi and lo planes [2][T][H], then two parts' candidates (fp32 logit, int32 id) [T][2][16] each
+    return T <= 0 || H <= 0 ? 0 : (size_t)T * (size_t)H * 4 + (size_t)T * 256;
+}
 
 smoe_status smoe_shared_gate(const float* x, const float* wsg, int64_t T, int H, float* sg, void* stream) {
     if (T < 0 || H < 4 || H % 4 != 0) return SMOE_ERR_ARG;

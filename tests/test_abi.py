@@ -48,8 +48,8 @@ def test_sizing_helpers(lib):
     assert binding.tiles_bytes(128, 16) == 16 * 18
     assert binding.group_work_bytes(81920, 512) >= 512 * 4
     assert binding.pack_q2_bytes(2, 128, 64) == 2 * 128 * (16 + 4)
-    # the router's scratch: the bf16 hi and lo planes of the activations
-    assert binding.router_work_bytes(8192, 2560) == 2 * 2 * 8192 * 2560
+    # the router's scratch: the bf16 hi and lo planes of the activations, then two halves' top-16 candidates
+    assert binding.router_work_bytes(8192, 2560) == 2 * 2 * 8192 * 2560 + 8192 * 2 * 16 * 8
     assert binding.router_work_bytes(0, 2560) == 0
 
 
