@@ -124,6 +124,8 @@ smoe_status smoe_group(const int32_t* ids, int64_t T, int K, int E, int32_t* cou
  * 192 KiB) lives in a __device__ array inside the library that every GPU loading it keeps until the process exits.
  * No cudaMalloc, cudaFree or allocating routine is called.  The first call on a device looks the array's device
  * address up (cudaGetSymbolAddress, with that device current); make that first call before any stream capture.
+ * The address is kept with the identity of the device's context: the first call after that context was destroyed
+ * (cudaDeviceReset) looks it up again, so it too belongs before any capture.
  * Every call on a device shares the one array: calls whose kernels overlap on the GPU race and give wrong tables.
  * A size whose scratch would not fit is refused with SMOE_ERR_UNSUPPORTED (no valid T, K, E reaches it). */
 smoe_status smoe_group_noalloc(const int32_t* ids, int64_t T, int K, int E, int32_t* counts, int32_t* offsets,

@@ -22,9 +22,6 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-TILE_ROWS = 192  # must equal oracle_tile_rows() in the C++ file (checked at load)
-
-
 def build(force: bool = False) -> str:
     """Compile the oracle with g++ (no fused multiply-add contraction, so the fp32 q8 rule is exact IEEE)."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
@@ -52,9 +49,8 @@ def lib():
             L.oracle_f2h.restype = ctypes.c_uint16
             L.oracle_h2f.argtypes = [ctypes.c_uint16]
             L.oracle_h2f.restype = ctypes.c_float
-            L.oracle_tile_rows.restype = i64
             L.oracle_route.argtypes = [vp, i64, c_int, c_int, vp, vp, c_int]
-            L.oracle_group.argtypes = [vp, i64, c_int, c_int, vp, vp, vp, vp, vp]
+            L.oracle_group.argtypes = [vp, i64, c_int, c_int, vp, vp, vp, vp]
             L.oracle_group.restype = c_int
             L.oracle_quantize_q8.argtypes = [vp, i64, i64, vp, vp, c_int]
             L.oracle_gateup.argtypes = [vp, vp, vp, vp, c_int, vp, vp, c_int, c_int, vp, c_int]
@@ -66,6 +62,8 @@ def lib():
             L.oracle_layer.restype = c_int
             L.oracle_layer_tokens.argtypes = [vp, vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp,
                                               vp, c_int]
+            L.oracle_layer_tokens_h.argtypes = [vp, vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp,
+                                                vp, vp, vp, vp, c_int]
             L.oracle_layer_bruteforce.argtypes = [vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, c_int]
             L.oracle_bf16_split.argtypes = [vp, i64, vp, vp]
             L.oracle_router_logits.argtypes = [vp, vp, i64, c_int, c_int, vp, c_int]
@@ -76,7 +74,6 @@ def lib():
             L.oracle_layer_shared.argtypes = [vp, vp, i64, c_int, c_int, c_int, c_int, vp, vp, vp, vp, vp, vp, vp, vp,
                                               vp, vp, c_int]
             L.oracle_layer_shared.restype = c_int
-            assert L.oracle_tile_rows() == TILE_ROWS
             _lib = L
     return _lib
 
@@ -109,10 +106,6 @@ def route(logits: np.ndarray, K: int, nthreads: int = 0):
     return ids, w
 
 
-def max_tiles(n: int, E: int) -> int:
-    return (n + TILE_ROWS - 1) // TILE_ROWS + min(E, n)
-
-
 def group(ids: np.ndarray, E: int):
     ids = _c(ids, np.int32)
     T, K = ids.shape
@@ -121,12 +114,10 @@ def group(ids: np.ndarray, E: int):
     offsets = np.empty(E + 1, np.int32)
     src = np.empty(n, np.int32)
     slot = np.empty(n, np.int32)
-    tiles = np.zeros(4 + 4 * max_tiles(n, E), np.int32)
-    rc = lib().oracle_group(_ptr(ids), T, K, E, _ptr(counts), _ptr(offsets), _ptr(src), _ptr(slot), _ptr(tiles))
+    rc = lib().oracle_group(_ptr(ids), T, K, E, _ptr(counts), _ptr(offsets), _ptr(src), _ptr(slot))
     if rc != 0:
         raise ValueError("routed id out of range")
-    nt = int(tiles[0])
-    return dict(counts=counts, offsets=offsets, src=src, slot=slot, tiles=tiles[4:4 + 4 * nt].reshape(nt, 4).copy())
+    return dict(counts=counts, offsets=offsets, src=src, slot=slot)
 
 
 def quantize_q8(x: np.ndarray, nthreads: int = 0):
@@ -214,6 +205,26 @@ def layer_tokens(inp: dict, tokens, nthreads: int = 0):
     lib().oracle_layer_tokens(_ptr(logits), _ptr(x), _ptr(tokens), ntok, H, E, K, F, _ptr(a), _ptr(b), _ptr(c),
                               _ptr(d), _ptr(y), _ptr(ids), _ptr(w), nthreads)
     return y, ids, w
+
+
+def layer_tokens_h(inp: dict, tokens, nthreads: int = 0):
+    """layer_tokens plus each listed token's step-5 intermediates per slot k: returns (y [ntok][H], ids, w,
+    h fp32 [ntok][K][F], hc int8 [ntok][K][F], hs fp16 bits [ntok][K][F/32])."""
+    logits, x = _c(inp["logits"], np.float32), _c(inp["x"], np.float32)
+    H = x.shape[1]
+    E, K, F = inp["E"], inp["K"], inp["F"]
+    tokens = _c(tokens, np.int64)
+    ntok = tokens.shape[0]
+    a, b, c, d = _weights(inp)
+    y = np.empty((ntok, H), np.float64)
+    ids = np.empty((ntok, K), np.int32)
+    w = np.empty((ntok, K), np.float64)
+    h = np.empty((ntok, K, F), np.float32)
+    hc = np.empty((ntok, K, F), np.int8)
+    hs = np.empty((ntok, K, F // 32), np.uint16)
+    lib().oracle_layer_tokens_h(_ptr(logits), _ptr(x), _ptr(tokens), ntok, H, E, K, F, _ptr(a), _ptr(b), _ptr(c),
+                                _ptr(d), _ptr(y), _ptr(ids), _ptr(w), _ptr(h), _ptr(hc), _ptr(hs), nthreads)
+    return y, ids, w, h, hc, hs
 
 
 def layer_bruteforce(inp: dict, nthreads: int = 0) -> np.ndarray:

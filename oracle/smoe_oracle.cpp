@@ -27,8 +27,9 @@
 //   R4 top-k order: by logit descending, ties to the lower expert id; ids are emitted in that order.
 //   R5 weights: softmax, top-K, renormalised over the K:  w_k = exp(l_k - l_1) / sum_{j in top-K} exp(l_j - l_1);
 //      the full softmax denominator cancels.
-//   R6 grouping: stable by pair index i = t*K + k (the host loop's order); the pages' 64-row tiles become tiles of at
-//      most 192 rows, each expert's c rows split into ceil(c/192) parts [floor(i*c/nt), floor((i+1)*c/nt)).
+//   R6 grouping: stable by pair index i = t*K + k (the host loop's order).  The pages' group() also emits a tile list
+//      (64-row tiles) that only schedules their kernels; which rows share a tile changes no value of the block, so
+//      the oracle defines no tile list (the library's own is checked by the invariants any valid tiling meets).
 //   R7 SwiGLU: h_j = silu(g_j) * u_j, silu(g) = g / (1 + exp(-g)), gate = rows [0, F), up = rows [F, 2F); h is
 //      rounded to fp32 before the q8 rule of R3 (the rule is defined on fp32 input).
 //   R8 combine: Y[t] = sum over k (in k order) of w[t][k] * Dm[slot[t*K+k]].
@@ -177,8 +178,6 @@ extern "C" {
 uint16_t oracle_f2h(float f) { return f2h_rne(f); }
 float oracle_h2f(uint16_t h) { return h2f(h); }
 
-/// Most rows in one tile of the tile list (R6).
-int64_t oracle_tile_rows() { return 192; }
 
 // ------------------------------------------------------------------------------------------------ step 1: route
 /// [P1] Prefill::run, MoE half, route(logits, ids, w, T, n_expert): softmax over the E router logits of each token,
@@ -247,12 +246,10 @@ void oracle_router_route(const float* x, const uint16_t* wr, int64_t T, int H, i
 
 // ------------------------------------------------------------------------------------------------ step 2: group
 /// [P1] the host grouping loop of Prefill::run (count per expert, exclusive offsets, then in pair order
-/// slot[i] = next row of expert ids[i], src[row] = i / K), and [P3] moe_fused.hpp group(): the same tables plus a
-/// tile list over each expert's rows (R6).
-/// tiles int32: [0] = number of tiles, [1..3] = 0, then per tile {expert, first row, rows, 0}.
+/// slot[i] = next row of expert ids[i], src[row] = i / K), as [P3] moe_fused.hpp group() builds the same tables (R6).
 /// Returns 0, or -1 if an id is out of range (nothing else is then defined).
 int oracle_group(const int32_t* ids, int64_t T, int K, int E, int32_t* counts, int32_t* offsets, int32_t* src,
-                 int32_t* slot, int32_t* tiles) {
+                 int32_t* slot) {
     const int64_t n = T * K;
     for (int e = 0; e < E; ++e) counts[e] = 0;
     for (int64_t i = 0; i < n; ++i) {
@@ -266,27 +263,6 @@ int oracle_group(const int32_t* ids, int64_t T, int K, int E, int32_t* counts, i
         const int32_t row = fill[(size_t)ids[i]]++;
         slot[i] = row;
         src[row] = (int32_t)(i / K);
-    }
-    if (tiles) {
-        const int64_t R = oracle_tile_rows();
-        int32_t nt_total = 0;
-        int32_t* out = tiles + 4;
-        for (int e = 0; e < E; ++e) {
-            const int64_t c = counts[e];
-            if (c == 0) continue;
-            const int64_t nt = (c + R - 1) / R;
-            for (int64_t i = 0; i < nt; ++i) {
-                const int64_t a = i * c / nt, b = (i + 1) * c / nt;
-                out[0] = e;
-                out[1] = (int32_t)(offsets[e] + a);
-                out[2] = (int32_t)(b - a);
-                out[3] = 0;
-                out += 4;
-                ++nt_total;
-            }
-        }
-        tiles[0] = nt_total;
-        tiles[1] = tiles[2] = tiles[3] = 0;
     }
     return 0;
 }
@@ -435,7 +411,7 @@ int oracle_layer(const float* logits, const float* x, int64_t T, int H, int E, i
     std::vector<int32_t> ids((size_t)n), counts((size_t)E), offsets((size_t)E + 1), src((size_t)n), slot((size_t)n);
     std::vector<double> w((size_t)n);
     oracle_route(logits, T, E, K, ids.data(), w.data(), nthreads);
-    if (oracle_group(ids.data(), T, K, E, counts.data(), offsets.data(), src.data(), slot.data(), nullptr) != 0)
+    if (oracle_group(ids.data(), T, K, E, counts.data(), offsets.data(), src.data(), slot.data()) != 0)
         return -1;
     std::vector<int8_t> xc((size_t)(T * H));
     std::vector<uint16_t> xs((size_t)(T * H / 32));
@@ -472,9 +448,25 @@ int oracle_layer_shared(const float* logits, const float* x, int64_t T, int H, i
 /// on where the grouping puts it).  Used where the whole chunk is too large for the oracle.  For each listed token
 /// t: route its logits, quantise its x row, and for each of its K experts: gate/up, SwiGLU + requant, down; then the
 /// weighted combine.  y double [ntok][H]; ids_out int32 [ntok][K] and w_out double [ntok][K] may be null.
+void oracle_layer_tokens_h(const float* logits, const float* x, const int64_t* tokens, int64_t ntok, int H, int E,
+                           int K, int F, const uint8_t* wgu_c, const uint16_t* wgu_s, const uint8_t* wd_c,
+                           const uint16_t* wd_s, double* y, int32_t* ids_out, double* w_out, float* h_out,
+                           int8_t* hc_out, uint16_t* hs_out, int nthreads);
+
 void oracle_layer_tokens(const float* logits, const float* x, const int64_t* tokens, int64_t ntok, int H, int E,
                          int K, int F, const uint8_t* wgu_c, const uint16_t* wgu_s, const uint8_t* wd_c,
                          const uint16_t* wd_s, double* y, int32_t* ids_out, double* w_out, int nthreads) {
+    oracle_layer_tokens_h(logits, x, tokens, ntok, H, E, K, F, wgu_c, wgu_s, wd_c, wd_s, y, ids_out, w_out, nullptr,
+                          nullptr, nullptr, nthreads);
+}
+
+/// oracle_layer_tokens that also hands out, per listed token s and slot k, the step-5 intermediates of that pair:
+/// h_out fp32 [ntok][K][F] (h rounded to fp32, the q8 rule's input), hc_out int8 [ntok][K][F] and hs_out fp16 bits
+/// [ntok][K][F/32] (its q8 codes and scales).  Any of the three may be null.
+void oracle_layer_tokens_h(const float* logits, const float* x, const int64_t* tokens, int64_t ntok, int H, int E,
+                           int K, int F, const uint8_t* wgu_c, const uint16_t* wgu_s, const uint8_t* wd_c,
+                           const uint16_t* wd_s, double* y, int32_t* ids_out, double* w_out, float* h_out,
+                           int8_t* hc_out, uint16_t* hs_out, int nthreads) {
     parallel_for(ntok, nthreads, [&](int64_t s0, int64_t s1) {
         std::vector<int32_t> ids((size_t)K);
         std::vector<double> w((size_t)K), gu((size_t)2 * F), dm((size_t)H);
@@ -493,6 +485,11 @@ void oracle_layer_tokens(const float* logits, const float* x, const int64_t* tok
                     gu[(size_t)j] = q2_q8_dot(wgu_c + wrow * (H / 4), wgu_s + wrow * (H / 32), xc.data(), xs.data(), H);
                 }
                 oracle_swiglu_requant(gu.data(), 1, F, hc.data(), hs.data(), 1);
+                const int64_t pk = s * K + k;
+                if (h_out)
+                    for (int j = 0; j < F; ++j) h_out[pk * F + j] = (float)(silu(gu[(size_t)j]) * gu[(size_t)(F + j)]);
+                if (hc_out) std::memcpy(hc_out + pk * F, hc.data(), (size_t)F);
+                if (hs_out) std::memcpy(hs_out + pk * (F / 32), hs.data(), (size_t)(F / 32) * sizeof(uint16_t));
                 for (int64_t o = 0; o < H; ++o) {
                     const int64_t wrow = e * H + o;
                     dm[(size_t)o] = q2_q8_dot(wd_c + wrow * (F / 4), wd_s + wrow * (F / 32), hc.data(), hs.data(), F);

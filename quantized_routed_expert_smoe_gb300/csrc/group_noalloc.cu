@@ -12,7 +12,10 @@
 // left by the previous call are simply replaced.  All calls on one device share the one array: two calls whose
 // kernels overlap on the GPU (different streams, no ordering between them) race on it and give wrong tables.
 // The first call on a device looks up the array's device address (cudaGetSymbolAddress with that device current);
-// that first call should come before any stream capture.
+// that first call should come before any stream capture.  The address is kept per device together with the identity
+// of the device's CUDA context; a call that finds a different context (the old one was destroyed, e.g. by
+// cudaDeviceReset, and the library's module loaded again) looks the address up again instead of using a stale one.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -28,12 +31,44 @@ static __device__ __align__(256) int32_t g_group_scratch[kNoallocScratchInts];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-int32_t* g_scratch_addr[kMaxDevices] = {};
+struct ScratchAddr {
+    int32_t* ptr;
+    unsigned long long ctx_id;  // the context the address belongs to (0: not known)
+};
+ScratchAddr g_scratch_addr[kMaxDevices] = {};
 
 bool aligned16(const void* p) { return p != nullptr && ((uintptr_t)p & 15u) == 0; }
 
-// The device address of this device's copy of the array, looked up once per device (with that device current).
-// In host code the array's name stands for a host-side shadow, never for device memory, so the kernels get this.
+// The unique id of the calling thread's current CUDA context (driver entry points looked up through the runtime,
+// so that the library needs no link to the driver library); false when there is none yet or the lookup fails.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+        cudaGetLastError();
+        looked_up = true;
+    }
+    CUcontext ctx = nullptr;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+        return false;
+    return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
+
+// The device address of this device's copy of the array, looked up with that device current on the first call and
+// again whenever the device's context has changed since.  In host code the array's name stands for a host-side
+// shadow, never for device memory, so the kernels get this address.
 smoe_status scratch_address(int32_t** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -41,15 +76,23 @@ smoe_status scratch_address(int32_t** out) {
         return SMOE_ERR_UNSUPPORTED;
     }
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchAddr& c = g_scratch_addr[dev];
+    unsigned long long id = 0;
+    const bool known = current_context_id(&id);
+    if (c.ptr == nullptr || !known || c.ctx_id != id) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_group_scratch) != cudaSuccess || p == nullptr) {
             cudaGetLastError();
+            c.ptr = nullptr;
             return SMOE_ERR_LAUNCH;
         }
-        g_scratch_addr[dev] = static_cast<int32_t*>(p);
+        c.ptr = static_cast<int32_t*>(p);
+        // the lookup has made the context current if it was not yet; a context that still cannot be identified
+        // leaves ctx_id 0, and every call then looks the address up again
+        unsigned long long id2 = 0;
+        c.ctx_id = current_context_id(&id2) ? id2 : 0ull;
     }
-    *out = g_scratch_addr[dev];
+    *out = c.ptr;
     return SMOE_OK;
 }
 
@@ -59,8 +102,8 @@ extern "C" smoe_status smoe_group_noalloc(const int32_t* ids, int64_t T, int K, 
                                           int32_t* offsets, int32_t* src, int32_t* slot, int32_t* tiles,
                                           size_t tiles_bytes, void* stream) {
     if (T < 0 || E < 1 || E > SMOE_MAX_EXPERTS || K < 1 || K > SMOE_MAX_TOPK) return SMOE_ERR_ARG;
+    if (T > (int64_t)(INT32_MAX / 2) / K) return SMOE_ERR_ARG;  // checked before T * K can overflow
     const int64_t n = T * K;
-    if (n > INT32_MAX / 2) return SMOE_ERR_ARG;
     if (!aligned16(counts) || !aligned16(offsets) || !aligned16(tiles)) return SMOE_ERR_ARG;
     if (n > 0 && (!aligned16(ids) || !aligned16(src) || !aligned16(slot))) return SMOE_ERR_ARG;
     if (tiles_bytes < smoe_tiles_bytes(n, E)) return SMOE_ERR_ARG;

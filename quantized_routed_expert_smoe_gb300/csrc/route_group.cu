@@ -10,6 +10,7 @@
 
 #include <cfloat>
 #include <climits>
+#include <mutex>
 
 #include "smoe_device.cuh"
 #include "smoe_internal.h"
@@ -222,6 +223,27 @@ __global__ void __launch_bounds__(kGroupThreads) group_scatter_kernel(const int3
     }
 }
 
+// The scan and scatter kernels take more than 48 KB of dynamic shared memory at the largest E; the attribute that
+// allows it is set per device (it does not carry over to another device), once, and only marked done on success.
+cudaError_t group_attributes() {
+    static std::mutex mu;
+    static uint64_t done = 0;  // one bit per device
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done & (1ull << dev)) return cudaSuccess;
+    err = cudaFuncSetAttribute(group_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kMaxChunks * SMOE_MAX_EXPERTS * (int)sizeof(int32_t));
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(group_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)((size_t)SMOE_MAX_EXPERTS * 4 + (size_t)32 * SMOE_MAX_EXPERTS * 2));
+    if (err != cudaSuccess) return err;
+    done |= 1ull << dev;
+    return cudaSuccess;
+}
+
 int64_t group_chunk(int64_t n) {
     int64_t chunk = (n + kMaxChunks - 1) / kMaxChunks;
     chunk = (chunk + kGroupThreads - 1) / kGroupThreads * kGroupThreads;
@@ -256,23 +278,12 @@ cudaError_t launch_group(const int32_t* ids, int64_t n, int K, int E, int32_t* c
         group_hist_kernel<<<nchunks, kGroupThreads, E * sizeof(int32_t), s>>>(ids, n, E, chunk, hist, tiles);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }
-    static bool scan_attr_set = false;
-    if (!scan_attr_set) {
-        cudaFuncSetAttribute(group_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxChunks * SMOE_MAX_EXPERTS * (int)sizeof(int32_t));
-        scan_attr_set = true;
-    }
+    if ((err = group_attributes()) != cudaSuccess) return err;
     group_scan_kernel<<<1, kGroupThreads, (size_t)nchunks * E * sizeof(int32_t), s>>>(hist, nchunks, E, n, counts,
                                                                                        offsets, tiles);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (nchunks > 0) {
         const size_t smem = (size_t)E * sizeof(int32_t) + (size_t)32 * E * sizeof(uint16_t);
-        static bool attr_set = false;
-        if (!attr_set) {
-            cudaFuncSetAttribute(group_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)((size_t)SMOE_MAX_EXPERTS * 4 + (size_t)32 * SMOE_MAX_EXPERTS * 2));
-            attr_set = true;
-        }
         group_scatter_kernel<<<nchunks, kGroupThreads, smem, s>>>(ids, n, K, E, chunk, hist, src, slot);
         if ((err = cudaGetLastError()) != cudaSuccess) return err;
     }

@@ -80,8 +80,8 @@ smoe_status smoe_group(const int32_t* ids, int64_t T, int K, int E, int32_t* cou
                        int32_t* slot, int32_t* tiles, size_t tiles_bytes, void* work, size_t work_bytes,
                        void* stream) {
     if (T < 0 || E < 1 || E > SMOE_MAX_EXPERTS || K < 1 || K > SMOE_MAX_TOPK) return SMOE_ERR_ARG;
+    if (T > (int64_t)(INT32_MAX / 2) / K) return SMOE_ERR_ARG;  // checked before T * K can overflow
     const int64_t n = T * K;
-    if (n > INT32_MAX / 2) return SMOE_ERR_ARG;
     if (!aligned16(counts) || !aligned16(offsets) || !aligned16(tiles)) return SMOE_ERR_ARG;
     if (n > 0 && (!aligned16(ids) || !aligned16(src) || !aligned16(slot))) return SMOE_ERR_ARG;
     if (tiles_bytes < smoe_tiles_bytes(n, E)) return SMOE_ERR_ARG;

@@ -91,8 +91,18 @@ def test_host_side_rejections_need_no_gpu(lib):
     assert lib.smoe_router_topk(fake, fake, 4, 128, 272, 2, fake, fake, fake, null) == ARG
     assert lib.smoe_router_topk(fake, fake, 4, 128, 64, 17, fake, fake, fake, null) == ARG
     assert lib.smoe_router_topk(fake, fake, 0, 128, 64, 2, fake, fake, fake, null) == 0  # empty chunk
-    # group: tiles buffer too small
+    # group: tiles buffer too small; a T whose T * K would overflow is refused before the product is formed
     assert lib.smoe_group(fake, 8, 2, 4, fake, fake, fake, fake, fake, 16, fake, 1 << 20, null) == ARG
+    assert lib.smoe_group(fake, 1 << 62, 32, 4, fake, fake, fake, fake, fake, 1 << 40, fake, 1 << 40, null) == ARG
+    # the allocation-free grouping: the same host-side checks (tiles buffer too small, E above the maximum, a huge
+    # T, misaligned outputs) before it looks at the device or its scratch array
+    assert lib.smoe_group_noalloc(fake, 8, 2, 4, fake, fake, fake, fake, fake, 16, null) == ARG
+    assert lib.smoe_group_noalloc(fake, 8, 2, 2048, fake, fake, fake, fake, fake, 1 << 20, null) == ARG
+    assert lib.smoe_group_noalloc(fake, 1 << 62, 32, 4, fake, fake, fake, fake, fake, 1 << 40, null) == ARG
+    assert lib.smoe_group_noalloc(fake, 1 << 40, 4, 4, fake, fake, fake, fake, fake, 1 << 40, null) == ARG
+    assert lib.smoe_group_noalloc(fake, 8, 2, 4, odd, fake, fake, fake, fake, 1 << 20, null) == ARG
+    assert lib.smoe_group_noalloc(fake, 8, 2, 4, fake, fake, fake, odd, fake, 1 << 20, null) == ARG
+    assert lib.smoe_group_noalloc(fake, 8, 0, 4, fake, fake, fake, fake, fake, 1 << 20, null) == ARG
     # well-formed arguments on a machine without an sm_103 device: a clean error, never a fallback
     st = lib.smoe_route_topk(fake, 4, 16, 2, fake, fake, null)
     if not _has_gpu():

@@ -10,7 +10,8 @@ Bars (the library's contract):
     straddle a rounding boundary (at most 1e-4 of the codes; each such code differs by 1 and sits within 1e-3 of a
     .5 tie, each such scale sits within 1e-5 of an fp16 rounding midpoint);
   * the block's output, per token row: max |y_gpu - y_oracle| <= 2e-3 * RMS(y_oracle row).
-Full-size chunks are compared on every routing / grouping / q8 value and on sampled rows for the products.
+Full-size chunks are compared on every routing / grouping / q8 value and on every output row of the block; the
+products alone on the rows of 40+ experts spread over the routing's count order.
 """
 import numpy as np
 import pytest
@@ -19,7 +20,8 @@ import scipy.special
 import oracle
 from quantized_routed_expert_smoe_gb300 import synth
 
-from helpers import deq_a, deq_w, i16, packed_q2, to_operand
+from helpers import (check_h_decisions, check_tile_list, deq_a, deq_w, i16, packed_q2, tie_correction,
+                     tile_list, to_operand)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -117,9 +119,13 @@ def gpu_group(B, ids, E):
                 tiles=t[4:4 + 4 * nt].reshape(nt, 4), header=t[:4], tiles_raw=t, src_full=host(src))
 
 
-def assert_group_equal(g, go):
-    for k in ("counts", "offsets", "src", "slot", "tiles"):
+def assert_group_equal(B, g, go):
+    """The grouping tables bit-exact with the oracle's; the library's tile list (its own scheduling structure, which
+    the oracle does not define) valid over them."""
+    for k in ("counts", "offsets", "src", "slot"):
         assert np.array_equal(g[k], go[k]), k
+    n = int(go["offsets"][-1])
+    check_tile_list(g["tiles"], go["offsets"], B.TILE_ROWS, B.max_tiles(n, len(go["counts"])))
 
 
 @pytest.mark.parametrize("name", ALL)
@@ -129,23 +135,23 @@ def test_group_bit_exact(B, name):
     ids, _ = oracle.route(inp["logits"], cfg.K)
     g = gpu_group(B, ids, cfg.E)
     assert g["header"][1] == 0 and g["header"][2] == ids.size
-    assert_group_equal(g, oracle.group(ids, cfg.E))
+    assert_group_equal(B, g, oracle.group(ids, cfg.E))
 
 
 def test_group_edge_cases(B):
     # one expert takes every pair: several tiles, one ragged
     ids = np.zeros((1000, 1), np.int32)
     ids[::7] = 3
-    assert_group_equal(gpu_group(B, ids, 4), oracle.group(ids, 4))
+    assert_group_equal(B, gpu_group(B, ids, 4), oracle.group(ids, 4))
     # a long chunk over few experts (several scatter rounds per chunk, many chunks)
     rng = np.random.default_rng(3)
     ids = rng.integers(0, 5, size=(70001, 3)).astype(np.int32)
-    assert_group_equal(gpu_group(B, ids, 5), oracle.group(ids, 5))
+    assert_group_equal(B, gpu_group(B, ids, 5), oracle.group(ids, 5))
     ids = rng.integers(0, 1024, size=(3001, 7)).astype(np.int32)
-    assert_group_equal(gpu_group(B, ids, 1024), oracle.group(ids, 1024))
+    assert_group_equal(B, gpu_group(B, ids, 1024), oracle.group(ids, 1024))
     # a single pair
     ids = np.array([[2]], np.int32)
-    assert_group_equal(gpu_group(B, ids, 4), oracle.group(ids, 4))
+    assert_group_equal(B, gpu_group(B, ids, 4), oracle.group(ids, 4))
     # an id out of range is reported in the header, never faults
     ids = np.array([[0, 1], [9, 2]], np.int32)
     g = gpu_group(B, ids, 4)
@@ -229,10 +235,12 @@ def test_gather_q8_operand_form(B):
 
 # ------------------------------------------------------------------------------------------------ expert products
 def _tiles_dev(B, g, n, E):
+    """A tile list over the oracle's grouping (test input): near-equal tiles of at most the library's tile rows."""
+    tl = tile_list(g["offsets"], B.TILE_ROWS)
     raw = np.zeros(B.tiles_bytes(n, E) // 4, np.int32)
-    nt = g["tiles"].shape[0]
+    nt = tl.shape[0]
     raw[0], raw[2] = nt, n
-    raw[4:4 + 4 * nt] = g["tiles"].ravel()
+    raw[4:4 + 4 * nt] = tl.ravel()
     return dev(raw)
 
 
@@ -374,10 +382,21 @@ def test_gateup_parity(B, name):
     gu = gpu_gateup(B, xc, xs, g, inp["wgu_c"], inp["wgu_s"], cfg.n, cfg.E)
     if name == "tiny":
         experts = range(cfg.E)
-    else:  # the busiest expert (several tiles when skewed), the quietest routed one, and two in between
+    else:
+        # 40 experts spread over the count order -- the busiest (several tiles when skewed), the quietest routed
+        # one and the ranks between -- plus every tile-count class (1, 2, ... tiles) and each row count modulo 16
+        # (the MMA pads N to a multiple of 16) that the chunk has
         order = np.argsort(g["counts"], kind="stable")
         routed = order[g["counts"][order] > 0]
-        experts = sorted({int(routed[-1]), int(routed[0]), int(routed[len(routed) // 2]), 0})
+        pick = {int(routed[i]) for i in np.linspace(0, len(routed) - 1, 40).round().astype(int)}
+        for key in (lambda c: -(-c // B.TILE_ROWS), lambda c: c % 16):
+            seen = set()
+            for e in routed[::-1]:
+                k = key(int(g["counts"][e]))
+                if k not in seen:
+                    seen.add(k)
+                    pick.add(int(e))
+        experts = sorted(pick)
     rows, want, mag = gateup_reference(xc, xs, g, inp["wgu_c"], inp["wgu_s"], cfg.H, cfg.F, experts)
     check_products(rows_of(gu, rows), want, mag, f"gate/up {name}")
     assert bool(torch.isfinite(gu).all())
@@ -498,19 +517,27 @@ def test_block_parity(B, name):
     assert np.array_equal(host(blk.src)[:cfg.n], go["src"]) and np.array_equal(host(blk.slot)[:cfg.n], go["slot"])
     xc_o, xs_o = oracle.quantize_q8(inp["x"])
     assert np.array_equal(host(blk.xc), xc_o) and np.array_equal(host(blk.xs).view(np.uint16), xs_o)
-    # the output, row by row
-    if name == "tiny":
-        toks = np.arange(cfg.T)
-        y_o = oracle.layer(inp)
-    else:
-        rng = np.random.default_rng(cfg.seed)
-        toks = np.unique(np.concatenate([[0, cfg.T - 1], rng.choice(cfg.T, 30, replace=False)]))
-        y_o, ids_t, _ = oracle.layer_tokens(inp, toks)
-        assert np.array_equal(ids_t, ids_o[toks])
-    y_s = y[toks] if name != "tiny" else y
+    # the output, every row of the chunk (the oracle one token at a time: ~3,000 pairs/s on 16 host threads, so
+    # t8192 takes ~30 s and t32768 ~2 min).  H codes are decided by floating point: where the oracle's fp32 h lies
+    # within a few ulps of a rounding boundary the GPU's fp32 GU (accumulated in another order) can land on the other
+    # side, and both codes are valid.  So the GPU's H decisions are checked to differ from the oracle's only at such
+    # near ties, what those decisions add to the output is accounted exactly (a single code can move a small-RMS row
+    # by more than the bar), and then every row must be within the bar.
+    y_o, ids_t, w_t, h_o, hc_o, hs_o = oracle.layer_tokens_h(inp, np.arange(cfg.T))
+    assert np.array_equal(ids_t, ids_o)
+    rows = host(blk.slot)[:cfg.n].reshape(cfg.T, cfg.K)
+    hc_g = host(blk.hc)[rows]
+    hs_g = host(blk.hs).view(np.uint16)[rows]
+    sflip, cflip = check_h_decisions(hc_g, hs_g, h_o, hc_o, hs_o)
+    corr = tie_correction(hc_g, hs_g, hc_o, hs_o, ids_o, w_t, inp["wd_c"], inp["wd_s"])
     rms = np.sqrt((y_o ** 2).mean(axis=1))
-    err = np.abs(y_s - y_o).max(axis=1)
-    assert np.all(err <= 2e-3 * rms), f"worst err/rms {float((err / rms).max()):.3e}"
+    raw = np.abs(y - y_o).max(axis=1) / rms
+    err = np.abs(y - y_o - corr).max(axis=1) / rms
+    worst = int(np.argmax(err))
+    print(f"block {name}: {int(sflip.sum())} H scales and {int(cflip.sum())} H codes decided at near ties; every row "
+          f"within {float(err[worst]):.3e} * RMS of the oracle with those decisions (worst token {worst}); without "
+          f"them worst {float(raw.max()):.3e} (token {int(np.argmax(raw))}), rows over 2e-3 {int((raw > 2e-3).sum())}")
+    assert np.all(err <= 2e-3), f"worst err/rms {float(err.max()):.3e} at token {worst}"
     assert np.isfinite(y).all()
     del blk
     torch.cuda.empty_cache()

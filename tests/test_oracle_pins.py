@@ -101,20 +101,11 @@ def _check_group(ids, E, g):
     slot = np.empty(n, np.int32)
     slot[order] = np.arange(n)
     assert np.array_equal(g["slot"], slot)
-    tiles = g["tiles"]
-    covered = np.zeros(n, np.int32)
+    # every row of expert e holds a pair routed to e, in ascending pair order
     for e in range(E):
-        te = tiles[tiles[:, 0] == e]
-        c = int(g["counts"][e])
-        assert len(te) == (c + oracle.TILE_ROWS - 1) // oracle.TILE_ROWS
-        if c == 0:
-            continue
-        assert te[0, 1] == g["offsets"][e] and np.all(te[1:, 1] == te[:-1, 1] + te[:-1, 2])
-        assert te[:, 2].sum() == c and te[:, 2].max() <= oracle.TILE_ROWS and te[:, 2].max() - te[:, 2].min() <= 1
-        for r0, rows in te[:, 1:3]:
-            covered[r0:r0 + rows] += 1
-    assert np.all(covered == 1)
-    assert np.all(np.diff(tiles[:, 0]) >= 0)
+        r0, r1 = int(g["offsets"][e]), int(g["offsets"][e + 1])
+        pairs = order[r0:r1]
+        assert np.all(flat[pairs] == e) and np.all(np.diff(pairs) > 0)
 
 
 @pytest.mark.parametrize("cfg", ["tiny", "t1024", "skew8192"])
@@ -133,7 +124,9 @@ def test_group_edge_cases():
     g = oracle.group(ids, 8)
     _check_group(ids, 8, g)
     assert g["counts"].tolist() == [299, 0, 0, 300, 0, 1, 0, 0]
-    assert g["tiles"][:, 2].tolist() == [149, 150, 150, 150, 1]
+    assert g["offsets"].tolist() == [0, 299, 299, 299, 599, 599, 600, 600, 600]
+    # the pair of token 7 routed to expert 5 is the only row of expert 5, and its k is 0
+    assert g["src"][599] == 7 and g["slot"][14] == 599
     with pytest.raises(ValueError):
         oracle.group(np.array([[0, 8]], np.int32), 8)
     with pytest.raises(ValueError):

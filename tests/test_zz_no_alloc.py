@@ -49,3 +49,29 @@ def test_noalloc_group_matches_group_on_two_calls_in_a_row():
         got = _tables(binding, "noalloc", ids, E)
         for w, g in zip(want, got):
             assert np.array_equal(w, g)
+
+
+def test_noalloc_group_empty_chunk_and_bad_ids():
+    """An empty chunk (T = 0: no pairs, no chunks of the counting pass) gives an empty tile list and all-zero
+    offsets, as smoe_group does; a routed id outside [0, E) is reported in the tile-list header exactly as
+    smoe_group reports it, and the call after it (a good routing) is unaffected."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_routed_expert_smoe_gb300 import build, binding
+    build.build()
+    binding.load_library()
+    binding.device_check()
+    empty = np.zeros((0, 4), np.int32)
+    for fn in ("alloc", "noalloc"):
+        counts, offsets, _, _, tiles = _tables(binding, fn, empty, 8)
+        assert np.all(counts == 0) and np.all(offsets == 0)
+        assert tiles[0] == 0 and tiles[1] == 0 and tiles[2] == 0
+    bad = np.array([[0, 1], [9, 2], [3, -1]], np.int32)
+    want = _tables(binding, "alloc", bad, 4)
+    got = _tables(binding, "noalloc", bad, 4)
+    assert want[4][1] == 4 and got[4][1] == 4  # SMOE_ERR_RANGE in header[1]
+    for w, g in zip(want, got):
+        assert np.array_equal(w, g)
+    good = np.random.default_rng(9).integers(0, 64, size=(500, 6)).astype(np.int32)
+    for w, g in zip(_tables(binding, "alloc", good, 64), _tables(binding, "noalloc", good, 64)):
+        assert np.array_equal(w, g)
