@@ -182,6 +182,40 @@ smoe_status smoe_experts_gateup(const uint16_t* xop, int32_t* tiles, int64_t n, 
 smoe_status smoe_experts_gateup_swiglu(const uint16_t* xop, int32_t* tiles, int64_t n, int E, const uint8_t* wgs, int H,
                                        int F, int8_t* hc, uint16_t* hs, uint16_t* hop, void* stream);
 
+/* One expert's 2-bit weight matrix in the row-major Q2 form (page "Strata compare v0.1.35...v0.1.37", moe_fused.hpp
+ * experts(): the batch carries one weight blob pointer per expert): codes uint8 [rows][cols/4] and scales fp16 bits
+ * [rows][cols/32], each pointer 16-byte aligned. */
+typedef struct {
+    const uint8_t* codes;
+    const uint16_t* scales;
+} smoe_q2w;
+
+/* Bytes of the scratch of smoe_experts_gateup_q8 / smoe_experts_down_q8 for n routed rows (one size serves both). */
+size_t smoe_experts_q8_work_bytes(int64_t n, int E, int H, int F);
+
+/* Step 4 in the form of moe_fused.hpp experts(batch, ..., Xq, src, ...): the grouped gate/up product straight from the
+ * per-token q8 activations and the routed rows' token indices, with the weights given per expert.
+ *   xc, xs   int8 [in_rows][H] and fp16 [in_rows][H/32], from smoe_quantize_q8.
+ *   src      int32 [n], from smoe_group: routed row r reads token src[r] (entries outside [0, in_rows) read zeros).
+ *   tiles    from smoe_group (header[3] receives SMOE_ERR_TIMEOUT, or SMOE_ERR_ARG when a descriptor is null or
+ *            misaligned: that expert's weights are then taken as zero).
+ *   w_gu     DEVICE array of E descriptors, expert e's gate/up matrix [2F][H] (rows [0, F) gate, [F, 2F) up).
+ *   work     caller scratch of smoe_experts_q8_work_bytes(n, E, H, F) bytes: the call lays the routed rows out in the
+ *            operand form and packs the weights there, then runs smoe_experts_gateup's product.  A caller that calls
+ *            repeatedly with the same weights saves the packing by calling smoe_pack_q2 once and smoe_experts_gateup.
+ *   gu       fp32 [n][2F] out, exactly as smoe_experts_gateup computes it.   H % 128 == 0, F % 64 == 0. */
+smoe_status smoe_experts_gateup_q8(const int8_t* xc, const uint16_t* xs, int64_t in_rows, const int32_t* src,
+                                   int32_t* tiles, int64_t n, int E, const smoe_q2w* w_gu, int H, int F, void* work,
+                                   size_t work_bytes, float* gu, void* stream);
+
+/* Step 6 in the same form: the grouped down product from planar q8 H (routed-row order) and per-expert weights.
+ *   hc, hs   int8 [n][F] and fp16 [n][F/32], from smoe_swiglu_requant.
+ *   w_d      DEVICE array of E descriptors, expert e's down matrix [H][F].
+ *   tiles, work as smoe_experts_gateup_q8;  dm fp32 [n][H] out, exactly as smoe_experts_down computes it. */
+smoe_status smoe_experts_down_q8(const int8_t* hc, const uint16_t* hs, int32_t* tiles, int64_t n, int E,
+                                 const smoe_q2w* w_d, int H, int F, void* work, size_t work_bytes, float* dm,
+                                 void* stream);
+
 /* Step 5 -- SwiGLU and requantisation.  Page "src/prefill/prefill.cpp": mmq::swiglu(GU, H, rows, ...) then the
  * int8 rounding of H; moe_fused.hpp: "SwiGLU, H as int8".
  *   gu fp32 [n][2F] -> h_j = silu(gu[r][j]) * gu[r][F + j] (fp32; silu(g) = g / (1 + exp(-g))), then the q8 rule:

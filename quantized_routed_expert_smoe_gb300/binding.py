@@ -60,6 +60,13 @@ _SIGS = {
     "smoe_experts_gateup_swiglu": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                     ctypes.c_void_p], ctypes.c_int),
+    "smoe_experts_q8_work_bytes": ([ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
+    "smoe_experts_gateup_q8": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_experts_down_q8": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                              ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                              ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_swiglu_requant": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                              ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_experts_down": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
@@ -220,6 +227,40 @@ def smoe_experts_gateup_swiglu(xop, tiles, n, E, wgs, H, F, hc, hs, hop, stream=
     _check("smoe_experts_gateup_swiglu", load_library().smoe_experts_gateup_swiglu(
         _dev(xop, torch.float16, "xop"), _dev(tiles, torch.int32, "tiles"), n, E, _dev(wgs, torch.uint8, "wgs"), H, F,
         _dev(hc, torch.int8, "hc"), _dev(hs, torch.int16, "hs"), _dev(hop, torch.float16, "hop"), _stream(stream)))
+
+
+def experts_q8_work_bytes(n: int, E: int, H: int, F: int) -> int:
+    return int(load_library().smoe_experts_q8_work_bytes(n, E, H, F))
+
+
+def q2_descriptors(experts):
+    """A device array of smoe_q2w descriptors (two 64-bit pointers each) for a list of (codes, scales) CUDA tensors,
+    one per expert: codes uint8 [rows][cols/4], scales int16 bits [rows][cols/32].  The tensors must stay alive while
+    the descriptors are used."""
+    ptrs = []
+    for c, sc in experts:
+        _dev(c, torch.uint8, "codes")
+        _dev(sc, torch.int16, "scales")
+        ptrs += [c.data_ptr(), sc.data_ptr()]
+    dev = experts[0][0].device if experts else torch.device("cuda")
+    return torch.tensor(ptrs, dtype=torch.int64).to(dev)
+
+
+def smoe_experts_gateup_q8(xc, xs, src, tiles, n, E, w_gu, H, F, work, gu, stream=None):
+    """gate/up from per-token q8 activations (xc int8 [T][H], xs int16 bits [T][H/32]), src int32 [n] and a device
+    array of E weight descriptors (q2_descriptors); work: uint8 scratch of experts_q8_work_bytes(n, E, H, F)."""
+    _check("smoe_experts_gateup_q8", load_library().smoe_experts_gateup_q8(
+        _dev(xc, torch.int8, "xc"), _dev(xs, torch.int16, "xs"), xc.shape[0], _dev(src, torch.int32, "src"),
+        _dev(tiles, torch.int32, "tiles"), n, E, _dev(w_gu, torch.int64, "w_gu"), H, F, _dev(work, torch.uint8, "work"),
+        work.numel(), _dev(gu, torch.float32, "gu"), _stream(stream)))
+
+
+def smoe_experts_down_q8(hc, hs, tiles, n, E, w_d, H, F, work, dm, stream=None):
+    """down from planar q8 H (hc int8 [n][F], hs int16 bits [n][F/32]) and a device array of E weight descriptors."""
+    _check("smoe_experts_down_q8", load_library().smoe_experts_down_q8(
+        _dev(hc, torch.int8, "hc"), _dev(hs, torch.int16, "hs"), _dev(tiles, torch.int32, "tiles"), n, E,
+        _dev(w_d, torch.int64, "w_d"), H, F, _dev(work, torch.uint8, "work"), work.numel(),
+        _dev(dm, torch.float32, "dm"), _stream(stream)))
 
 
 def smoe_swiglu_requant(gu, hc, hs, hop=None, stream=None):

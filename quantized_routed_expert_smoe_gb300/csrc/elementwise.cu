@@ -55,6 +55,18 @@ __device__ __forceinline__ void split_pairs(uint4 qp, __half2 d2, uint4& hi, uin
     lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// round-half-away(x / d) for the q8 rule, where the quotient is the IEEE (correctly rounded) fp32 division, from a
+// multiply by the correctly rounded reciprocal inv = RN(1/d): g = RN(x * inv) is within |x/d| 2^-23 of x/d and
+// RN(x/d) within |x/d| 2^-24, so both round to the same integer unless a half-integer lies within |x/d| 2^-22 of g.
+// In the q8 rule |x/d| < 127.1 (d >= amax/127 (1 - 2^-11)), so that margin is below 2^-14: only values whose g lies
+// within 2^-14 of a half-integer (exact .5 ties included) take the IEEE division itself.
+__device__ __forceinline__ float q8_round(float x, float d, float inv) {
+    const float g = x * inv;
+    const float a = fabsf(g);
+    if (fabsf((a - truncf(a)) - 0.5f) <= 6.103515625e-05f) return roundf(__fdiv_rn(x, d));  // 2^-14
+    return roundf(g);
+}
+
 // q8 of the 8 values v held by this thread, its block being spread over 4 consecutive lanes; returns the 8 codes
 // packed little-endian and the block's fp16 scale bits.
 __device__ __forceinline__ uint2 q8_encode8(const float (&v)[8], uint16_t* scale_bits) {
@@ -66,12 +78,13 @@ __device__ __forceinline__ uint2 q8_encode8(const float (&v)[8], uint16_t* scale
     const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
     const float d = __half2float(dh);
     *scale_bits = __half_as_ushort(dh);
+    const float inv = d != 0.0f ? __frcp_rn(d) : 0.0f;
     uint32_t lo = 0, hi = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         int q = 0;
         if (d != 0.0f) {
-            float r = roundf(__fdiv_rn(v[i], d));
+            float r = q8_round(v[i], d, inv);
             r = fminf(fmaxf(r, -127.0f), 127.0f);
             q = (int)r;
         }
@@ -208,42 +221,57 @@ __global__ void __launch_bounds__(256) shared_gate_kernel(const float4* __restri
 // `half` > 0 packs a gate/up matrix for the fused SwiGLU product: tile mt holds outputs j in [64 mt, 64 mt + 64),
 // and its row 32 q + l is gate row 64 mt + 16 q + l (l < 16) or up row half + 64 mt + 16 q + l - 16 (l >= 16), so
 // that each 32-row warp of the product holds the gate and up rows of the same 16 outputs.
-__device__ __forceinline__ int64_t packed_source_row(int64_t e, int mt, int r, int rows, int half) {
-    if (half <= 0) return e * rows + (int64_t)mt * 128 + r;
+// the source row of packed row r of 128-row tile mt, within one expert's matrix
+__device__ __forceinline__ int packed_source_row(int mt, int r, int half) {
+    if (half <= 0) return mt * 128 + r;
     const int q = r >> 5, l = r & 31;
     const int j = 64 * mt + 16 * q + (l & 15);
-    return e * rows + (l < 16 ? j : half + j);
+    return l < 16 ? j : half + j;
 }
 
+// desc == nullptr: the E experts contiguous in codes / scales; else expert e's matrix at desc[e] (a block whose
+// descriptor is null or not 16-byte aligned is written as zeros and reported in status[0] as SMOE_ERR_ARG)
 __global__ void __launch_bounds__(160) pack_q2_kernel(const uint8_t* __restrict__ codes,
-                                                      const uint16_t* __restrict__ scales, int rows, int cols,
-                                                      int half, uint8_t* __restrict__ packed) {
+                                                      const uint16_t* __restrict__ scales,
+                                                      const smoe_q2w* __restrict__ desc, int rows, int cols,
+                                                      int half, uint8_t* __restrict__ packed, int32_t* status) {
     const int64_t blk = blockIdx.x;  // ((e * rows/128 + mt) * cols/64 + kt)
     const int nkt = cols / 64, nmt = rows / 128;
     const int kt = (int)(blk % nkt);
     const int64_t emt = blk / nkt;  // e * nmt + mt
     const int64_t e = emt / nmt;
     const int mt = (int)(emt - e * nmt);
+    const uint8_t* ce = codes + e * rows * (int64_t)(cols / 4);
+    const uint16_t* se = scales + e * rows * (int64_t)(cols / 32);
+    if (desc != nullptr) {
+        ce = desc[e].codes;
+        se = desc[e].scales;
+    }
     uint8_t* out = packed + blk * 2560;
     const int t = threadIdx.x;
+    if (ce == nullptr || se == nullptr || (((uintptr_t)ce | (uintptr_t)se) & 15u) != 0) {
+        if (t < 160) *reinterpret_cast<uint4*>(out + t * 16) = make_uint4(0u, 0u, 0u, 0u);
+        if (t == 0 && status != nullptr) status[0] = SMOE_ERR_ARG;
+        return;
+    }
     if (t < 128) {
-        const int64_t sr = packed_source_row(e, mt, t, rows, half);
-        const uint4 v = *reinterpret_cast<const uint4*>(codes + sr * (cols / 4) + kt * 16);
+        const int64_t sr = packed_source_row(mt, t, half);
+        const uint4 v = *reinterpret_cast<const uint4*>(ce + sr * (cols / 4) + kt * 16);
         *reinterpret_cast<uint4*>(out + t * 16) = v;
     } else {
         const int r = (t - 128) * 4;  // four rows' scale pairs per piece
         uint32_t v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int64_t sr = packed_source_row(e, mt, r + j, rows, half);
-            v[j] = *reinterpret_cast<const uint32_t*>(scales + sr * (cols / 32) + kt * 2);
+            const int64_t sr = packed_source_row(mt, r + j, half);
+            v[j] = *reinterpret_cast<const uint32_t*>(se + sr * (cols / 32) + kt * 2);
         }
         *reinterpret_cast<uint4*>(out + 2048 + r * 4) = make_uint4(v[0], v[1], v[2], v[3]);
     }
 }
 
-// Routed rows of the q8 activations in operand form: out row r = codes row src[r] scaled by its scales and split
-// into the hi and lo planes, in operand order.  One warp per output row.  Lane l makes the output words (8 fp16
+// Routed rows of the q8 activations in operand form: out row r = codes row src[r] (row r itself when src is null)
+// scaled by its scales and split into the hi and lo planes, in operand order.  One warp per output row.  Lane l makes the output words (8 fp16
 // each) l, l + 32, ... of both planes, so every store instruction writes 512 contiguous bytes: word w is half w % 2
 // of group w / 2, i.e. values 4h..4h+3 and 8+4h..8+4h+3 of the group (h = w % 2).  An src entry outside
 // [0, in_rows) gives zero rows.
@@ -257,7 +285,7 @@ __global__ void __launch_bounds__(256) gather_q8_kernel(const uint32_t* __restri
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int64_t plane = n * words;  // uint4 words per plane
     for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n; r += warps) {
-        const int32_t t = __ldg(src + r);
+        const int64_t t = src != nullptr ? (int64_t)__ldg(src + r) : r;  // no src: row r itself
         uint4* o = out + r * words;
         if (t < 0 || t >= in_rows) {
             for (int w = lane; w < words; w += 32) {
@@ -323,11 +351,11 @@ cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc,
     return cudaGetLastError();
 }
 
-cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, int half,
-                           uint8_t* packed, cudaStream_t s) {
+cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, const smoe_q2w* desc, int E, int rows,
+                           int cols, int half, uint8_t* packed, int32_t* status, cudaStream_t s) {
     const int64_t blocks = (int64_t)E * (rows / 128) * (cols / 64);
     if (blocks == 0) return cudaSuccess;
-    pack_q2_kernel<<<(unsigned)blocks, 160, 0, s>>>(codes, scales, rows, cols, half, packed);
+    pack_q2_kernel<<<(unsigned)blocks, 160, 0, s>>>(codes, scales, desc, rows, cols, half, packed, status);
     return cudaGetLastError();
 }
 

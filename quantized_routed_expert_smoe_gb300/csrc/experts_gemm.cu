@@ -5,17 +5,18 @@
 // of its routed rows from the per-token int8 activations against its 2-bit weights, then down into one fp32 row per
 // routed pair.  Per output:  sum_b dB[b] * (dW[b] * sum_{i in b} (qW - 2) * qB)  over the 32-value blocks b of K.
 //
-// Arithmetic.  The int8 tensor rate of this part is far below its fp16 rate, so the contraction runs as
-// tcgen05.mma.kind::f16 on fp16 operands that carry the quantised values EXACTLY:
+// Arithmetic.  The 5th-generation tensor cores of this part have no int8 kind (ptxas rejects kind::i8 for
+// sm_103a), so the contraction runs as tcgen05.mma.kind::f16 on fp16 operands that carry the quantised values
+// EXACTLY:
 //   - the weight operand is d_w * (q_w - 2), q_w in {0..3}: d_w times {-2, -1, 0, 1}, exact in fp16;
 //   - the row operand d * q (at most 18 significant bits) comes as two fp16 parts, hi = fp16_rn(d q) and
 //     lo = d q - hi (exact), written by the routed-row gather (activations) and by SwiGLU (H).
 // Every product of a weight and a part is exact in fp32, and the K loop runs two MMAs per 16-wide K step (A x hi,
 // A x lo).  The tensor core's fp32 accumulation aligns its addends with truncation, which over a whole row of K
 // costs about 3e-6 of the result -- enough to flip requantised H codes -- so for gate/up (whose output is
-// requantised) each 64-wide K slice accumulates from zero into one of two tensor-memory buffers (a small partial,
-// so a small truncation error) and the promoter warps add each finished partial into fp32 registers with
-// round-to-nearest while the tensor core fills the other buffer.  The down product feeds the fp32 combine only,
+// requantised) each 128-wide piece of K (two slices) accumulates from zero into one of two tensor-memory buffers (a
+// small partial, so a small truncation error) and the promoter warps add each finished partial into fp32 registers
+// with round-to-nearest while the tensor core fills the other buffer.  The down product feeds the fp32 combine only,
 // where 4e-6 is far inside the output bound, so it accumulates the whole K in one buffer, read once at the end.
 //
 // Data movement, chosen to keep the CUDA-core work per slice small (shared-memory traffic and the converters'
@@ -27,10 +28,20 @@
 //
 // Tile: one CTA = one tile of the tile list (an expert and up to 192 of its routed rows, contiguous in routed-row
 // order; the MMA's N, a multiple of 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB:
-// weights are the M operand so that a small expert wastes little).  Five warpgroups, registers rebalanced with
-// setmaxnreg:
-//   warpgroup 0   warps 0 and 2, one lane each: the MMAs of alternate slices (four K16 steps x two parts a slice;
-//                 one thread's waits overlap the other's MMAs); warp 0 also allocates the tensor memory;
+// weights are the M operand so that a small expert wastes little).
+//
+// Two forms.  The CTA-pair form (any weight matrix with an even number of 128-row slices) runs the MMAs over a pair
+// of CTAs with tcgen05 cta_group::2: M = 256, each CTA decoding and accumulating its own 128 weight rows, and the
+// tile's B rows split between the two CTAs' shared memories (a tile of at most 96 rows: its hi rows in the even CTA
+// and its lo rows in the odd one, one MMA of 2N; a larger tile: N/2 rows of each part in each).  The tensor cores
+// of both SMs read both halves, so each SM takes in half the row bytes per MMA of the single-CTA form, its ring
+// slots are half as large and twice as many slices are in flight.  The even CTA issues the pair's MMAs: both CTAs'
+// converter warps and B arrivals meet on its `ready` barrier and both CTAs' promoter warps on its `pempty`; its
+// commits release the slots in every CTA of the cluster and the partials in both.  The single-CTA form (an odd
+// number of 128-row slices) issues its own MMAs.  Five warpgroups, registers rebalanced with setmaxnreg:
+//   warpgroup 0   warps 0 and 2, one lane each: the MMAs of alternate slices -- of alternate slice pairs for
+//                 gate/up (four K16 steps x two parts a slice; one thread's waits overlap the other's MMAs); warp 0
+//                 also allocates the tensor memory; warp 3 (two pairs): relays its CTA's landed B rows to the leader;
 //                 warp 1: the producer -- per 64-wide K slice, one TMA tile load of the tile's rows of each part
 //                 (128-byte swizzle; in a cluster, multicast by one CTA to all) and one bulk copy of the packed
 //                 weight block into a ring slot;
@@ -42,17 +53,18 @@
 //                 tensor memory.
 // Tensor memory (512 columns): 4 A buffers of 32 columns, then 2 partial buffers of 192 columns (a tile's partial
 // takes N of them, or 2N for a tile of at most 96 rows, which stacks its hi and lo rows into one MMA; gate/up
-// promotes every slice's partial, down one partial per MMA thread at the item's end).  A tile has at most 192 rows:
-// a promoter thread then holds its 64 accumulators and two 32-column loads.
+// promotes a partial every two slices, down one partial per MMA thread at the item's end).  A tile has at most 192
+// rows: a promoter thread then holds its 64 accumulators and two 32-column loads.
 //
 // Synchronisation: a satisfied mbarrier wait still costs a round trip of a few hundred cycles, and the ring's slots
 // circulate through a chain of latencies (slot released -> copies issued -> landed -> A decoded -> MMAs -> released),
 // so each role waits as little as it can and nothing waits on what it does not need.  A slot's packed weights land
-// on their own barrier, so the converters decode while the B tiles are still in flight; they wait on nothing else
-// -- the ring has as many slots as A buffers, so a slot's new contents also mean that the MMAs of the slice that
-// last used its A buffer have completed -- and test the next slot's barrier while a slice's stores complete.  The
-// MMA thread waits once per slice, in one round trip, on "A decoded", "B tiles landed" and, for a slice that starts
-// a partial in a buffer used before, "the promoters have taken that buffer's previous partial".
+// on their own barrier, so the converters decode while the B tiles are still in flight; in the single form they
+// wait on nothing else -- its ring has as many slots as A buffers, so a slot's new contents also mean that the MMAs
+// of the slice that last used its A buffer have completed (the pair form's ring is twice as deep, so there they also
+// wait for that slice's release) -- and test the next slot's barrier while a slice's stores complete.  The MMA
+// thread waits once per slice, in one round trip, on "A decoded", "B tiles landed" and, for a slice that starts a
+// partial in a buffer used before, "the promoters have taken that buffer's previous partial".
 //
 // K order: within each group of 16 K values, operand position 2m holds value m and position 2m+1 value m+8
 // (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so the contraction is unchanged
@@ -60,6 +72,8 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "smoe_device.cuh"
 #include "smoe_internal.h"
@@ -109,6 +123,17 @@ __host__ __device__ constexpr int slot_bytes(int N) { return (2 * N * 128 + kWBl
 static_assert(kRingBytes / slot_bytes(kMaxBN) >= 3, "the ring must hold three slices of a full tile");
 static_assert(kMaxStackN % kRowBox == 0 && kMaxBN % kRowBox == 0 && kMaxBN <= 256, "box heights");
 
+// CTA-pair form (tcgen05 cta_group::2): the two CTAs of a pair hold 128 weight rows each (M = 256) and split the
+// tile's B rows between their shared memories, so each SM receives half of the row bytes per MMA of the single form.
+// A slot holds at most kPairRows rows of each part (a stacked tile: all N rows of ONE part -- hi in the leader, lo in
+// the peer; a larger tile: N/2 rows of both parts), then the packed weights at a fixed offset.
+constexpr int kPairRows = kMaxBN / 2;          // 96
+constexpr int kPairBox = 8;                    // box-height step of the pair maps (N/2 is a multiple of 8)
+constexpr int kPairWOfs = 2 * kPairRows * 128;  // the packed weight block within a pair slot
+constexpr int kPairSlot = (kPairWOfs + kWBlock + 1023) & ~1023;
+static_assert(kPairRows / kPairBox == kNumMaps && kMaxStackN <= kPairRows, "pair boxes");
+static_assert(kRingBytes / kPairSlot >= 4, "the pair ring must hold four slices");
+
 // bulk copy (no tensor map) of `bytes` (a multiple of 16) into shared memory, completing on `bar`
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -122,6 +147,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
         ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
+}
+
+// TMA: a 2D tile into this CTA's shared memory whose completion is counted on the barrier at shared::cluster address
+// `bar`, which may be the other CTA's of this CTA's pair (the pair's even CTA gathers both CTAs' bytes)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
 
 // TMA 2D tile multicast to the CTAs of `mask` in the cluster: same shared-memory offset and mbarrier in each
@@ -149,6 +183,71 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 // every thread of every CTA of the cluster
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// --- barriers that receive arrivals from the other CTA of a pair.  What crosses between the two CTAs is tensor
+// memory (ordered by tcgen05.wait::st/ld and the tcgen05 thread-sync fences around the barrier) and shared memory
+// written by TMA (the async proxy, completed through the barrier's byte count), never generic stores that the other
+// CTA loads, so the arrivals and waits keep the default CTA-scope release / acquire: a cluster-scope one is a full
+// memory fence on every arrival and every poll, which stalled the pipeline's threads for most of their time.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) { return mbar_try_wait(bar, parity); }
+// wait (bounded, as mbar_wait) for the phases of two barriers
+__device__ __forceinline__ bool mbar_wait2_cl(uint64_t* bar0, uint32_t parity0, uint64_t* bar1, uint32_t parity1,
+                                              volatile int* abort) {
+    const uint32_t a0 = smem_u32(bar0), a1 = smem_u32(bar1);
+    bool d0 = mbar_try_wait_cl(a0, parity0), d1 = mbar_try_wait_cl(a1, parity1);
+    if (d0 && d1) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (!d0) d0 = mbar_try_wait_cl(a0, parity0);
+        if (!d1) d1 = mbar_try_wait_cl(a1, parity1);
+        if (d0 && d1) return true;
+        if (abort != nullptr && *abort) return false;
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    return mbar_wait2_cl(bar, parity, bar, parity, abort);
+}
+// the shared::cluster address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+// one arrival on the barrier at shared::cluster address `addr` (of this CTA or another CTA of the cluster)
+__device__ __forceinline__ void mbar_arrive_cl(uint32_t addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]^T over a CTA pair: M = 256 (A rows 0-127 and D in this CTA's tensor memory,
+// rows 128-255 in the peer's at the same address), B's first N/2 rows from this CTA's shared memory and the rest from
+// the peer's at the same address.  Issued by one thread of the pair's even CTA.
+__device__ __forceinline__ void mma_f16_ta_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive once on `bar` in every CTA of `mask` when the pair MMAs issued so far by this thread have completed
+__device__ __forceinline__ void mma_commit_pair_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+// tensor-memory allocation of a CTA pair: one warp of EACH CTA of the pair executes these (collectively)
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
 // named barrier of `count` threads (whole warps)
@@ -233,9 +332,10 @@ struct Item {
     int e, row0, rows, N, m0;
     bool stacked;  // N <= kMaxStackN: hi and lo rows in one MMA of 2N columns
     int ncols;     // partial columns
-    int lo_rows;   // slot row where the lo part starts (N stacked, kMaxBN otherwise)
+    int lo_rows;   // slot row where the lo part starts (N stacked, kMaxBN otherwise; pair form: kPairRows)
     int map;       // tensor maps of its parts (one box per part)
 };
+template <bool kPair>
 __device__ __forceinline__ bool load_item(const int32_t* tiles, int item, int mgroups, int C, uint32_t crank,
                                           const ExpertsGemmArgs& p, Item& t) {
     const int ti = item / mgroups, mg = item - ti * mgroups;
@@ -251,20 +351,34 @@ __device__ __forceinline__ bool load_item(const int32_t* tiles, int item, int mg
     t.m0 = (mg * C + (int)crank) * kBM;
     t.stacked = t.N <= kMaxStackN;
     t.ncols = t.stacked ? 2 * t.N : t.N;
-    t.lo_rows = t.stacked ? t.N : kMaxBN;
-    t.map = t.N / kRowBox - 1;
+    if (kPair) {
+        // each CTA's box: all N rows of its one part (stacked) or N/2 rows of each part
+        t.lo_rows = kPairRows;
+        t.map = (t.stacked ? t.N : t.N / 2) / kPairBox - 1;
+    } else {
+        t.lo_rows = t.stacked ? t.N : kMaxBN;
+        t.map = t.N / kRowBox - 1;
+    }
     return true;
 }
 
+// kPair: the CTA-pair form (cluster of C = 2 or 4 CTAs = C/2 pairs).  Ranks 2q and 2q + 1 form pair q; the even CTA
+// (the leader) issues the pair's MMAs.  Per slice the leader waits on its `ready` barrier, which both CTAs' converter
+// warps (A decoded into their tensor memory) and B relays (their B rows landed) arrive on, and -- before a partial
+// buffer is reused -- on `pempty`, which both CTAs' promoter warps arrive on.  The leader's commits signal slot
+// releases in every CTA of the cluster and partials and the final drain in both CTAs of its pair.
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const ExpertsGemmArgs p,
                                                                    const __grid_constant__ GemmMaps maps) {
     int32_t* tiles = p.tiles;
     if (tiles[1] != 0) return;  // the grouping failed: nothing to do (the same answer in every CTA)
     const int n_tiles = tiles[0];
     const int nk = p.K / kBK;  // slices of an item
-    // two MMA threads take alternate slices (stream = global slice index mod 2).  Two-level: a partial per slice;
-    // else one partial per stream of an item (slices kt and kt + 2 ... of the same parity), summed by the promoters
-    const int pitem = p.two_level ? nk : min(2, nk);  // partials an item
+    // two MMA threads take alternate groups of G slices.  Two-level: a partial per pair of slices (G = 2; K is a
+    // multiple of 128 there); else one partial per thread of an item (G = 1: slices kt, kt + 2, ... of one parity),
+    // summed by the promoters
+    const int G = p.two_level ? 2 : 1;
+    const int pitem = p.two_level ? nk / 2 : min(2, nk);  // partials an item
 
     // persistent: cluster cid of NC takes items cid, cid + NC, ...; its CTAs take the C weight slices of an item
     const int C = p.cluster;
@@ -273,19 +387,26 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const int mgroups = p.a_rows / kBM / C;
     const int n_items = n_tiles * mgroups;
     const int cid = blockIdx.x / C, NC = gridDim.x / C;
+    // pair form: this CTA's position in its pair (0 = the leader) and the pair's two CTAs
+    const uint32_t ppos = crank & 1u, leader = crank & ~1u;
+    const uint16_t pmask = (uint16_t)(3u << leader);
 
     // fixed geometry for every item (tiles of up to kMaxBN rows): a ring of `depth` slots, na A buffers and nbuf
     // partial buffers of kMaxBN columns in tensor memory
-    constexpr int sbytes = slot_bytes(kMaxBN);
-    constexpr int depth = kRingBytes / sbytes < kMaxRing ? kRingBytes / sbytes : kMaxRing;
+    constexpr int sbytes = kPair ? kPairSlot : slot_bytes(kMaxBN);
     constexpr int na = ((int)kTmemCols - 2 * kMaxBN) / (int)kACols;
+    // the single form: as many ring slots as A buffers (its slots are large); the pair form: twice as many (its slots
+    // hold half the B rows), so that twice the slices are in flight against the ring's chain of latencies
+    constexpr int depth = kPair ? 2 * na : na;
     constexpr uint32_t part_base = (uint32_t)na * kACols;
     constexpr int nbuf = ((int)kTmemCols - (int)part_base) / kMaxBN;
     static_assert(na >= 2 && na <= kMaxA && nbuf >= 2 && nbuf <= kMaxBufs, "tensor-memory split");
-    // slice gs uses ring slot and A buffer gs mod depth.  Its copies can land only after the producer has seen the
-    // slot's previous slice (gs - depth) released by this CTA's MMA commit, which follows that slice's MMAs, the last
-    // readers of the A buffer: "weights landed" also means "A buffer free", so the converters wait for nothing else
-    static_assert(depth == na, "ring slots and A buffers advance together");
+    static_assert(depth <= kMaxRing && depth <= kMaxA && depth * sbytes <= kRingBytes, "ring");
+    // slice gs uses ring slot gs mod depth and A buffer gs mod na.  Single form (depth == na): its copies can land
+    // only after the producer has seen the slot's previous slice (gs - depth) released by the MMA commits, which
+    // follow that slice's MMAs, the last readers of the A buffer, so "weights landed" also means "A buffer free".
+    // Pair form (depth == 2 na): the converters also wait for the release of slice gs - na, the previous user of the
+    // A buffer, before they overwrite it
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -293,33 +414,46 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     uint64_t* sfull = reinterpret_cast<uint64_t*>(smem_raw + kSmemBytes - kBarBytes);  // slot r's B tiles [kMaxRing]
     uint64_t* wfull = sfull + kMaxRing;     // slot r's packed weight block landed [kMaxRing]
     uint64_t* sempty = wfull + kMaxRing;    // the MMAs and the converters are done with slot r [kMaxRing]
-    uint64_t* afull = sempty + kMaxRing;    // A buffer a decoded [kMaxA]
+    uint64_t* afull = sempty + kMaxRing;    // A buffer a decoded [kMaxA]; pair form (leader): slot a's A and B ready
     uint64_t* pfull = afull + kMaxA;        // partial in tensor-memory buffer b is complete [kMaxBufs]
     uint64_t* pempty = pfull + kMaxBufs;    // the promoters have added buffer b into their registers [kMaxBufs]
     uint64_t* accf = pempty + kMaxBufs;     // every MMA has completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* total_slot = const_cast<int*>(abort_flag + 1);  // slices this CTA ran (for the teardown)
     float* scratch = reinterpret_cast<float*>(smem_raw + kSmemBytes - kBarBytes - kScratchBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
+        // pair form: arrivals are per warp (converters, promoters) and come from both CTAs of the pair
+        const int n_pairs = C / 2;
         for (int r = 0; r < kMaxRing; ++r) {
             mbar_init(&sfull[r], 1);                 // the arrival that posts the B tiles' byte count
             mbar_init(&wfull[r], 1);                 // the arrival that posts the weight block's
-            mbar_init(&sempty[r], C + kConverters);  // the MMAs' commit of every CTA of the cluster, own converters
+            // the MMAs' commits (every CTA / every pair of the cluster), then the own converters
+            mbar_init(&sempty[r], kPair ? n_pairs + kConverters / 32 : C + kConverters);
         }
-        for (int a = 0; a < kMaxA; ++a) mbar_init(&afull[a], kConverters);
+        // pair form: both CTAs' converter warps, plus (two pairs) both CTAs' B relays; one pair counts its B bytes on
+        // the leader's sfull instead
+        for (int a = 0; a < kMaxA; ++a)
+            mbar_init(&afull[a], kPair ? 2 * (kConverters / 32 + (C == 4 ? 1 : 0)) : kConverters);
         for (int b = 0; b < kMaxBufs; ++b) {
             mbar_init(&pfull[b], 1);
-            mbar_init(&pempty[b], kPromoters);
+            mbar_init(&pempty[b], kPair ? 2 * (kPromoters / 32) : kPromoters);
         }
         mbar_init(accf, 2);  // one final commit of each MMA thread
         *abort_flag = 0;
+        *total_slot = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(tmem_slot, kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(tmem_slot, kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -328,35 +462,46 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const uint32_t tmem = *tmem_slot;
     const uint32_t ring_s = smem_u32(ring);
     bool ok = true;
-    int total = 0;  // slices this CTA ran (warp 0 lane 0 uses it at the end)
 
     if (warp < 4) {
         setmaxnreg_dec<kRegsWg0>();
-        if ((warp == 0 || warp == 2) && lane == 0) {
+        if ((warp == 0 || warp == 2) && lane == 0 && (!kPair || ppos == 0)) {
             // ------------------------------------------------------------------ MMA issue (two threads)
-            // stream st issues the global slices gs = st, st + 2, ...: A buffer gs mod na, the slot's hi and lo tiles,
-            // the slice's partial buffer; the other thread's waits overlap this one's MMAs.  Positions advance by
+            // stream st issues the global slices of groups st, st + 2, ... (slice gs: ring slot gs mod depth, A buffer
+            // gs mod na -- both powers of two --, the slot's hi and lo tiles, the slice's partial buffer); the other
+            // thread's waits overlap this one's MMAs.  The item's first slice and its partial index advance by
             // counting (a division by a runtime value costs tens of cycles on this thread's critical path).
             const int st = warp >> 1;
-            int gs = st, base = 0, seq = 0;  // this thread's next global slice; the item's first; items done
-            int r = st % depth, ab = st % na;
-            uint32_t aph = (uint32_t)(st / na) & 1u;
+            int gs = st * G, base = 0, seq = 0;  // this thread's next global slice; the item's first; items done
             Item t;
             for (int item = cid; item < n_items && ok; item += NC) {
-                if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
-                const uint32_t idesc = idesc_f16_f32(kBM, t.ncols);
-                for (; gs < base + nk && ok; gs += 2) {
+                if (!load_item<kPair>(tiles, item, mgroups, C, crank, p, t)) continue;
+                const uint32_t idesc = idesc_f16_f32(kPair ? 2 * kBM : kBM, t.ncols);
+                for (; gs < base + nk && ok; gs += (G == 1 || (gs & 1)) ? G + 1 : 1) {
                     const int kt = gs - base;
-                    // the slice's partial: a partial per slice (two-level), else the item's partial kt mod 2
-                    const int gp = seq * pitem + (p.two_level ? kt : (pitem == 2 ? (kt & 1) : 0));
+                    const int r = gs % depth, ab = gs % na;
+                    const uint32_t aph = (uint32_t)(gs / depth) & 1u;  // parity of slot r's barriers for slice gs
+                    // the slice's partial: one per pair of slices (two-level), else the item's partial kt mod 2
+                    const int gp = seq * pitem + (p.two_level ? kt >> 1 : (pitem == 2 ? (kt & 1) : 0));
                     const int b = gp % nbuf;
-                    const bool first = p.two_level || kt < 2, last = p.two_level || kt + 2 >= nk;
+                    const bool first = p.two_level ? (kt & 1) == 0 : kt < 2;
+                    const bool last = p.two_level ? (kt & 1) == 1 : kt + 2 >= nk;
                     // A decoded and the slot's B tiles landed (slot r = A buffer ab: the same phase); a slice that
                     // starts a partial in a buffer used before also needs the promoters to have taken the previous
                     // partial there (partial gp - nbuf: phase gp / nbuf - 1 of its pempty).  The waits overlap.
                     const bool reuse = first && gp >= nbuf;
-                    if (!mbar_wait3(&afull[ab], aph, &sfull[r], aph, reuse ? &pempty[b] : &afull[ab],
-                                    reuse ? (uint32_t)(gp / nbuf - 1) & 1u : aph, abort_flag)) {
+                    const uint32_t eph = reuse ? (uint32_t)(gp / nbuf - 1) & 1u : aph;
+                    bool got;
+                    if constexpr (kPair) {
+                        if (C == 2)  // the pair's B bytes of both CTAs land on this CTA's sfull
+                            got = mbar_wait3(&afull[r], aph, &sfull[r], aph, reuse ? &pempty[b] : &afull[r], eph,
+                                             abort_flag);
+                        else
+                            got = mbar_wait2_cl(&afull[r], aph, reuse ? &pempty[b] : &afull[r], eph, abort_flag);
+                    } else
+                        got = mbar_wait3(&afull[ab], aph, &sfull[r], aph, reuse ? &pempty[b] : &afull[ab], eph,
+                                         abort_flag);
+                    if (!got) {
                         ok = false;
                         break;
                     }
@@ -365,57 +510,80 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     const uint32_t d = tmem + part_base + (uint32_t)(b * kMaxBN);
                     const uint32_t a = tmem + (uint32_t)ab * kACols;
                     if (t.stacked) {
+                        // pair form: the leader's slot holds the N hi rows and the peer's the N lo rows (at the same
+                        // offset), i.e. the MMA's columns [0, N) and [N, 2N)
 #pragma unroll
-                        for (int k16 = 0; k16 < 4; ++k16)
-                            mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
-                                       (first && k16 == 0) ? 0u : 1u);
+                        for (int k16 = 0; k16 < 4; ++k16) {
+                            if constexpr (kPair)
+                                mma_f16_ta_pair(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
+                                                (first && k16 == 0) ? 0u : 1u);
+                            else
+                                mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
+                                           (first && k16 == 0) ? 0u : 1u);
+                        }
                     } else {
 #pragma unroll
                         for (int k16 = 0; k16 < 4; ++k16) {
-                            mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
-                                       (first && k16 == 0) ? 0u : 1u);
-                            mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
+                            if constexpr (kPair) {
+                                mma_f16_ta_pair(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
+                                                (first && k16 == 0) ? 0u : 1u);
+                                mma_f16_ta_pair(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
+                            } else {
+                                mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
+                                           (first && k16 == 0) ? 0u : 1u);
+                                mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
+                            }
                         }
                     }
-                    if (C > 1) mma_commit_mc(&sempty[r], cmask);
-                    else mma_commit(&sempty[r]);
-                    if (last) mma_commit(&pfull[b]);
-                    if ((r += 2) >= depth) r -= depth;
-                    if ((ab += 2) >= na) {
-                        ab -= na;
-                        aph ^= 1u;
+                    if constexpr (kPair) {
+                        mma_commit_pair_mc(&sempty[r], cmask);  // slot r free in every CTA (B multicast spans pairs)
+                        if (last) mma_commit_pair_mc(&pfull[b], pmask);
+                    } else {
+                        if (C > 1) mma_commit_mc(&sempty[r], cmask);
+                        else mma_commit(&sempty[r]);
+                        if (last) mma_commit(&pfull[b]);
                     }
                 }
                 base += nk;
                 ++seq;
             }
-            total = base;
-            mma_commit(accf);  // completes once every MMA issued above has completed (abort path included)
+            // completes once every MMA issued above has completed (abort path included)
+            if constexpr (kPair) mma_commit_pair_mc(accf, pmask);
+            else mma_commit(accf);
         } else if (warp == 1) {
             // ------------------------------------------------------------------ producer (one warp)
-            // lane 0 waits for the slot and posts its byte count; then every lane issues one or two of the slice's
-            // copies (a TMA instruction costs its issuing thread ~100 cycles, so one thread could not keep up)
+            // lane 0 waits for the slot and posts its byte counts and the weight copy; lanes 1 and 2 issue the B copies
             if (lane < 2 * kNumMaps) {
                 const CUtensorMap* m = lane < kNumMaps ? &maps.hi[lane] : &maps.lo[lane - kNumMaps];
                 asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
             }
             int gs = 0, r = 0;
             uint32_t eph = 0;  // parity of the sempty phase the next wrap waits for
+            const uint32_t sfull_leader = kPair ? cluster_addr(&sfull[0], leader) : 0u;
             Item t;
             for (int item = cid; item < n_items && ok; item += NC) {
-                if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
+                if (!load_item<kPair>(tiles, item, mgroups, C, crank, p, t)) continue;
                 const uint8_t* wblocks =
                     p.wp + ((int64_t)t.e * (p.a_rows / kBM) + t.m0 / kBM) * nk * (int64_t)kWBlock;
-                const uint32_t b_bytes = 2u * (uint32_t)t.N * 128u;
+                // the B bytes that land in THIS CTA's slot per slice: both parts of N rows (single form); N rows of
+                // one part (pair form, stacked) or N/2 rows of both parts (pair form)
+                const uint32_t b_bytes = kPair ? (uint32_t)t.N * 128u : 2u * (uint32_t)t.N * 128u;
                 const CUtensorMap* const mhi = &maps.hi[t.map];
                 const CUtensorMap* const mlo = &maps.lo[t.map];
                 for (int kt = 0; kt < nk; ++kt, ++gs) {
                     bool go = true;
                     if (lane == 0) {
-                        if (gs >= depth && !mbar_wait(&sempty[r], eph, abort_flag)) go = false;
+                        bool free_ = true;
+                        if (gs >= depth) {
+                            if constexpr (kPair) free_ = mbar_wait_cl(&sempty[r], eph, abort_flag);
+                            else free_ = mbar_wait(&sempty[r], eph, abort_flag);
+                        }
+                        if (!free_) go = false;
                         else {
                             mbar_arrive_expect_tx(&wfull[r], (uint32_t)kWBlock);
-                            mbar_arrive_expect_tx(&sfull[r], b_bytes);
+                            // one pair: the leader's sfull counts both CTAs' B bytes; the peer arms none
+                            if (!kPair || C != 2) mbar_arrive_expect_tx(&sfull[r], b_bytes);
+                            else if (ppos == 0) mbar_arrive_expect_tx(&sfull[r], 2u * b_bytes);
                         }
                     }
                     if (!__shfl_sync(0xffffffffu, go, 0)) {
@@ -424,17 +592,37 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     }
                     const uint32_t slot = ring_s + (uint32_t)(r * sbytes);
                     // lane 0 the weights (on their own barrier: the converters need nothing else), lanes 1 and 2 the
-                    // hi and lo boxes; in a cluster, CTA 0 copies hi and CTA 1 lo for all (C = 2 or 4), the others only
-                    // their weights
+                    // hi and lo boxes
                     if (lane == 0)
-                        bulk_load(slot + (uint32_t)(2 * t.lo_rows * 128), wblocks + (int64_t)kt * kWBlock, kWBlock,
-                                  &wfull[r]);
+                        bulk_load(slot + (uint32_t)(kPair ? kPairWOfs : 2 * t.lo_rows * 128),
+                                  wblocks + (int64_t)kt * kWBlock, kWBlock, &wfull[r]);
                     const int part = lane - 1;
                     if (part == 0 || part == 1) {
-                        const uint32_t dst = slot + (uint32_t)(part ? t.lo_rows * 128 : 0);
                         const CUtensorMap* map = part ? mlo : mhi;
-                        if (C == 1) tma_load_2d(dst, map, kt * kBK, t.row0, &sfull[r]);
-                        else if ((int)crank == part) tma_load_2d_mc(dst, map, kt * kBK, t.row0, &sfull[r], cmask);
+                        if constexpr (kPair) {
+                            // this CTA's rows: stacked -- part ppos, all N rows; else rows [ppos N/2, (ppos + 1) N/2)
+                            // of both parts.  With two pairs the CTAs at the same position need the same rows: the
+                            // pair-0 CTA copies hi and the pair-1 CTA lo, each multicast to both (stacked: the pair-0
+                            // CTA copies the one part)
+                            const bool mine = t.stacked ? part == (int)ppos : true;
+                            const int y = t.row0 + (t.stacked ? 0 : (int)ppos * (t.N / 2));
+                            const uint32_t dst = slot + (uint32_t)((t.stacked ? 0 : part) * kPairRows * 128);
+                            if (mine) {
+                                if (C == 2) {
+                                    tma_load_2d_pair(dst, map, kt * kBK, y, sfull_leader + (uint32_t)(r * 8));
+                                } else {
+                                    const uint16_t mc = (uint16_t)((1u << ppos) | (1u << (ppos + 2)));
+                                    const int issuer = t.stacked ? 0 : part;  // the pair that issues this copy
+                                    if ((int)(crank >> 1) == issuer) tma_load_2d_mc(dst, map, kt * kBK, y, &sfull[r], mc);
+                                }
+                            }
+                        } else {
+                            // in a cluster, CTA 0 copies hi and CTA 1 lo for all (C = 2 or 4), the others only their
+                            // weights
+                            const uint32_t dst = slot + (uint32_t)(part ? t.lo_rows * 128 : 0);
+                            if (C == 1) tma_load_2d(dst, map, kt * kBK, t.row0, &sfull[r]);
+                            else if ((int)crank == part) tma_load_2d_mc(dst, map, kt * kBK, t.row0, &sfull[r], cmask);
+                        }
                     }
                     if (++r == depth) {
                         r = 0;
@@ -442,13 +630,37 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     }
                 }
             }
+            if (lane == 0) *total_slot = gs;
             // no copy may still be writing shared memory when the CTA exits (on the abort path nobody has waited
             // for the last slices): wait, bounded, for the last `depth` slices issued
+            // (one pair: the peer's B copies are counted on the leader's sfull, which the leader waits for here before
+            // the final cluster barrier that the peer cannot pass without it)
             if (lane == 0)
                 for (int k = max(0, gs - depth); k < gs; ++k) {
                     mbar_wait(&wfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
-                    mbar_wait(&sfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
+                    if (!kPair || C != 2 || ppos == 0) mbar_wait(&sfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
                 }
+        } else if (kPair && C == 4 && warp == 3 && lane == 0) {
+            // ------------------------------------------------------------------ B relay (pair form)
+            // in slice order: once this CTA's B rows of the slice have landed, one arrival on the leader's `ready`
+            const uint32_t ready0 = cluster_addr(&afull[0], leader);
+            int gs = 0, r = 0;
+            uint32_t ph = 0;
+            Item t;
+            for (int item = cid; item < n_items && ok; item += NC) {
+                if (!load_item<kPair>(tiles, item, mgroups, C, crank, p, t)) continue;
+                for (int kt = 0; kt < nk; ++kt, ++gs) {
+                    if (!mbar_wait_cl(&sfull[r], ph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cl(ready0 + (uint32_t)(r * sizeof(uint64_t)));
+                    if (++r == depth) {
+                        r = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
         }
         __syncwarp();
     } else if (warp < 16) {
@@ -461,11 +673,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         const int cg = (warp - 4) >> 2;  // promoter warpgroup 0..2
         const int mrow = 32 * q + lane;
         constexpr int kChunks = kMaxBN / 96;  // most 32-column chunks of a thread
+        // pair form: a promoter warp arrives once on the leader's pempty when all its lanes have loaded the partial
+        const uint32_t pempty0 = kPair ? cluster_addr(&pempty[0], leader) : 0u;
         int b = 0;
         uint32_t bph = 0;
         Item t;
         for (int item = cid; item < n_items && ok; item += NC) {
-            if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
+            if (!load_item<kPair>(tiles, item, mgroups, C, crank, p, t)) continue;
             const int N = t.N;
             const bool stacked = t.stacked;
             const int mine = (N / 32 - cg + 2) / 3;                         // whole 32-column chunks of this thread
@@ -476,7 +690,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
 #pragma unroll
                 for (int k = 0; k < 32; ++k) acc[i][k] = 0.0f;
             for (int g = 0; g < pitem && ok; ++g) {
-                if (!mbar_wait(&pfull[b], bph, abort_flag)) {
+                bool got;
+                if constexpr (kPair) got = mbar_wait_cl(&pfull[b], bph, abort_flag);
+                else got = mbar_wait(&pfull[b], bph, abort_flag);
+                if (!got) {
                     ok = false;
                     break;
                 }
@@ -525,7 +742,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     }
                 }
                 tc_fence_before();
-                mbar_arrive(&pempty[b]);
+                if constexpr (kPair) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cl(pempty0 + (uint32_t)(b * sizeof(uint64_t)));
+                } else {
+                    mbar_arrive(&pempty[b]);
+                }
                 if (++b == nbuf) {
                     b = 0;
                     bph ^= 1u;
@@ -618,29 +840,41 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         // thread = weight row ct = TMEM lane of its warp: 64 weights a slice into the 32 columns of A buffer ab
         const int ct = threadIdx.x - 512;
         const uint32_t lane_base = (uint32_t)(ct & ~31) << 16;
-        int r = 0;           // the slice's ring slot = its A buffer
+        // pair form: a converter warp arrives once on the leader's `ready` when all its lanes' stores are done
+        const uint32_t ready0 = kPair ? cluster_addr(&afull[0], leader) : 0u;
+        int r = 0;           // the slice's ring slot (single form: also its A buffer)
         uint32_t rph = 0;    // that slot's wfull parity
+        int gs = 0;          // the slice's global index
         bool ready = false;  // its copies are known to have landed (tested while the previous slice was stored)
         Item t;
         for (int item = cid; item < n_items && ok; item += NC) {
-            if (!load_item(tiles, item, mgroups, C, crank, p, t)) continue;
-            const int wofs = 2 * t.lo_rows * 128;  // the packed weight block within a slot
-            for (int kt = 0; kt < nk && ok; ++kt) {
+            if (!load_item<kPair>(tiles, item, mgroups, C, crank, p, t)) continue;
+            const int wofs = kPair ? kPairWOfs : 2 * t.lo_rows * 128;  // the packed weight block within a slot
+            for (int kt = 0; kt < nk && ok; ++kt, ++gs) {
                 if (!ready && !mbar_wait(&wfull[r], rph, abort_flag)) {
                     ok = false;
                     break;
                 }
+                if constexpr (kPair) {
+                    // the A buffer's previous slice (gs - na) has been released by its MMAs' commits
+                    const int pg = gs - na;
+                    if (pg >= 0 && !mbar_wait(&sempty[pg % depth], (uint32_t)(pg / depth) & 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 tc_fence_after();
+                const int ab = kPair ? gs % na : r;
                 const uint8_t* wb = ring + r * sbytes + wofs;
                 const uint4 codes = *reinterpret_cast<const uint4*>(wb + ct * 16);
                 const __half2 sc = *reinterpret_cast<const __half2*>(wb + 2048 + ct * 4);
                 uint32_t col[16];  // one 32-value block at a time
                 decode_weights16(codes.x, __low2half2(sc), col);
                 decode_weights16(codes.y, __low2half2(sc), col + 8);
-                tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)r * kACols, col);
+                tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols, col);
                 decode_weights16(codes.z, __high2half2(sc), col);
                 decode_weights16(codes.w, __high2half2(sc), col + 8);
-                tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)r * kACols + 16u, col);
+                tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols + 16u, col);
                 const int rn = r + 1 == depth ? 0 : r + 1;
                 const uint32_t rphn = r + 1 == depth ? rph ^ 1u : rph;
                 // the next global slice (of this item or the next) uses slot rn: test its barrier while the stores
@@ -648,8 +882,16 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 ready = mbar_test(smem_u32(&wfull[rn]), rphn);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&afull[r]);
-                mbar_arrive(&sempty[r]);
+                if constexpr (kPair) {
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive_cl(ready0 + (uint32_t)(r * sizeof(uint64_t)));
+                        mbar_arrive(&sempty[r]);
+                    }
+                } else {
+                    mbar_arrive(&afull[r]);
+                    mbar_arrive(&sempty[r]);
+                }
                 r = rn;
                 rph = rphn;
             }
@@ -662,18 +904,28 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
-        mbar_wait(accf, 0, nullptr);  // every MMA has completed before the tensor memory is released
+        // every MMA has completed before the tensor memory is released (pair form: the leader's final commits arrive
+        // in both CTAs of the pair)
+        if constexpr (kPair) mbar_wait_cl(accf, 0, nullptr);
+        else mbar_wait(accf, 0, nullptr);
         if (C > 1 && lane == 0) {
-            // every CTA of the cluster has delivered its last slot releases here (its MMAs are done with them):
-            // nothing arrives on this CTA's barriers after it leaves
-            for (int k = max(0, total - depth); k < total; ++k)
-                if (!mbar_wait(&sempty[k % depth], (uint32_t)(k / depth) & 1u, abort_flag)) break;
+            // every MMA commit that targets this CTA's slot barriers has arrived (each slot's last phase completes
+            // only after all of them): nothing arrives on this CTA's barriers after it leaves
+            const int total = *total_slot;
+            for (int k = max(0, total - depth); k < total; ++k) {
+                bool done;
+                if constexpr (kPair) done = mbar_wait_cl(&sempty[k % depth], (uint32_t)(k / depth) & 1u, abort_flag);
+                else done = mbar_wait(&sempty[k % depth], (uint32_t)(k / depth) & 1u, abort_flag);
+                if (!done) break;
+            }
         }
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        if constexpr (kPair) tmem_dealloc_pair(tmem, kTmemCols);
+        else tmem_dealloc(tmem, kTmemCols);
     }
-    // no CTA leaves while another may still copy into its shared memory or arrive on its barriers
+    // no CTA leaves while another may still copy into its shared memory, arrive on its barriers or (pair form) read
+    // its tensor memory
     if (C > 1) cluster_sync();
 }
 
@@ -707,26 +959,22 @@ bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uin
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// resident clusters of the kernel per device and cluster size (looked up once)
-int g_resident[64][5] = {};
+// per-device, once: the dynamic shared-memory attribute of both forms, and the resident clusters of each form and
+// cluster size
+struct DeviceState {
+    bool attr = false;
+    int resident[2][5] = {};
+};
+DeviceState g_dev[64];
+std::mutex g_dev_mu;
 
-}  // namespace
-
-cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    static uint64_t attr_done = 0;  // one bit per device
-    if (dev < 64 && !(attr_done & (1ull << dev))) {
-        cudaError_t err = cudaFuncSetAttribute(experts_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               kSmemBytes);
-        if (err != cudaSuccess) return err;
-        attr_done |= 1ull << dev;
-    }
-    if (max_tiles <= 0) return cudaSuccess;
+template <bool kPair>
+cudaError_t launch_form(const ExpertsGemmArgs& a, int64_t max_tiles, int dev, cudaStream_t s) {
     GemmMaps maps;
     const uint16_t* lo = a.bop + a.b_rows * (int64_t)a.K;
+    const int step = kPair ? kPairBox : kRowBox;
     for (int m = 0; m < kNumMaps; ++m) {
-        const uint32_t box = (uint32_t)(kRowBox * (m + 1));
+        const uint32_t box = (uint32_t)(step * (m + 1));
         if (!make_map(&maps.hi[m], a.bop, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
                       box, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !make_map(&maps.lo[m], lo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)a.K, (uint64_t)a.b_rows, kBK,
@@ -736,9 +984,11 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     const int mt = a.a_rows / kBM;
     ExpertsGemmArgs args = a;
     // clusters share the row tiles through L2 once instead of once per weight slice; they pay off when tiles are
-    // large (L2 bandwidth bounds the product), not for small tiles, whose CTAs would only wait on one another
+    // large (L2 bandwidth bounds the product), not for small tiles, whose CTAs would only wait on one another.  The
+    // pair form is a cluster of one pair, or of two pairs that share each row tile by multicast.
     const bool large = a.b_rows >= (int64_t)kClusterRows * a.n_experts;
-    args.cluster = !large ? 1 : (mt % 4 == 0 ? 4 : (mt % 2 == 0 ? 2 : 1));
+    if (kPair) args.cluster = (large && mt % 4 == 0) ? 4 : 2;
+    else args.cluster = !large ? 1 : (mt % 4 == 0 ? 4 : (mt % 2 == 0 ? 2 : 1));
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
@@ -754,21 +1004,49 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     const int64_t items = max_tiles * (mt / args.cluster);
     cfg.gridDim = dim3((unsigned)(args.cluster * 512));
     int resident = 0;
-    if (dev < 64 && args.cluster <= 4 && g_resident[dev][args.cluster] > 0) {
-        resident = g_resident[dev][args.cluster];
-    } else {
-        cudaError_t err = cudaOccupancyMaxActiveClusters(&resident, experts_gemm_kernel, &cfg);
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        resident = g_dev[dev].resident[kPair][args.cluster];
+    }
+    if (resident <= 0) {
+        cudaError_t err = cudaOccupancyMaxActiveClusters(&resident, experts_gemm_kernel<kPair>, &cfg);
         if (err != cudaSuccess || resident <= 0) {
             cudaGetLastError();
             return err != cudaSuccess ? err : cudaErrorInvalidConfiguration;
         }
-        if (dev < 64 && args.cluster <= 4) g_resident[dev][args.cluster] = resident;
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        g_dev[dev].resident[kPair][args.cluster] = resident;
     }
     const int64_t nclusters = items < resident ? items : resident;
     cfg.gridDim = dim3((unsigned)(nclusters * args.cluster));
-    const cudaError_t err = cudaLaunchKernelEx(&cfg, experts_gemm_kernel, args, maps);
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, experts_gemm_kernel<kPair>, args, maps);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        if (!g_dev[dev].attr) {
+            err = cudaFuncSetAttribute(experts_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+            if (err == cudaSuccess)
+                err = cudaFuncSetAttribute(experts_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           kSmemBytes);
+            if (err != cudaSuccess) return err;
+            g_dev[dev].attr = true;
+        }
+    }
+    if (max_tiles <= 0) return cudaSuccess;
+    // the CTA-pair form needs an even number of 128-row weight slices (each pair takes 256 rows)
+    if ((a.a_rows / kBM) % 2 == 0) return launch_form<true>(a, max_tiles, dev, s);
+    return launch_form<false>(a, max_tiles, dev, s);
 }
 
 }  // namespace smoe

@@ -19,61 +19,102 @@ namespace smoe {
 namespace {
 
 // ------------------------------------------------------------------------------------------------ route
-// One warp per token.  Lane l holds the logits of experts l, l+32, l+64, ...; each of the K rounds takes the warp's
-// largest remaining (value, id) -- ties to the lower id -- by a butterfly of shuffles, so every lane learns the
-// winner and the owner lane retires it.  Lane k keeps round k's winner, then the K weights are
-// exp(l_k - l_1) / sum_j exp(l_j - l_1), summed in k order.
+// One warp per token.  Every logit becomes a 64-bit key that orders like (value descending, expert id ascending):
+// the high word maps the fp32 value to an unsigned integer of the same order (-0 taken as +0, so that equal values
+// tie and the lower id wins, as in a float comparison), the low word is 0xFFFF - id.  The largest key is the best
+// expert.  Lane l holds the logits of experts 4l..4l+3 + 128 i (float4 loads) and keeps its own three largest keys in
+// order; each of the K rounds takes the warp's largest head by a butterfly of shuffles and the lane that owned it pops
+// it.  Winners leave in descending key order, so a lane that has popped all three rescans its keys below the last one
+// it popped.  Lane k keeps round k's winner; the K weights are exp(l_k - l_1) / sum_j exp(l_j - l_1), summed in k
+// order.
+__device__ __forceinline__ uint64_t route_key(float v, int e) {
+    if (v == 0.0f) v = 0.0f;  // -0 -> +0
+    const uint32_t b = __float_as_uint(v);
+    const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return ((uint64_t)o << 32) | (uint32_t)(0xFFFF - e);
+}
+__device__ __forceinline__ float key_value(uint64_t k) {
+    const uint32_t o = (uint32_t)(k >> 32);
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+}
+__device__ __forceinline__ int key_id(uint64_t k) { return 0xFFFF - (int)(k & 0xFFFFu); }
+
+// the lane's three largest keys below `bound` among kv (0 = empty), in order
+template <int NV>
+__device__ __forceinline__ void top3(const uint64_t (&kv)[NV], uint64_t bound, uint64_t& a, uint64_t& b,
+                                     uint64_t& c) {
+    a = b = c = 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const uint64_t k = kv[i] < bound ? kv[i] : 0ull;
+        if (k > c) {
+            if (k > b) {
+                c = b;
+                if (k > a) {
+                    b = a;
+                    a = k;
+                } else {
+                    b = k;
+                }
+            } else {
+                c = k;
+            }
+        }
+    }
+}
+
 template <int VPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int K,
                                                          int32_t* __restrict__ ids, float* __restrict__ w) {
+    constexpr int NQ = VPL / 4;  // float4 loads a lane
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     const float* lt = logits + t * E;
-    float v[VPL];
+    uint64_t kv[VPL];
+    const bool vec = (E & 3) == 0;  // rows 16-byte aligned: E % 4 == 0 (the pointer itself is 16-byte aligned)
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = e < E ? __ldg(lt + e) : -INFINITY;
-    }
-    float my_v = -INFINITY;
-    int my_i = INT_MAX;
-    for (int k = 0; k < K; ++k) {
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && (v[i] > bv || (v[i] == bv && e < bi))) {
-                bv = v[i];
-                bi = e;
-            }
+    for (int i = 0; i < NQ; ++i) {
+        const int e0 = 128 * i + 4 * lane;
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (vec && e0 + 3 < E) f = __ldg(reinterpret_cast<const float4*>(lt + e0));
+        else if (e0 < E) {
+            f.x = __ldg(lt + e0);
+            if (e0 + 1 < E) f.y = __ldg(lt + e0 + 1);
+            if (e0 + 2 < E) f.z = __ldg(lt + e0 + 2);
+            if (e0 + 3 < E) f.w = __ldg(lt + e0 + 3);
         }
+        kv[4 * i + 0] = e0 + 0 < E ? route_key(f.x, e0 + 0) : 0ull;
+        kv[4 * i + 1] = e0 + 1 < E ? route_key(f.y, e0 + 1) : 0ull;
+        kv[4 * i + 2] = e0 + 2 < E ? route_key(f.z, e0 + 2) : 0ull;
+        kv[4 * i + 3] = e0 + 3 < E ? route_key(f.w, e0 + 3) : 0ull;
+    }
+    uint64_t h0, h1, h2;
+    top3(kv, ~0ull, h0, h1, h2);
+    int popped = 0;
+    uint64_t mine = 0;
+    for (int k = 0; k < K; ++k) {
+        uint64_t best = h0;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
+            const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
+            best = o > best ? o : best;
         }
-        if (lane == k) {
-            my_v = bv;
-            my_i = bi;
+        if (lane == k) mine = best;
+        if (best == h0) {  // this lane owned the winner (keys are unique): pop it
+            h0 = h1;
+            h1 = h2;
+            h2 = 0;
+            if (++popped % 3 == 0) top3(kv, best, h0, h1, h2);
         }
-        // retire the winner: its owner lane sets it to -inf, below every finite logit, so it cannot win again
-        // while live candidates remain (K <= E)
-#pragma unroll
-        for (int i = 0; i < VPL; ++i)
-            if (lane + 32 * i == bi) v[i] = -INFINITY;
     }
-    const float lmax = __shfl_sync(0xffffffffu, my_v, 0);
-    const float ex = lane < K ? expf(my_v - lmax) : 0.0f;
+    const float lmax = key_value(__shfl_sync(0xffffffffu, mine, 0));
+    const float mv = key_value(mine);
+    const float ex = lane < K ? expf(mv - lmax) : 0.0f;
     float sum = 0.0f;
     for (int k = 0; k < K; ++k) sum += __shfl_sync(0xffffffffu, ex, k);
     if (lane < K) {
-        ids[t * K + lane] = my_i;
+        ids[t * K + lane] = key_id(mine);
         w[t * K + lane] = __fdiv_rn(ex, sum);
     }
 }

@@ -110,7 +110,8 @@ smoe_status smoe_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, in
     if (!aligned16(codes) || !aligned16(scales) || !aligned16(packed)) return SMOE_ERR_ARG;
     if ((int64_t)E * (rows / 128) * (cols / 64) > INT32_MAX) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    return launch_status(smoe::launch_pack_q2(codes, scales, E, rows, cols, 0, packed, (cudaStream_t)stream));
+    return launch_status(
+        smoe::launch_pack_q2(codes, scales, nullptr, E, rows, cols, 0, packed, nullptr, (cudaStream_t)stream));
 }
 
 smoe_status smoe_pack_q2_swiglu(const uint8_t* codes, const uint16_t* scales, int E, int F, int H, uint8_t* packed,
@@ -119,7 +120,8 @@ smoe_status smoe_pack_q2_swiglu(const uint8_t* codes, const uint16_t* scales, in
     if (!aligned16(codes) || !aligned16(scales) || !aligned16(packed)) return SMOE_ERR_ARG;
     if ((int64_t)E * (2 * F / 128) * (H / 64) > INT32_MAX) return SMOE_ERR_ARG;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
-    return launch_status(smoe::launch_pack_q2(codes, scales, E, 2 * F, H, F, packed, (cudaStream_t)stream));
+    return launch_status(
+        smoe::launch_pack_q2(codes, scales, nullptr, E, 2 * F, H, F, packed, nullptr, (cudaStream_t)stream));
 }
 
 static smoe_status check_gemm_shape(int64_t n, int E, int H, int F) {
@@ -184,6 +186,61 @@ smoe_status smoe_experts_down(const uint16_t* hop, int32_t* tiles, int64_t n, in
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
     smoe::ExpertsGemmArgs a{hop, tiles, wd, H, F, dm, n, E, false, 1, nullptr, nullptr, nullptr};
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
+}
+
+size_t smoe_experts_q8_work_bytes(int64_t n, int E, int H, int F) {
+    if (n < 0 || E < 1 || H < 1 || F < 1) return 0;
+    // the routed rows in operand form (fp16 [2][n][K]), then the packed weights; the larger of the two products
+    const size_t gu = (size_t)4 * (size_t)n * (size_t)H + smoe_pack_q2_bytes(E, 2 * F, H);
+    const size_t dn = (size_t)4 * (size_t)n * (size_t)F + smoe_pack_q2_bytes(E, H, F);
+    return gu > dn ? gu : dn;
+}
+
+smoe_status smoe_experts_gateup_q8(const int8_t* xc, const uint16_t* xs, int64_t in_rows, const int32_t* src,
+                                   int32_t* tiles, int64_t n, int E, const smoe_q2w* w_gu, int H, int F, void* work,
+                                   size_t work_bytes, float* gu, void* stream) {
+    const smoe_status st = check_gemm_shape(n, E, H, F);
+    if (st != SMOE_OK) return st;
+    if (n == 0) return SMOE_OK;
+    if (in_rows < 1 || n > INT32_MAX) return SMOE_ERR_ARG;
+    if (!aligned16(xc) || !aligned16(xs) || !aligned16(src) || !aligned16(tiles) || !aligned16(w_gu) ||
+        !aligned16(work) || !aligned16(gu))
+        return SMOE_ERR_ARG;
+    if (work_bytes < smoe_experts_q8_work_bytes(n, E, H, F)) return SMOE_ERR_ARG;
+    if ((int64_t)E * (2 * F / 128) * (H / 64) > INT32_MAX) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    uint16_t* xop = static_cast<uint16_t*>(work);
+    uint8_t* wp = static_cast<uint8_t*>(work) + (size_t)4 * (size_t)n * (size_t)H;
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t err = smoe::launch_gather_q8(xc, xs, in_rows, H, src, n, xop, s);
+    if (err == cudaSuccess) err = smoe::launch_pack_q2(nullptr, nullptr, w_gu, E, 2 * F, H, 0, wp, tiles + 3, s);
+    if (err != cudaSuccess) return launch_status(err);
+    smoe::ExpertsGemmArgs a{xop, tiles, wp, 2 * F, H, gu, n, E, true, 1, nullptr, nullptr, nullptr};
+    return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), s));
+}
+
+smoe_status smoe_experts_down_q8(const int8_t* hc, const uint16_t* hs, int32_t* tiles, int64_t n, int E,
+                                 const smoe_q2w* w_d, int H, int F, void* work, size_t work_bytes, float* dm,
+                                 void* stream) {
+    const smoe_status st = check_gemm_shape(n, E, H, F);
+    if (st != SMOE_OK) return st;
+    if (n == 0) return SMOE_OK;
+    if (n > INT32_MAX) return SMOE_ERR_ARG;
+    if (!aligned16(hc) || !aligned16(hs) || !aligned16(tiles) || !aligned16(w_d) || !aligned16(work) ||
+        !aligned16(dm))
+        return SMOE_ERR_ARG;
+    if (work_bytes < smoe_experts_q8_work_bytes(n, E, H, F)) return SMOE_ERR_ARG;
+    if ((int64_t)E * (H / 128) * (F / 64) > INT32_MAX) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    uint16_t* hop = static_cast<uint16_t*>(work);
+    uint8_t* wp = static_cast<uint8_t*>(work) + (size_t)4 * (size_t)n * (size_t)F;
+    const cudaStream_t s = (cudaStream_t)stream;
+    // H is already in routed-row order: the operand form of row r is row r itself (no src)
+    cudaError_t err = smoe::launch_gather_q8(hc, hs, n, F, nullptr, n, hop, s);
+    if (err == cudaSuccess) err = smoe::launch_pack_q2(nullptr, nullptr, w_d, E, H, F, 0, wp, tiles + 3, s);
+    if (err != cudaSuccess) return launch_status(err);
+    smoe::ExpertsGemmArgs a{hop, tiles, wp, H, F, dm, n, E, false, 1, nullptr, nullptr, nullptr};
+    return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), s));
 }
 
 smoe_status smoe_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,

@@ -6,6 +6,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "smoe.h"
+
 namespace smoe {
 
 size_t group_work_bytes(int64_t n, int E);
@@ -17,8 +19,8 @@ cudaError_t launch_quantize_q8(const float* x, int64_t rows, int cols, int8_t* c
                                cudaStream_t s);
 cudaError_t launch_swiglu_requant(const float* gu, int64_t n, int F, int8_t* hc, uint16_t* hs, uint16_t* hop,
                                   cudaStream_t s);
-cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, int E, int rows, int cols, int half,
-                           uint8_t* packed, cudaStream_t s);
+cudaError_t launch_pack_q2(const uint8_t* codes, const uint16_t* scales, const smoe_q2w* desc, int E, int rows,
+                           int cols, int half, uint8_t* packed, int32_t* status, cudaStream_t s);
 cudaError_t launch_gather_q8(const int8_t* codes, const uint16_t* scales, int64_t in_rows, int cols,
                              const int32_t* src, int64_t n, uint16_t* out, cudaStream_t s);
 cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,

@@ -191,6 +191,35 @@ def test_quantize_bit_exact_full_and_edges(B):
     c, s = gpu_q8(B, e)
     co, so = oracle.quantize_q8(e)
     assert np.array_equal(c, co) and np.array_equal(s, so)
+    # quotients x / d on and within a few ulps of the .5 ties between codes, for several block scales: the first value
+    # of each block fixes amax (so d = fp16(amax / 127)), the others sit at (k + 0.5) d and 1..3 ulps either side
+    rows = []
+    for A in (1.0, 3.7, 0.01, 1.3e-4, 300.0, 6.1e-5):
+        d = np.float32(np.float16(np.float32(A) / np.float32(127.0)))
+        vals = []
+        for k in range(0, 127, 3):
+            tie = np.float32((k + 0.5) * np.float64(d))
+            for u in (-3, -2, -1, 0, 1, 2, 3):
+                v = tie
+                for _ in range(abs(u)):
+                    v = np.nextafter(v, np.float32(np.inf if u > 0 else -np.inf))
+                vals.append(v if (k + u) % 2 else -v)
+        vals = np.array(vals, np.float32)
+        nb = -(-len(vals) // 31)
+        blk = np.zeros((nb, 32), np.float32)
+        blk[:, 0] = np.float32(A)
+        flat = np.zeros(nb * 31, np.float32)
+        flat[:len(vals)] = vals
+        blk[:, 1:] = flat.reshape(nb, 31)
+        rows.append(blk.reshape(-1))
+    n = max(len(r) for r in rows)
+    n = -(-n // 32) * 32
+    e = np.zeros((len(rows), n), np.float32)
+    for i, r in enumerate(rows):
+        e[i, :len(r)] = r
+    c, s = gpu_q8(B, e)
+    co, so = oracle.quantize_q8(e)
+    assert np.array_equal(c, co) and np.array_equal(s, so)
     # an odd number of rows of the tiny width
     x = synth.make_rows(3, 256, seed=5)
     c, s = gpu_q8(B, x)
