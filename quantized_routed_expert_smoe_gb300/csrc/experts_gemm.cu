@@ -35,16 +35,17 @@
 // tile's B rows split between the two CTAs' shared memories (a tile of at most 96 rows: its hi rows in the even CTA
 // and its lo rows in the odd one, one MMA of 2N; a larger tile: N/2 rows of each part in each).  The tensor cores
 // of both SMs read both halves, so each SM takes in half the row bytes per MMA of the single-CTA form, its ring
-// slots are half as large and twice as many slices are in flight.  The even CTA issues the pair's MMAs: both CTAs'
-// converter warps and B arrivals meet on its `ready` barrier and both CTAs' promoter warps on its `pempty`; its
-// commits release the slots in every CTA of the cluster and the partials in both.  The single-CTA form (an odd
-// number of 128-row slices) issues its own MMAs.  Five warpgroups, registers rebalanced with setmaxnreg:
+// slots are half as large and twice as many slices are in flight.  A cluster is one pair.  The even CTA issues the
+// pair's MMAs: both CTAs' converter warps meet on its `ready` barrier, both CTAs' B copies count their bytes on its
+// slot barrier (the cta_group::2 form of the TMA load) and both CTAs' promoter warps arrive on its `pempty`; its
+// commits release the slots and signal the partials in both CTAs.  The single-CTA form (an odd number of 128-row
+// slices) issues its own MMAs.  No TMA load is multicast.  Five warpgroups, registers rebalanced with setmaxnreg:
 //   warpgroup 0   warps 0 and 2, one lane each: the MMAs of alternate slices -- of alternate slice pairs for
 //                 gate/up (four K16 steps x two parts a slice; one thread's waits overlap the other's MMAs); warp 0
-//                 also allocates the tensor memory; warp 3 (two pairs): relays its CTA's landed B rows to the leader;
+//                 also allocates the tensor memory;
 //                 warp 1: the producer -- per 64-wide K slice, one TMA tile load of the tile's rows of each part
-//                 (128-byte swizzle; in a cluster, multicast by one CTA to all) and one bulk copy of the packed
-//                 weight block into a ring slot;
+//                 (128-byte swizzle; pair form: this CTA's half of them) and one bulk copy of the packed weight
+//                 block into a ring slot;
 //   warpgroups 1-3  promoters: add each finished partial into fp32 registers (a TMEM lane a thread, every third
 //                 32-column chunk a warpgroup), then write the fp32 rows -- or, for the fused SwiGLU product (gate
 //                 and up rows interleaved in the packed weights), h = silu(g) * u requantised to q8, planar and in
@@ -93,7 +94,6 @@ constexpr uint32_t kACols = 32;                // one slice of A: 128 lanes x 64
 constexpr int kMaxA = 8;                       // A buffers at most
 constexpr int kMaxBufs = 4;                    // partial buffers at most
 constexpr int kMaxStackN = 96;                 // tiles up to this N stack hi and lo rows into one MMA
-constexpr int kClusterRows = 96;               // mean rows per expert from which CTAs of a tile form a cluster
 constexpr int kSmemBytes = 232448;             // the per-CTA maximum (227 KB): [align slack][ring][barriers]
 constexpr int kBarBytes = 512;
 constexpr int kScratchBytes = SMOE_TILE_ROWS * 4 * 4;  // SwiGLU epilogue: a warp's block amax per column [col][4]
@@ -158,23 +158,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// TMA 2D tile multicast to the CTAs of `mask` in the cluster: same shared-memory offset and mbarrier in each
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-// arrive once on `bar` in every CTA of `mask` when every tcgen05.mma issued so far by this thread has completed
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -381,15 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const int pitem = p.two_level ? nk / 2 : min(2, nk);  // partials an item
 
     // persistent: cluster cid of NC takes items cid, cid + NC, ...; its CTAs take the C weight slices of an item
-    const int C = p.cluster;
-    const uint32_t crank = C > 1 ? cluster_rank() : 0u;
-    const uint16_t cmask = (uint16_t)((1u << C) - 1u);
+    // (pair form: a cluster is one pair; single form: one CTA)
+    constexpr int C = kPair ? 2 : 1;
+    const uint32_t crank = kPair ? cluster_rank() : 0u;
     const int mgroups = p.a_rows / kBM / C;
     const int n_items = n_tiles * mgroups;
     const int cid = blockIdx.x / C, NC = gridDim.x / C;
-    // pair form: this CTA's position in its pair (0 = the leader) and the pair's two CTAs
-    const uint32_t ppos = crank & 1u, leader = crank & ~1u;
-    const uint16_t pmask = (uint16_t)(3u << leader);
+    // pair form: this CTA's position in its pair (0 = the leader, which issues the MMAs)
+    const uint32_t ppos = crank, leader = 0u;
+    constexpr uint16_t pmask = 3u;  // both CTAs of the pair
 
     // fixed geometry for every item (tiles of up to kMaxBN rows): a ring of `depth` slots, na A buffers and nbuf
     // partial buffers of kMaxBN columns in tensor memory
@@ -426,17 +409,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         // pair form: arrivals are per warp (converters, promoters) and come from both CTAs of the pair
-        const int n_pairs = C / 2;
         for (int r = 0; r < kMaxRing; ++r) {
-            mbar_init(&sfull[r], 1);                 // the arrival that posts the B tiles' byte count
+            // the arrival that posts the B tiles' byte count (pair form: the leader's, with both CTAs' bytes)
+            mbar_init(&sfull[r], 1);
             mbar_init(&wfull[r], 1);                 // the arrival that posts the weight block's
-            // the MMAs' commits (every CTA / every pair of the cluster), then the own converters
-            mbar_init(&sempty[r], kPair ? n_pairs + kConverters / 32 : C + kConverters);
+            // the MMAs' commit (the leader's, in both CTAs of a pair), then the own converters
+            mbar_init(&sempty[r], kPair ? 1 + kConverters / 32 : 1 + kConverters);
         }
-        // pair form: both CTAs' converter warps, plus (two pairs) both CTAs' B relays; one pair counts its B bytes on
-        // the leader's sfull instead
-        for (int a = 0; a < kMaxA; ++a)
-            mbar_init(&afull[a], kPair ? 2 * (kConverters / 32 + (C == 4 ? 1 : 0)) : kConverters);
+        // A decoded: every converter (pair form: the converter warps of both CTAs, on the leader's barrier)
+        for (int a = 0; a < kMaxA; ++a) mbar_init(&afull[a], kPair ? 2 * (kConverters / 32) : kConverters);
         for (int b = 0; b < kMaxBufs; ++b) {
             mbar_init(&pfull[b], 1);
             mbar_init(&pempty[b], kPair ? 2 * (kPromoters / 32) : kPromoters);
@@ -457,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     }
     tc_fence_before();
     __syncthreads();
-    if (C > 1) cluster_sync();  // every CTA's barriers are initialised before any remote copy or arrival
+    if (kPair) cluster_sync();  // both CTAs' barriers are initialised before any remote copy or arrival
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t ring_s = smem_u32(ring);
@@ -491,17 +472,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     // partial there (partial gp - nbuf: phase gp / nbuf - 1 of its pempty).  The waits overlap.
                     const bool reuse = first && gp >= nbuf;
                     const uint32_t eph = reuse ? (uint32_t)(gp / nbuf - 1) & 1u : aph;
-                    bool got;
-                    if constexpr (kPair) {
-                        if (C == 2)  // the pair's B bytes of both CTAs land on this CTA's sfull
-                            got = mbar_wait3(&afull[r], aph, &sfull[r], aph, reuse ? &pempty[b] : &afull[r], eph,
-                                             abort_flag);
-                        else
-                            got = mbar_wait2_cl(&afull[r], aph, reuse ? &pempty[b] : &afull[r], eph, abort_flag);
-                    } else
-                        got = mbar_wait3(&afull[ab], aph, &sfull[r], aph, reuse ? &pempty[b] : &afull[ab], eph,
-                                         abort_flag);
-                    if (!got) {
+                    // (pair form: the A barrier is the slot's, and both CTAs' B bytes land on this CTA's sfull)
+                    const int ai = kPair ? r : ab;
+                    if (!mbar_wait3(&afull[ai], aph, &sfull[r], aph, reuse ? &pempty[b] : &afull[ai], eph, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -536,11 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                         }
                     }
                     if constexpr (kPair) {
-                        mma_commit_pair_mc(&sempty[r], cmask);  // slot r free in every CTA (B multicast spans pairs)
+                        mma_commit_pair_mc(&sempty[r], pmask);  // slot r free in both CTAs
                         if (last) mma_commit_pair_mc(&pfull[b], pmask);
                     } else {
-                        if (C > 1) mma_commit_mc(&sempty[r], cmask);
-                        else mma_commit(&sempty[r]);
+                        mma_commit(&sempty[r]);
                         if (last) mma_commit(&pfull[b]);
                     }
                 }
@@ -581,8 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                         if (!free_) go = false;
                         else {
                             mbar_arrive_expect_tx(&wfull[r], (uint32_t)kWBlock);
-                            // one pair: the leader's sfull counts both CTAs' B bytes; the peer arms none
-                            if (!kPair || C != 2) mbar_arrive_expect_tx(&sfull[r], b_bytes);
+                            // pair form: the leader's sfull counts both CTAs' B bytes; the peer arms none
+                            if (!kPair) mbar_arrive_expect_tx(&sfull[r], b_bytes);
                             else if (ppos == 0) mbar_arrive_expect_tx(&sfull[r], 2u * b_bytes);
                         }
                     }
@@ -601,27 +573,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                         const CUtensorMap* map = part ? mlo : mhi;
                         if constexpr (kPair) {
                             // this CTA's rows: stacked -- part ppos, all N rows; else rows [ppos N/2, (ppos + 1) N/2)
-                            // of both parts.  With two pairs the CTAs at the same position need the same rows: the
-                            // pair-0 CTA copies hi and the pair-1 CTA lo, each multicast to both (stacked: the pair-0
-                            // CTA copies the one part)
+                            // of both parts; the copy counts its bytes on the leader's sfull
                             const bool mine = t.stacked ? part == (int)ppos : true;
                             const int y = t.row0 + (t.stacked ? 0 : (int)ppos * (t.N / 2));
                             const uint32_t dst = slot + (uint32_t)((t.stacked ? 0 : part) * kPairRows * 128);
-                            if (mine) {
-                                if (C == 2) {
-                                    tma_load_2d_pair(dst, map, kt * kBK, y, sfull_leader + (uint32_t)(r * 8));
-                                } else {
-                                    const uint16_t mc = (uint16_t)((1u << ppos) | (1u << (ppos + 2)));
-                                    const int issuer = t.stacked ? 0 : part;  // the pair that issues this copy
-                                    if ((int)(crank >> 1) == issuer) tma_load_2d_mc(dst, map, kt * kBK, y, &sfull[r], mc);
-                                }
-                            }
+                            if (mine) tma_load_2d_pair(dst, map, kt * kBK, y, sfull_leader + (uint32_t)(r * 8));
                         } else {
-                            // in a cluster, CTA 0 copies hi and CTA 1 lo for all (C = 2 or 4), the others only their
-                            // weights
                             const uint32_t dst = slot + (uint32_t)(part ? t.lo_rows * 128 : 0);
-                            if (C == 1) tma_load_2d(dst, map, kt * kBK, t.row0, &sfull[r]);
-                            else if ((int)crank == part) tma_load_2d_mc(dst, map, kt * kBK, t.row0, &sfull[r], cmask);
+                            tma_load_2d(dst, map, kt * kBK, t.row0, &sfull[r]);
                         }
                     }
                     if (++r == depth) {
@@ -633,34 +592,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             if (lane == 0) *total_slot = gs;
             // no copy may still be writing shared memory when the CTA exits (on the abort path nobody has waited
             // for the last slices): wait, bounded, for the last `depth` slices issued
-            // (one pair: the peer's B copies are counted on the leader's sfull, which the leader waits for here before
+            // (pair form: the peer's B copies are counted on the leader's sfull, which the leader waits for here before
             // the final cluster barrier that the peer cannot pass without it)
             if (lane == 0)
                 for (int k = max(0, gs - depth); k < gs; ++k) {
                     mbar_wait(&wfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
-                    if (!kPair || C != 2 || ppos == 0) mbar_wait(&sfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
+                    if (!kPair || ppos == 0) mbar_wait(&sfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
                 }
-        } else if (kPair && C == 4 && warp == 3 && lane == 0) {
-            // ------------------------------------------------------------------ B relay (pair form)
-            // in slice order: once this CTA's B rows of the slice have landed, one arrival on the leader's `ready`
-            const uint32_t ready0 = cluster_addr(&afull[0], leader);
-            int gs = 0, r = 0;
-            uint32_t ph = 0;
-            Item t;
-            for (int item = cid; item < n_items && ok; item += NC) {
-                if (!load_item<kPair>(tiles, item, mgroups, C, crank, p, t)) continue;
-                for (int kt = 0; kt < nk; ++kt, ++gs) {
-                    if (!mbar_wait_cl(&sfull[r], ph, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_cl(ready0 + (uint32_t)(r * sizeof(uint64_t)));
-                    if (++r == depth) {
-                        r = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
         }
         __syncwarp();
     } else if (warp < 16) {
@@ -908,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         // in both CTAs of the pair)
         if constexpr (kPair) mbar_wait_cl(accf, 0, nullptr);
         else mbar_wait(accf, 0, nullptr);
-        if (C > 1 && lane == 0) {
+        if (kPair && lane == 0) {
             // every MMA commit that targets this CTA's slot barriers has arrived (each slot's last phase completes
             // only after all of them): nothing arrives on this CTA's barriers after it leaves
             const int total = *total_slot;
@@ -926,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     }
     // no CTA leaves while another may still copy into its shared memory, arrive on its barriers or (pair form) read
     // its tensor memory
-    if (C > 1) cluster_sync();
+    if (kPair) cluster_sync();
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -983,12 +921,8 @@ cudaError_t launch_form(const ExpertsGemmArgs& a, int64_t max_tiles, int dev, cu
     }
     const int mt = a.a_rows / kBM;
     ExpertsGemmArgs args = a;
-    // clusters share the row tiles through L2 once instead of once per weight slice; they pay off when tiles are
-    // large (L2 bandwidth bounds the product), not for small tiles, whose CTAs would only wait on one another.  The
-    // pair form is a cluster of one pair, or of two pairs that share each row tile by multicast.
-    const bool large = a.b_rows >= (int64_t)kClusterRows * a.n_experts;
-    if (kPair) args.cluster = (large && mt % 4 == 0) ? 4 : 2;
-    else args.cluster = !large ? 1 : (mt % 4 == 0 ? 4 : (mt % 2 == 0 ? 2 : 1));
+    // the pair form is a cluster of one CTA pair; the single form runs without clusters
+    args.cluster = kPair ? 2 : 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;

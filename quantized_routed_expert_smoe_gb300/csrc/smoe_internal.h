@@ -42,7 +42,7 @@ struct ExpertsGemmArgs {
     int64_t b_rows;       // n
     int n_experts;        // E
     bool two_level;       // add every 64-wide K slice into fp32 registers (gate/up); else one accumulator over K
-    int cluster;          // CTAs per cluster sharing a tile's rows (set by the launcher)
+    int cluster;          // CTAs per cluster: 2 (a CTA pair) or 1 (set by the launcher)
     // SwiGLU mode (gate/up with weights packed interleaved): h = silu(gate) * up requantised in the epilogue
     int8_t* hc;           // [b_rows][a_rows / 2] q8 codes of h, or null: fp32 rows to `out`
     uint16_t* hs;         // [b_rows][a_rows / 64] fp16 scales
