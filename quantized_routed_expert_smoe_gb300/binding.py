@@ -325,17 +325,21 @@ class SmoeBlock:
     takes it and the combine adds sigmoid(x . w_sg) times its row.
 
     router: optional bf16 router weights (uint16 / int16 bits [E][H]); the block then computes the router projection
-    itself (smoe_router_topk) and run() ignores its logits argument."""
+    itself (smoe_router_topk) and run() ignores its logits argument.
+
+    fused: run gate/up, SwiGLU and the requantisation as one product (smoe_experts_gateup_swiglu, the gate/up weights
+    packed interleaved); GU is then never written."""
 
     def __init__(self, T: int, H: int, E: int, K: int, F: int, wgu_c, wgu_s, wd_c, wd_s, device="cuda",
-                 shared=None, router=None):
+                 shared=None, router=None, fused=False):
         load_library()
         device_check()
         self.T, self.H, self.E, self.K, self.F = T, H, E, K, F
         dev = torch.device(device)
         as_t = lambda a, dt: torch.as_tensor(a).to(device=dev, dtype=dt).contiguous()
         # the expert weights, packed once for the expert products (the row-major copies are not kept)
-        self.wgu = pack_weights(wgu_c, wgu_s, dev)
+        self.fused = bool(fused)
+        self.wgu = pack_weights(wgu_c, wgu_s, dev, swiglu=self.fused)
         self.wd = pack_weights(wd_c, wd_s, dev)
         n = T * K
         self.n = n
@@ -351,7 +355,7 @@ class SmoeBlock:
         self.xc = e(T, H, dt=torch.int8)
         self.xs = e(T, H // 32, dt=torch.int16)
         self.xop = e(2, max(n, 1), H, dt=torch.float16)  # routed rows, operand form (hi, lo)
-        self.gu = e(n, 2 * F, dt=torch.float32)
+        self.gu = e(0 if self.fused else n, 2 * F, dt=torch.float32)
         self.hc = e(n, F, dt=torch.int8)
         self.hs = e(n, F // 32, dt=torch.int16)
         self.hop = e(2, max(n, 1), F, dt=torch.float16)
@@ -397,8 +401,12 @@ class SmoeBlock:
                    self.work, stream)
         smoe_quantize_q8(x, self.xc, self.xs, stream)
         smoe_gather_q8(self.xc, self.xs, self.src[:self.n], self.xop, stream)
-        smoe_experts_gateup(self.xop, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.gu, stream)
-        smoe_swiglu_requant(self.gu, self.hc, self.hs, self.hop, stream)
+        if self.fused:
+            smoe_experts_gateup_swiglu(self.xop, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.hc,
+                                       self.hs, self.hop, stream)
+        else:
+            smoe_experts_gateup(self.xop, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.gu, stream)
+            smoe_swiglu_requant(self.gu, self.hc, self.hs, self.hop, stream)
         smoe_experts_down(self.hop, self.tiles, self.n, self.E, self.wd, self.H, self.F, self.dm, stream)
         if not self.shared:
             smoe_combine(self.dm, self.slot, self.w, y, stream)
