@@ -15,6 +15,7 @@
 // remainder is exact in fp16); within every group of 16 values position 2j holds value j and position 2j+1 value
 // j+8 (j = 0..7) -- the K order in which the products unpack 2-bit weights in pairs.  SwiGLU writes it for H beside
 // the planar codes; the routed-row gather writes it for the activations of every routed pair.
+#include <climits>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -337,7 +338,11 @@ cudaError_t launch_quantize_q8(const float* x, int64_t rows, int cols, int8_t* c
                                cudaStream_t s) {
     const int64_t n8 = rows * (int64_t)cols / 8;
     if (n8 == 0) return cudaSuccess;
-    quantize_q8_kernel<<<grid_for(n8, 256), 256, 0, s>>>(reinterpret_cast<const float4*>(x), n8, cols,
+    // one group of 8 values a thread and no grid-stride loop: the blocks stream through the SMs as earlier ones
+    // retire, which keeps more loads in flight than a resident grid looping over the rows
+    const int64_t blocks = (n8 + 255) / 256;
+    if (blocks > INT32_MAX) return cudaErrorInvalidValue;
+    quantize_q8_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(x), n8, cols,
                                                         reinterpret_cast<uint2*>(codes), scales);
     return cudaGetLastError();
 }
