@@ -124,6 +124,14 @@ def _stream(stream):
     return ctypes.c_void_p(int(stream))
 
 
+def _as_stream(stream, device):
+    if stream is None:
+        return torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    return torch.cuda.ExternalStream(int(stream), device=device)
+
+
 def _dev(t: torch.Tensor, dtype, name: str):
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
@@ -365,6 +373,7 @@ class SmoeBlock:
         if router is not None:
             self.router = _as_i16(router, dev)
             self.router_work = e(max(router_work_bytes(T, H), 16), dt=torch.uint8)
+        self._side = None  # side stream for the quantisation (created on the first run)
         self.shared = shared is not None
         if self.shared:
             lift = lambda a: a[None] if a.ndim == 2 else a  # one expert: [rows][..] -> [1][rows][..]
@@ -391,15 +400,27 @@ class SmoeBlock:
             self.sg = e(max(T, 4), dt=torch.float32)
 
     def run(self, logits, x, stream=None, out=None):
-        """y = the block on (logits [T][E], x [T][H]); into `out` (fp32 [T][H] on the device) when given."""
+        """y = the block on (logits [T][E], x [T][H]); into `out` (fp32 [T][H] on the device) when given.
+
+        The q8 quantisation of x depends on neither the routing nor the grouping, so it runs on a side stream beside
+        them (forked from and joined back into `stream` with events; the same holds inside a CUDA-graph capture)."""
         y = self.y if out is None else out
+        main = _as_stream(stream, x.device)
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=x.device)
+            self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
+        self._fork.record(main)
+        self._side.wait_event(self._fork)
+        smoe_quantize_q8(x, self.xc, self.xs, self._side)
+        self._join.record(self._side)
         if self.router is not None:
-            smoe_router_topk(x, self.router, self.ids, self.w, self.router_work, stream)
+            smoe_router_topk(x, self.router, self.ids, self.w, self.router_work, main)
         else:
-            smoe_route_topk(logits, self.ids, self.w, stream)
+            smoe_route_topk(logits, self.ids, self.w, main)
         smoe_group(self.ids, self.E, self.counts, self.offsets, self.src[:self.n], self.slot[:self.n], self.tiles,
-                   self.work, stream)
-        smoe_quantize_q8(x, self.xc, self.xs, stream)
+                   self.work, main)
+        main.wait_event(self._join)
+        stream = main
         smoe_gather_q8(self.xc, self.xs, self.src[:self.n], self.xop, stream)
         if self.fused:
             smoe_experts_gateup_swiglu(self.xop, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.hc,
@@ -420,6 +441,15 @@ class SmoeBlock:
         smoe_combine_shared(self.dm, self.slot, self.w, self.ds, self.sg[:T], y, stream)
         return y
 
+    def capture(self, logits, x, out=None):
+        """A CUDA graph of one run() on these device inputs (their buffers, read again at every replay): replaying it
+        issues the block's kernels without the host's per-launch cost.  run() must have been called once before (the
+        libraries' one-time set-up per device is not captured)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(logits, x, out=out)
+        return g
+
     def device_status(self):
         """(group status, kernel status) from the tiles header; reads the device (synchronises)."""
         h = self.tiles[:4].cpu().tolist()
@@ -434,9 +464,13 @@ class SmoePipeline:
     start(event): the copies of the first step wait for `event` (e.g. recorded on the compute stream before a timed
     region); submit(h_logits, h_x, h_y) queues one step -- h_y (pinned fp32 [T][H]) holds the result once the step's
     copy back has completed; drain(): the compute stream waits for every queued copy back; synchronize(): the host
-    waits for all of it."""
+    waits for all of it.
 
-    def __init__(self, block: "SmoeBlock", stream=None):
+    graphs=True: each of the two device buffer sets gets a CUDA graph of the block's run() on it (captured here; the
+    block must have run once before), and a step replays its set's graph instead of launching the kernels one by
+    one."""
+
+    def __init__(self, block: "SmoeBlock", stream=None, graphs=False):
         self.blk = block
         dev = block.y.device
         T, H, E = block.T, block.H, block.E
@@ -451,6 +485,10 @@ class SmoePipeline:
         self.ev_done = [torch.cuda.Event(), torch.cuda.Event()]  # slot b's step has computed
         self.ev_out = [torch.cuda.Event(), torch.cuda.Event()]   # slot b's output is back on the host
         self.i = 0
+        self.graphs = None
+        if graphs:
+            torch.cuda.synchronize(dev)
+            self.graphs = [block.capture(self.d_logits[b], self.d_x[b], out=self.d_y[b]) for b in range(2)]
 
     def start(self, event):
         self.copy_in.wait_event(event)
@@ -468,7 +506,11 @@ class SmoePipeline:
         self.compute.wait_event(self.ev_in[b])
         if self.i >= 2:
             self.compute.wait_event(self.ev_out[b])  # slot b's previous output is back on the host
-        self.blk.run(self.d_logits[b], self.d_x[b], stream=self.compute, out=self.d_y[b])
+        if self.graphs is not None:
+            with torch.cuda.stream(self.compute):
+                self.graphs[b].replay()
+        else:
+            self.blk.run(self.d_logits[b], self.d_x[b], stream=self.compute, out=self.d_y[b])
         self.ev_done[b].record(self.compute)
         with torch.cuda.stream(self.copy_out):
             self.copy_out.wait_event(self.ev_done[b])

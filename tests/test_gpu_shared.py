@@ -96,8 +96,10 @@ def test_block_with_shared_expert(B, name):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("with_shared,with_router", [(False, False), (True, False), (True, True)])
-def test_pipeline_matches_run(B, with_shared, with_router):
+@pytest.mark.parametrize("with_shared,with_router,graphs", [(False, False, False), (True, False, False),
+                                                             (True, True, False), (False, False, True),
+                                                             (True, True, True)])
+def test_pipeline_matches_run(B, with_shared, with_router, graphs):
     # SmoePipeline (host in, host out, copies overlapped with the neighbouring steps' compute) gives every step's
     # output bit for bit as the plain run on device inputs, over more steps than it has buffers
     cfg = synth.CONFIGS["tiny"]
@@ -112,7 +114,7 @@ def test_pipeline_matches_run(B, with_shared, with_router):
     xs = [synth.make_rows(cfg.T, cfg.H, seed=40 + s) for s in range(steps)]
     lgs = [synth.make_rows(cfg.T, cfg.E, seed=50 + s, scale=0.5) for s in range(steps)]
     want = [host(blk.run(dev(lgs[s]), dev(xs[s]))).copy() for s in range(steps)]
-    pipe = B.SmoePipeline(blk)
+    pipe = B.SmoePipeline(blk, graphs=graphs)  # (graphs: each buffer set's run() captured, then replayed)
     # a block with its own router projection takes no logits: the pipeline copies none
     h_in = [(None if with_router else torch.from_numpy(lgs[s]).pin_memory(), torch.from_numpy(xs[s]).pin_memory())
             for s in range(steps)]
