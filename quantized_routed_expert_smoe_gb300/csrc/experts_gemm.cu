@@ -87,8 +87,9 @@ constexpr int kBK = 64;                        // K values per slice: one 128-by
 constexpr int kMaxBN = SMOE_TILE_ROWS;         // routed rows per tile (MMA N <= 224)
 constexpr int kThreads = 640;                  // five warpgroups
 constexpr int kPromoters = 384;                // warpgroups 1-3
-constexpr int kConverters = 128;               // warpgroup 4
+constexpr int kConverters = 128;               // warpgroup 4 (a weight row a thread)
 constexpr int kMaxRing = 8;                    // slices in flight at most
+constexpr int kMmaThreads = 2;                 // MMA-issuing threads (warps 0, 2): slice groups in turn
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACols = 32;                // one slice of A: 128 lanes x 64 fp16
 constexpr int kMaxA = 8;                       // A buffers at most
@@ -98,13 +99,14 @@ constexpr int kSmemBytes = 232448;             // the per-CTA maximum (227 KB): 
 constexpr int kBarBytes = 512;
 constexpr int kScratchBytes = SMOE_TILE_ROWS * 4 * 4;  // SwiGLU epilogue: a warp's block amax per column [col][4]
 constexpr int kRingBytes = kSmemBytes - 1024 - kBarBytes - kScratchBytes;
-// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 gives back to 40, the converters
-// to 56 and the promoters take 128: 128 x 40 + 384 x 128 + 128 x 56 = 61,440.  Per SM sub-partition (one warp of
-// each warpgroup): 32 x (40 + 3 x 128 + 56) = 15,360 <= 16,384.
-constexpr int kRegsWg0 = 40;
-constexpr int kRegsConv = 56;
+// registers: launched at 96 a thread (640 x 96 = 61,440 of 65,536); warpgroup 0 and the converters give back to 48,
+// the promoters take 128: 128 x 48 + 128 x 48 + 384 x 128 = 61,440.  Per SM sub-partition (one warp of each
+// warpgroup): 32 x (48 + 48 + 3 x 128) = 15,360 <= 16,384.
+constexpr int kRegsLaunch = 96;
+constexpr int kRegsWg0 = 48;
+constexpr int kRegsConv = 48;
 constexpr int kRegsProm = 128;
-static_assert(128 * kRegsWg0 + kConverters * kRegsConv + kPromoters * kRegsProm <= kThreads * 96,
+static_assert(128 * kRegsWg0 + kConverters * kRegsConv + kPromoters * kRegsProm <= kThreads * kRegsLaunch,
               "register split exceeds the launch");
 static_assert(kMaxBN <= 224 && kMaxBN % 32 == 0, "two partial buffers and two A buffers must fit in tensor memory");
 static_assert(kMaxBN % 96 == 0, "the promoter warpgroups take whole 32-column chunks in turn");
@@ -202,17 +204,6 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cl(uint32_t addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem desc]^T over a CTA pair: M = 256 (A rows 0-127 and D in this CTA's tensor memory,
-// rows 128-255 in the peer's at the same address), B's first N/2 rows from this CTA's shared memory and the rest from
-// the peer's at the same address.  Issued by one thread of the pair's even CTA.
-__device__ __forceinline__ void mma_f16_ta_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                                uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 // arrive once on `bar` in every CTA of `mask` when the pair MMAs issued so far by this thread have completed
 __device__ __forceinline__ void mma_commit_pair_mc(uint64_t* bar, uint16_t mask) {
     asm volatile(
@@ -275,15 +266,53 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, fp16 operands, fp32 accumulate; issued by one thread.
-__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+// One 64-wide K slice of MMAs (four K16 steps), issued back to back from one asm block: A columns a + 8 k and B
+// descriptor b + 2 k (its start address 32 bytes further along the 128-byte swizzled rows) for step k; accumulate
+// 0 starts the accumulator at step 0.  The issuing thread runs in order and each tensor-core instruction holds it
+// for tens of cycles, so the operand arithmetic comes first and the MMAs follow without anything between them.
+// kGroup: 2 = the pair form (cta_group::2), 1 = one CTA.
+#define SMOE_MMA_SLICE4(GROUP)                                                                                      \
+    "{\n\t.reg .pred p, t;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"                                  \
+    "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, %3, %3;\n\t"                                                           \
+    "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"                                        \
+    "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"                                           \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [%1], %2, %3, p;\n\t"                                         \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], b1, %3, t;\n\t"                                         \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a2], b2, %3, t;\n\t"                                         \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a3], b3, %3, t;\n\t}"
+template <int kGroup>
+__device__ __forceinline__ void mma_slice4(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    if constexpr (kGroup == 2)
+        asm volatile(SMOE_MMA_SLICE4("2")::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
+    else
+        asm volatile(SMOE_MMA_SLICE4("1")::"r"(d), "r"(a), "l"(b), "r"(idesc), "r"(accumulate) : "memory");
 }
+#undef SMOE_MMA_SLICE4
+// The same with both parts of the row operand: per step k, the hi rows (descriptor bh + 2 k) then the lo rows
+// (bl + 2 k) into the same accumulator.
+#define SMOE_MMA_SLICE8(GROUP)                                                                                      \
+    "{\n\t.reg .pred p, t;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 h1, h2, h3, l1, l2, l3;\n\t"                     \
+    "setp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 t, %4, %4;\n\t"                                                           \
+    "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\t"                                        \
+    "add.u64 h1, %2, 2;\n\tadd.u64 h2, %2, 4;\n\tadd.u64 h3, %2, 6;\n\t"                                           \
+    "add.u64 l1, %3, 2;\n\tadd.u64 l2, %3, 4;\n\tadd.u64 l3, %3, 6;\n\t"                                           \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [%1], %2, %4, p;\n\t"                                         \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [%1], %3, %4, t;\n\t"                                         \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], h1, %4, t;\n\t"                                         \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a1], l1, %4, t;\n\t"                                         \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a2], h2, %4, t;\n\t"                                         \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a2], l2, %4, t;\n\t"                                         \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a3], h3, %4, t;\n\t"                                         \
+    "tcgen05.mma.cta_group::" GROUP ".kind::f16 [%0], [a3], l3, %4, t;\n\t}"
+template <int kGroup>
+__device__ __forceinline__ void mma_slice8(uint32_t d, uint32_t a, uint64_t bh, uint64_t bl, uint32_t idesc,
+                                           uint32_t accumulate) {
+    if constexpr (kGroup == 2)
+        asm volatile(SMOE_MMA_SLICE8("2")::"r"(d), "r"(a), "l"(bh), "l"(bl), "r"(idesc), "r"(accumulate) : "memory");
+    else
+        asm volatile(SMOE_MMA_SLICE8("1")::"r"(d), "r"(a), "l"(bh), "l"(bl), "r"(idesc), "r"(accumulate) : "memory");
+}
+#undef SMOE_MMA_SLICE8
 
 // (a0, a1) += (p0, p1), each rounded to nearest (packed fp32x2 add)
 __device__ __forceinline__ void add2(float& a0, float& a1, uint32_t p0, uint32_t p1) {
@@ -293,15 +322,24 @@ __device__ __forceinline__ void add2(float& a0, float& a1, uint32_t p0, uint32_t
         : "r"(p0), "r"(p1));
 }
 
-// 16 weights (codes: value i at bits 2i..2i+1) as 8 TMEM columns of fp16 pairs (value m, value m+8): d * (q - 2)
+// 16 weights (codes: value i at bits 2i..2i+1) as 8 TMEM columns of fp16 pairs (value m, value m+8): d * (q - 2).
+// Pair m's codes sit at bits 2m of each 16-bit half.  OR-ed under the exponent of 2^(10 - 2m) they read as the fp16
+// value 2^(10 - 2m) + q exactly (a mantissa bit at position 2m weighs 2^(10 - 2m - 10 + 2m) = 1), so pairs 0-4 need
+// no shift; pairs 5-7 take the word shifted by 10 (their codes at bits 0, 2, 4).  Subtracting 2^e + 2 leaves q - 2
+// exactly, and the product with d is exact in fp16.
+__device__ __forceinline__ uint32_t decode_pair(uint32_t codes, int pos, __half2 d2) {
+    const int e = 10 - 2 * pos;
+    const uint32_t expo = (uint32_t)(e + 15) << 10;
+    const uint32_t v = (codes & (0x00030003u << (2 * pos))) | (expo | (expo << 16));
+    const __half2 base = __float2half2_rn((float)((1 << e) + 2));
+    return h2_as_u32(__hmul2(__hsub2(u32_as_h2(v), base), d2));
+}
 __device__ __forceinline__ void decode_weights16(uint32_t codes, __half2 d2, uint32_t* col) {
-    const __half2 k1026 = __float2half2_rn(1026.0f);
+    const uint32_t high = codes >> 10;
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        // values m and m+8 as fp16 1024 + q in the two halves, then (1024 + q - 1026) * d = d * (q - 2)
-        const uint32_t v = ((codes >> (2 * m)) & 0x00030003u) | 0x64006400u;
-        col[m] = h2_as_u32(__hmul2(__hsub2(u32_as_h2(v), k1026), d2));
-    }
+    for (int m = 0; m < 5; ++m) col[m] = decode_pair(codes, m, d2);
+#pragma unroll
+    for (int m = 5; m < 8; ++m) col[m] = decode_pair(high, m - 5, d2);
 }
 
 struct GemmMaps {
@@ -357,11 +395,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     if (tiles[1] != 0) return;  // the grouping failed: nothing to do (the same answer in every CTA)
     const int n_tiles = tiles[0];
     const int nk = p.K / kBK;  // slices of an item
-    // two MMA threads take alternate groups of G slices.  Two-level: a partial per pair of slices (G = 2; K is a
-    // multiple of 128 there); else one partial per thread of an item (G = 1: slices kt, kt + 2, ... of one parity),
-    // summed by the promoters
-    const int G = p.two_level ? 2 : 1;
-    const int pitem = p.two_level ? nk / 2 : min(2, nk);  // partials an item
+    // A stage is S consecutive slices (pair form: S = 2, K a multiple of 128; single form: S = 1) with one set of
+    // ring barriers: one wait of the MMA thread, one commit, one arrival of each converter warp for S slices' work.
+    constexpr int S = kPair ? 2 : 1;
+    const int nsi = nk / S;  // stages of an item
+    // two MMA threads take alternate groups of Gs stages.  Two-level: a partial per 128 values of K (Gs = 2 / S
+    // stages); else one partial per thread of an item (Gs = 1: stages ks, ks + 2, ... of one parity), summed by the
+    // promoters
+    const int Gs = p.two_level ? 2 / S : 1;
+    const int pitem = p.two_level ? nk / 2 : min(kMmaThreads, nsi);  // partials an item
 
     // persistent: cluster cid of NC takes items cid, cid + NC, ...; its CTAs take the C weight slices of an item
     // (pair form: a cluster is one pair; single form: one CTA)
@@ -381,29 +423,33 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     // the single form: as many ring slots as A buffers (its slots are large); the pair form: twice as many (its slots
     // hold half the B rows), so that twice the slices are in flight against the ring's chain of latencies
     constexpr int depth = kPair ? 2 * na : na;
+    constexpr int nst = depth / S;  // stage slots of the ring (stage slot j: ring slots S j .. S j + S - 1)
+    static_assert(depth % S == 0 && na % S == 0, "whole stages");
     constexpr uint32_t part_base = (uint32_t)na * kACols;
     constexpr int nbuf = ((int)kTmemCols - (int)part_base) / kMaxBN;
     static_assert(na >= 2 && na <= kMaxA && nbuf >= 2 && nbuf <= kMaxBufs, "tensor-memory split");
     static_assert(depth <= kMaxRing && depth <= kMaxA && depth * sbytes <= kRingBytes, "ring");
-    // slice gs uses ring slot gs mod depth and A buffer gs mod na.  Single form (depth == na): its copies can land
+    // slice gs uses ring slot gs mod depth and A buffer gs mod na; its stage gs / S uses stage slot (gs / S) mod nst,
+    // whose barriers it shares with the other slices of the stage.  Single form (depth == na): its copies can land
     // only after the producer has seen the slot's previous slice (gs - depth) released by the MMA commits, which
     // follow that slice's MMAs, the last readers of the A buffer, so "weights landed" also means "A buffer free".
-    // Pair form (depth == 2 na): the converters also wait for the release of slice gs - na, the previous user of the
-    // A buffer, before they overwrite it
+    // Pair form (depth == 2 na): the converters also wait for the release of stage gs / S - na / S, the previous user
+    // of the stage's A buffers, before they overwrite them
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t* ring = smem_raw + pad;
-    uint64_t* sfull = reinterpret_cast<uint64_t*>(smem_raw + kSmemBytes - kBarBytes);  // slot r's B tiles [kMaxRing]
-    uint64_t* wfull = sfull + kMaxRing;     // slot r's packed weight block landed [kMaxRing]
-    uint64_t* sempty = wfull + kMaxRing;    // the MMAs and the converters are done with slot r [kMaxRing]
-    uint64_t* afull = sempty + kMaxRing;    // A buffer a decoded [kMaxA]; pair form (leader): slot a's A and B ready
+    // (indexed by stage slot)
+    uint64_t* sfull = reinterpret_cast<uint64_t*>(smem_raw + kSmemBytes - kBarBytes);  // the stage's B tiles [nst]
+    uint64_t* wfull = sfull + kMaxRing;     // the stage's packed weight blocks landed [nst]
+    uint64_t* sempty = wfull + kMaxRing;    // the MMAs and the converters are done with the stage's slots [nst]
+    uint64_t* afull = sempty + kMaxRing;    // the stage's A buffers decoded [nst] (pair form: on the leader)
     uint64_t* pfull = afull + kMaxA;        // partial in tensor-memory buffer b is complete [kMaxBufs]
     uint64_t* pempty = pfull + kMaxBufs;    // the promoters have added buffer b into their registers [kMaxBufs]
     uint64_t* accf = pempty + kMaxBufs;     // every MMA has completed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* total_slot = const_cast<int*>(abort_flag + 1);  // slices this CTA ran (for the teardown)
+    int* total_slot = const_cast<int*>(abort_flag + 1);  // stages this CTA ran (for the teardown)
     float* scratch = reinterpret_cast<float*>(smem_raw + kSmemBytes - kBarBytes - kScratchBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -422,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             mbar_init(&pfull[b], 1);
             mbar_init(&pempty[b], kPair ? 2 * (kPromoters / 32) : kPromoters);
         }
-        mbar_init(accf, 2);  // one final commit of each MMA thread
+        mbar_init(accf, kMmaThreads);  // one final commit of each MMA thread
         *abort_flag = 0;
         *total_slot = 0;
         fence_mbar_init();
@@ -442,81 +488,71 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t ring_s = smem_u32(ring);
+    const uint64_t desc_ring = sdesc_k_sw128(ring_s);  // slot r's hi rows: + (r * sbytes) >> 4
     bool ok = true;
 
     if (warp < 4) {
         setmaxnreg_dec<kRegsWg0>();
-        if ((warp == 0 || warp == 2) && lane == 0 && (!kPair || ppos == 0)) {
+        if ((warp == 0 || (kMmaThreads == 2 && warp == 2)) && lane == 0 && (!kPair || ppos == 0)) {
             // ------------------------------------------------------------------ MMA issue (two threads)
             // stream st issues the global slices of groups st, st + 2, ... (slice gs: ring slot gs mod depth, A buffer
             // gs mod na -- both powers of two --, the slot's hi and lo tiles, the slice's partial buffer); the other
             // thread's waits overlap this one's MMAs.  The item's first slice and its partial index advance by
             // counting (a division by a runtime value costs tens of cycles on this thread's critical path).
             const int st = warp >> 1;
-            int gs = st * G, base = 0, seq = 0;  // this thread's next global slice; the item's first; items done
+            int gst = st * Gs, sbase = 0, seq = 0;  // this thread's next global stage; the item's first; items done
             Item t;
             for (int item = cid; item < n_items && ok; item += NC) {
                 if (!load_item<kPair>(tiles, item, mgroups, C, crank, p, t)) continue;
                 const uint32_t idesc = idesc_f16_f32(kPair ? 2 * kBM : kBM, t.ncols);
-                for (; gs < base + nk && ok; gs += (G == 1 || (gs & 1)) ? G + 1 : 1) {
-                    const int kt = gs - base;
-                    const int r = gs % depth, ab = gs % na;
-                    const uint32_t aph = (uint32_t)(gs / depth) & 1u;  // parity of slot r's barriers for slice gs
-                    // the slice's partial: one per pair of slices (two-level), else the item's partial kt mod 2
-                    const int gp = seq * pitem + (p.two_level ? kt >> 1 : (pitem == 2 ? (kt & 1) : 0));
+                for (; gst < sbase + nsi && ok; gst += (Gs == 1 || (gst & 1)) ? (kMmaThreads - 1) * Gs + 1 : 1) {
+                    const int ks = gst - sbase;  // the stage within the item
+                    const int j = gst % nst;
+                    const uint32_t aph = (uint32_t)(gst / nst) & 1u;  // parity of stage slot j's barriers for it
+                    // the stage's partial: one per 128 values of K (two-level), else the item's partial of this thread
+                    const int gp = seq * pitem + (p.two_level ? ks / Gs : (pitem == 2 ? (ks & 1) : 0));
                     const int b = gp % nbuf;
-                    const bool first = p.two_level ? (kt & 1) == 0 : kt < 2;
-                    const bool last = p.two_level ? (kt & 1) == 1 : kt + 2 >= nk;
-                    // A decoded and the slot's B tiles landed (slot r = A buffer ab: the same phase); a slice that
-                    // starts a partial in a buffer used before also needs the promoters to have taken the previous
-                    // partial there (partial gp - nbuf: phase gp / nbuf - 1 of its pempty).  The waits overlap.
+                    const bool first = p.two_level ? ks % Gs == 0 : ks < kMmaThreads;
+                    const bool last = p.two_level ? ks % Gs == Gs - 1 : ks + kMmaThreads >= nsi;
+                    // A decoded and the stage's B tiles landed; a stage that starts a partial in a buffer used before
+                    // also needs the promoters to have taken the previous partial there (partial gp - nbuf: phase
+                    // gp / nbuf - 1 of its pempty).  The waits overlap.  (Pair form: both CTAs' converters arrive on
+                    // the leader's afull and both CTAs' B bytes land on its sfull.)
                     const bool reuse = first && gp >= nbuf;
                     const uint32_t eph = reuse ? (uint32_t)(gp / nbuf - 1) & 1u : aph;
-                    // (pair form: the A barrier is the slot's, and both CTAs' B bytes land on this CTA's sfull)
-                    const int ai = kPair ? r : ab;
-                    if (!mbar_wait3(&afull[ai], aph, &sfull[r], aph, reuse ? &pempty[b] : &afull[ai], eph, abort_flag)) {
+                    // the stage's operands, before the wait (its round trip hides this arithmetic)
+                    const uint32_t d = tmem + part_base + (uint32_t)(b * kMaxBN);
+                    const int g0 = gst * S;  // the stage's first global slice
+                    uint64_t bh[S], bl[S];
+                    uint32_t a[S];
+#pragma unroll
+                    for (int q = 0; q < S; ++q) {
+                        bh[q] = desc_ring + (uint64_t)((((g0 + q) % depth) * sbytes) >> 4);
+                        bl[q] = bh[q] + (uint64_t)(t.lo_rows * (128 >> 4));
+                        a[q] = tmem + (uint32_t)((g0 + q) % na) * kACols;
+                    }
+                    const uint32_t acc = first ? 0u : 1u;
+                    if (!mbar_wait3(&afull[j], aph, &sfull[j], aph, reuse ? &pempty[b] : &afull[j], eph, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t hi = ring_s + (uint32_t)(r * sbytes), lo = hi + (uint32_t)(t.lo_rows * 128);
-                    const uint32_t d = tmem + part_base + (uint32_t)(b * kMaxBN);
-                    const uint32_t a = tmem + (uint32_t)ab * kACols;
-                    if (t.stacked) {
-                        // pair form: the leader's slot holds the N hi rows and the peer's the N lo rows (at the same
-                        // offset), i.e. the MMA's columns [0, N) and [N, 2N)
+                    // a stacked tile: one MMA of 2N columns a step (pair form: the leader's slot holds the N hi rows
+                    // and the peer's the N lo rows at the same offset, i.e. columns [0, N) and [N, 2N))
 #pragma unroll
-                        for (int k16 = 0; k16 < 4; ++k16) {
-                            if constexpr (kPair)
-                                mma_f16_ta_pair(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
-                                                (first && k16 == 0) ? 0u : 1u);
-                            else
-                                mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
-                                           (first && k16 == 0) ? 0u : 1u);
-                        }
-                    } else {
-#pragma unroll
-                        for (int k16 = 0; k16 < 4; ++k16) {
-                            if constexpr (kPair) {
-                                mma_f16_ta_pair(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
-                                                (first && k16 == 0) ? 0u : 1u);
-                                mma_f16_ta_pair(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
-                            } else {
-                                mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(hi + 32 * k16), idesc,
-                                           (first && k16 == 0) ? 0u : 1u);
-                                mma_f16_ta(d, a + 8u * (uint32_t)k16, sdesc_k_sw128(lo + 32 * k16), idesc, 1u);
-                            }
-                        }
+                    for (int q = 0; q < S; ++q) {
+                        if (t.stacked) mma_slice4<C>(d, a[q], bh[q], idesc, q == 0 ? acc : 1u);
+                        else mma_slice8<C>(d, a[q], bh[q], bl[q], idesc, q == 0 ? acc : 1u);
                     }
                     if constexpr (kPair) {
-                        mma_commit_pair_mc(&sempty[r], pmask);  // slot r free in both CTAs
+                        mma_commit_pair_mc(&sempty[j], pmask);  // the stage's slots free in both CTAs
                         if (last) mma_commit_pair_mc(&pfull[b], pmask);
                     } else {
-                        mma_commit(&sempty[r]);
+                        mma_commit(&sempty[j]);
                         if (last) mma_commit(&pfull[b]);
                     }
                 }
-                base += nk;
+                sbase += nsi;
                 ++seq;
             }
             // completes once every MMA issued above has completed (abort path included)
@@ -529,8 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 const CUtensorMap* m = lane < kNumMaps ? &maps.hi[lane] : &maps.lo[lane - kNumMaps];
                 asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
             }
-            int gs = 0, r = 0;
-            uint32_t eph = 0;  // parity of the sempty phase the next wrap waits for
+            int gs = 0;
             const uint32_t sfull_leader = kPair ? cluster_addr(&sfull[0], leader) : 0u;
             Item t;
             for (int item = cid; item < n_items && ok; item += NC) {
@@ -543,31 +578,37 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 const CUtensorMap* const mhi = &maps.hi[t.map];
                 const CUtensorMap* const mlo = &maps.lo[t.map];
                 for (int kt = 0; kt < nk; ++kt, ++gs) {
-                    bool go = true;
-                    if (lane == 0) {
-                        bool free_ = true;
-                        if (gs >= depth) {
-                            if constexpr (kPair) free_ = mbar_wait_cl(&sempty[r], eph, abort_flag);
-                            else free_ = mbar_wait(&sempty[r], eph, abort_flag);
+                    const int gst = gs / S, j = gst % nst, r = gs % depth;
+                    if (gs % S == 0) {
+                        // a new stage: its slots free (the MMA commits of stage gst - nst and its converters), then
+                        // its barriers armed for all S slices' bytes
+                        bool go = true;
+                        if (lane == 0) {
+                            bool free_ = true;
+                            if (gst >= nst) {
+                                const uint32_t eph = (uint32_t)(gst / nst - 1) & 1u;
+                                if constexpr (kPair) free_ = mbar_wait_cl(&sempty[j], eph, abort_flag);
+                                else free_ = mbar_wait(&sempty[j], eph, abort_flag);
+                            }
+                            if (!free_) go = false;
+                            else {
+                                mbar_arrive_expect_tx(&wfull[j], (uint32_t)(S * kWBlock));
+                                // pair form: the leader's sfull counts both CTAs' B bytes; the peer arms none
+                                if (!kPair) mbar_arrive_expect_tx(&sfull[j], (uint32_t)S * b_bytes);
+                                else if (ppos == 0) mbar_arrive_expect_tx(&sfull[j], 2u * (uint32_t)S * b_bytes);
+                            }
                         }
-                        if (!free_) go = false;
-                        else {
-                            mbar_arrive_expect_tx(&wfull[r], (uint32_t)kWBlock);
-                            // pair form: the leader's sfull counts both CTAs' B bytes; the peer arms none
-                            if (!kPair) mbar_arrive_expect_tx(&sfull[r], b_bytes);
-                            else if (ppos == 0) mbar_arrive_expect_tx(&sfull[r], 2u * b_bytes);
+                        if (!__shfl_sync(0xffffffffu, go, 0)) {
+                            ok = false;
+                            break;
                         }
-                    }
-                    if (!__shfl_sync(0xffffffffu, go, 0)) {
-                        ok = false;
-                        break;
                     }
                     const uint32_t slot = ring_s + (uint32_t)(r * sbytes);
                     // lane 0 the weights (on their own barrier: the converters need nothing else), lanes 1 and 2 the
                     // hi and lo boxes
                     if (lane == 0)
                         bulk_load(slot + (uint32_t)(kPair ? kPairWOfs : 2 * t.lo_rows * 128),
-                                  wblocks + (int64_t)kt * kWBlock, kWBlock, &wfull[r]);
+                                  wblocks + (int64_t)kt * kWBlock, kWBlock, &wfull[j]);
                     const int part = lane - 1;
                     if (part == 0 || part == 1) {
                         const CUtensorMap* map = part ? mlo : mhi;
@@ -577,28 +618,26 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                             const bool mine = t.stacked ? part == (int)ppos : true;
                             const int y = t.row0 + (t.stacked ? 0 : (int)ppos * (t.N / 2));
                             const uint32_t dst = slot + (uint32_t)((t.stacked ? 0 : part) * kPairRows * 128);
-                            if (mine) tma_load_2d_pair(dst, map, kt * kBK, y, sfull_leader + (uint32_t)(r * 8));
+                            if (mine) tma_load_2d_pair(dst, map, kt * kBK, y, sfull_leader + (uint32_t)(j * 8));
                         } else {
                             const uint32_t dst = slot + (uint32_t)(part ? t.lo_rows * 128 : 0);
-                            tma_load_2d(dst, map, kt * kBK, t.row0, &sfull[r]);
+                            tma_load_2d(dst, map, kt * kBK, t.row0, &sfull[j]);
                         }
-                    }
-                    if (++r == depth) {
-                        r = 0;
-                        if (gs >= depth) eph ^= 1u;
                     }
                 }
             }
-            if (lane == 0) *total_slot = gs;
+            if (lane == 0) *total_slot = gs / S;
             // no copy may still be writing shared memory when the CTA exits (on the abort path nobody has waited
-            // for the last slices): wait, bounded, for the last `depth` slices issued
+            // for the last stages): wait, bounded, for the last `nst` stages issued
             // (pair form: the peer's B copies are counted on the leader's sfull, which the leader waits for here before
             // the final cluster barrier that the peer cannot pass without it)
-            if (lane == 0)
-                for (int k = max(0, gs - depth); k < gs; ++k) {
-                    mbar_wait(&wfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
-                    if (!kPair || ppos == 0) mbar_wait(&sfull[k % depth], (uint32_t)(k / depth) & 1u, nullptr);
+            if (lane == 0) {
+                const int stages = gs / S;
+                for (int k = max(0, stages - nst); k < stages; ++k) {
+                    mbar_wait(&wfull[k % nst], (uint32_t)(k / nst) & 1u, nullptr);
+                    if (!kPair || ppos == 0) mbar_wait(&sfull[k % nst], (uint32_t)(k / nst) & 1u, nullptr);
                 }
+            }
         }
         __syncwarp();
     } else if (warp < 16) {
@@ -780,29 +819,31 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         const uint32_t lane_base = (uint32_t)(ct & ~31) << 16;
         // pair form: a converter warp arrives once on the leader's `ready` when all its lanes' stores are done
         const uint32_t ready0 = kPair ? cluster_addr(&afull[0], leader) : 0u;
-        int r = 0;           // the slice's ring slot (single form: also its A buffer)
-        uint32_t rph = 0;    // that slot's wfull parity
         int gs = 0;          // the slice's global index
-        bool ready = false;  // its copies are known to have landed (tested while the previous slice was stored)
+        bool ready = false;  // the stage's copies are known to have landed (tested while the last stage was stored)
         Item t;
         for (int item = cid; item < n_items && ok; item += NC) {
             if (!load_item<kPair>(tiles, item, mgroups, C, crank, p, t)) continue;
             const int wofs = kPair ? kPairWOfs : 2 * t.lo_rows * 128;  // the packed weight block within a slot
             for (int kt = 0; kt < nk && ok; ++kt, ++gs) {
-                if (!ready && !mbar_wait(&wfull[r], rph, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                if constexpr (kPair) {
-                    // the A buffer's previous slice (gs - na) has been released by its MMAs' commits
-                    const int pg = gs - na;
-                    if (pg >= 0 && !mbar_wait(&sempty[pg % depth], (uint32_t)(pg / depth) & 1u, abort_flag)) {
+                const int gst = gs / S, j = gst % nst, r = gs % depth;
+                if (gs % S == 0) {
+                    // a new stage: all its weight blocks landed
+                    if (!ready && !mbar_wait(&wfull[j], (uint32_t)(gst / nst) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
+                    if constexpr (kPair) {
+                        // the stage's A buffers were last read by stage gst - na / S: released by its MMAs' commit
+                        const int pg = gst - na / S;
+                        if (pg >= 0 && !mbar_wait(&sempty[pg % nst], (uint32_t)(pg / nst) & 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    tc_fence_after();
                 }
-                tc_fence_after();
-                const int ab = kPair ? gs % na : r;
+                const int ab = gs % na;
                 const uint8_t* wb = ring + r * sbytes + wofs;
                 const uint4 codes = *reinterpret_cast<const uint4*>(wb + ct * 16);
                 const __half2 sc = *reinterpret_cast<const __half2*>(wb + 2048 + ct * 4);
@@ -813,25 +854,23 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 decode_weights16(codes.z, __high2half2(sc), col);
                 decode_weights16(codes.w, __high2half2(sc), col + 8);
                 tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols + 16u, col);
-                const int rn = r + 1 == depth ? 0 : r + 1;
-                const uint32_t rphn = r + 1 == depth ? rph ^ 1u : rph;
-                // the next global slice (of this item or the next) uses slot rn: test its barrier while the stores
-                // complete, so that a slice whose weights have landed costs no wait round trip
-                ready = mbar_test(smem_u32(&wfull[rn]), rphn);
-                tmem_st_wait();
-                tc_fence_before();
-                if constexpr (kPair) {
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive_cl(ready0 + (uint32_t)(r * sizeof(uint64_t)));
-                        mbar_arrive(&sempty[r]);
+                if (gs % S == S - 1) {
+                    // the stage's last slice: test the next stage's barrier while the stores complete (a stage whose
+                    // weights have landed then costs no wait round trip), then signal the stage
+                    ready = mbar_test(smem_u32(&wfull[(gst + 1) % nst]), (uint32_t)((gst + 1) / nst) & 1u);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    if constexpr (kPair) {
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive_cl(ready0 + (uint32_t)(j * sizeof(uint64_t)));
+                            mbar_arrive(&sempty[j]);
+                        }
+                    } else {
+                        mbar_arrive(&afull[j]);
+                        mbar_arrive(&sempty[j]);
                     }
-                } else {
-                    mbar_arrive(&afull[r]);
-                    mbar_arrive(&sempty[r]);
                 }
-                r = rn;
-                rph = rphn;
             }
         }
     }
@@ -849,11 +888,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         if (kPair && lane == 0) {
             // every MMA commit that targets this CTA's slot barriers has arrived (each slot's last phase completes
             // only after all of them): nothing arrives on this CTA's barriers after it leaves
-            const int total = *total_slot;
-            for (int k = max(0, total - depth); k < total; ++k) {
+            const int total = *total_slot;  // stages
+            for (int k = max(0, total - nst); k < total; ++k) {
                 bool done;
-                if constexpr (kPair) done = mbar_wait_cl(&sempty[k % depth], (uint32_t)(k / depth) & 1u, abort_flag);
-                else done = mbar_wait(&sempty[k % depth], (uint32_t)(k / depth) & 1u, abort_flag);
+                if constexpr (kPair) done = mbar_wait_cl(&sempty[k % nst], (uint32_t)(k / nst) & 1u, abort_flag);
+                else done = mbar_wait(&sempty[k % nst], (uint32_t)(k / nst) & 1u, abort_flag);
                 if (!done) break;
             }
         }
@@ -979,7 +1018,8 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
     }
     if (max_tiles <= 0) return cudaSuccess;
     // the CTA-pair form needs an even number of 128-row weight slices (each pair takes 256 rows)
-    if ((a.a_rows / kBM) % 2 == 0) return launch_form<true>(a, max_tiles, dev, s);
+    // the pair form: an even number of 128-row weight slices and whole stages of two 64-wide K slices
+    if ((a.a_rows / kBM) % 2 == 0 && (a.K / kBK) % 2 == 0) return launch_form<true>(a, max_tiles, dev, s);
     return launch_form<false>(a, max_tiles, dev, s);
 }
 
