@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     constexpr uint16_t pmask = 3u;  // both CTAs of the pair
 
     // fixed geometry for every item (tiles of up to kMaxBN rows): a ring of `depth` slots, na A buffers and nbuf
-    // partial buffers of kMaxBN columns in tensor memory
+    // partial buffers (nbuf set per launch, below) in tensor memory
     constexpr int sbytes = kPair ? kPairSlot : slot_bytes(kMaxBN);
     constexpr int na = ((int)kTmemCols - 2 * kMaxBN) / (int)kACols;
     // the single form: as many ring slots as A buffers (its slots are large); the pair form: twice as many (its slots
@@ -426,8 +426,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     constexpr int nst = depth / S;  // stage slots of the ring (stage slot j: ring slots S j .. S j + S - 1)
     static_assert(depth % S == 0 && na % S == 0, "whole stages");
     constexpr uint32_t part_base = (uint32_t)na * kACols;
-    constexpr int nbuf = ((int)kTmemCols - (int)part_base) / kMaxBN;
-    static_assert(na >= 2 && na <= kMaxA && nbuf >= 2 && nbuf <= kMaxBufs, "tensor-memory split");
+    constexpr int kPartCols = (int)kTmemCols - (int)part_base;  // the partial buffers' columns
+    static_assert(na >= 2 && na <= kMaxA && kPartCols / kMaxBN >= 2, "tensor-memory split");
     static_assert(depth <= kMaxRing && depth <= kMaxA && depth * sbytes <= kRingBytes, "ring");
     // slice gs uses ring slot gs mod depth and A buffer gs mod na; its stage gs / S uses stage slot (gs / S) mod nst,
     // whose barriers it shares with the other slices of the stage.  Single form (depth == na): its copies can land
@@ -450,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* total_slot = const_cast<int*>(abort_flag + 1);  // stages this CTA ran (for the teardown)
+    int* maxcols_slot = total_slot + 1;                  // the launch's widest partial (columns)
     float* scratch = reinterpret_cast<float*>(smem_raw + kSmemBytes - kBarBytes - kScratchBytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -471,6 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         mbar_init(accf, kMmaThreads);  // one final commit of each MMA thread
         *abort_flag = 0;
         *total_slot = 0;
+        *maxcols_slot = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -487,6 +489,27 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     if (kPair) cluster_sync();  // both CTAs' barriers are initialised before any remote copy or arrival
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // the launch's widest partial (every CTA finds the same in the tile list) sets the partial buffers: as many as
+    // tensor memory holds, at most kMaxBufs -- two for tiles of 97 rows and more, four for tiles of at most 48 rows
+    // (96 stacked columns), so that small tiles keep more partials in flight against the promoters' round trip
+    {
+        int m = 0;
+        for (int ti = threadIdx.x; ti < n_tiles; ti += kThreads) {
+            const int rows = tiles[4 * (1 + ti) + 2];
+            if (rows > 0 && rows <= kMaxBN) {
+                const int N = (rows + 15) & ~15;
+                m = max(m, N <= kMaxStackN ? 2 * N : N);
+            }
+        }
+        m = __reduce_max_sync(0xffffffffu, m);
+        if (lane == 0 && m > 0) atomicMax(maxcols_slot, m);
+    }
+    __syncthreads();
+    const int bufw = (max(*maxcols_slot, 32) + 31) & ~31;  // columns of a partial buffer
+    const int nbuf = min(kMaxBufs, kPartCols / bufw);      // 2, 3 or 4
+    // partial gp's buffer and its use of it (nbuf is a power of two or 3: no division on the MMA thread's path)
+    auto buf_of = [nbuf](int gp) { return nbuf == 3 ? gp % 3 : gp & (nbuf - 1); };
+    auto use_of = [nbuf](int gp) { return nbuf == 3 ? gp / 3 : gp >> (nbuf >> 1); };
     const uint32_t ring_s = smem_u32(ring);
     const uint64_t desc_ring = sdesc_k_sw128(ring_s);  // slot r's hi rows: + (r * sbytes) >> 4
     bool ok = true;
@@ -511,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     const uint32_t aph = (uint32_t)(gst / nst) & 1u;  // parity of stage slot j's barriers for it
                     // the stage's partial: one per 128 values of K (two-level), else the item's partial of this thread
                     const int gp = seq * pitem + (p.two_level ? ks / Gs : (pitem == 2 ? (ks & 1) : 0));
-                    const int b = gp % nbuf;
+                    const int b = buf_of(gp);
                     const bool first = p.two_level ? ks % Gs == 0 : ks < kMmaThreads;
                     const bool last = p.two_level ? ks % Gs == Gs - 1 : ks + kMmaThreads >= nsi;
                     // A decoded and the stage's B tiles landed; a stage that starts a partial in a buffer used before
@@ -519,9 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     // gp / nbuf - 1 of its pempty).  The waits overlap.  (Pair form: both CTAs' converters arrive on
                     // the leader's afull and both CTAs' B bytes land on its sfull.)
                     const bool reuse = first && gp >= nbuf;
-                    const uint32_t eph = reuse ? (uint32_t)(gp / nbuf - 1) & 1u : aph;
+                    const uint32_t eph = reuse ? (uint32_t)(use_of(gp) - 1) & 1u : aph;
                     // the stage's operands, before the wait (its round trip hides this arithmetic)
-                    const uint32_t d = tmem + part_base + (uint32_t)(b * kMaxBN);
+                    const uint32_t d = tmem + part_base + (uint32_t)(b * bufw);
                     const int g0 = gst * S;  // the stage's first global slice
                     uint64_t bh[S], bl[S];
                     uint32_t a[S];
@@ -675,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     break;
                 }
                 tc_fence_after();
-                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + part_base + (uint32_t)(b * kMaxBN);
+                const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + part_base + (uint32_t)(b * bufw);
                 uint32_t v[32];
                 if (stacked) {
                     // 16-column chunks cg + 3 i: hi columns c.. and lo columns N + c.., added in turn
