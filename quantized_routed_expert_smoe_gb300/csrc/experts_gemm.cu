@@ -326,20 +326,33 @@ __device__ __forceinline__ void add2(float& a0, float& a1, uint32_t p0, uint32_t
 // Pair m's codes sit at bits 2m of each 16-bit half.  OR-ed under the exponent of 2^(10 - 2m) they read as the fp16
 // value 2^(10 - 2m) + q exactly (a mantissa bit at position 2m weighs 2^(10 - 2m - 10 + 2m) = 1), so pairs 0-4 need
 // no shift; pairs 5-7 take the word shifted by 10 (their codes at bits 0, 2, 4).  Subtracting 2^e + 2 leaves q - 2
-// exactly, and the product with d is exact in fp16.
-__device__ __forceinline__ uint32_t decode_pair(uint32_t codes, int pos, __half2 d2) {
-    const int e = 10 - 2 * pos;
-    const uint32_t expo = (uint32_t)(e + 15) << 10;
-    const uint32_t v = (codes & (0x00030003u << (2 * pos))) | (expo | (expo << 16));
-    const __half2 base = __float2half2_rn((float)((1 << e) + 2));
-    return h2_as_u32(__hmul2(__hsub2(u32_as_h2(v), base), d2));
+// exactly, and the product with d is exact in fp16.  Three instructions a column, all on registers.
+template <int kPos>
+__device__ __forceinline__ uint32_t decode_pair(uint32_t codes, uint32_t d2) {
+    constexpr int e = 10 - 2 * kPos;
+    constexpr uint32_t mask = 0x00030003u << (2 * kPos);
+    constexpr uint32_t expo = ((uint32_t)(e + 15) << 10) * 0x00010001u;
+    constexpr uint32_t base = (((uint32_t)(e + 15) << 10) | (2u << (10 - e))) * 0x00010001u;  // 2^e + 2, both halves
+    uint32_t out;
+    asm("{\n\t.reg .b32 v;\n\t"
+        "lop3.b32 v, %1, %2, %3, 0xEA;\n\t"  // (codes & mask) | expo
+        "sub.rn.f16x2 v, v, %4;\n\t"
+        "mul.rn.f16x2 %0, v, %5;\n\t}"
+        : "=r"(out)
+        : "r"(codes), "n"(mask), "n"(expo), "r"(base), "r"(d2));
+    return out;
 }
-__device__ __forceinline__ void decode_weights16(uint32_t codes, __half2 d2, uint32_t* col) {
+// d2: the block's fp16 scale in both halves
+__device__ __forceinline__ void decode_weights16(uint32_t codes, uint32_t d2, uint32_t* col) {
     const uint32_t high = codes >> 10;
-#pragma unroll
-    for (int m = 0; m < 5; ++m) col[m] = decode_pair(codes, m, d2);
-#pragma unroll
-    for (int m = 5; m < 8; ++m) col[m] = decode_pair(high, m - 5, d2);
+    col[0] = decode_pair<0>(codes, d2);
+    col[1] = decode_pair<1>(codes, d2);
+    col[2] = decode_pair<2>(codes, d2);
+    col[3] = decode_pair<3>(codes, d2);
+    col[4] = decode_pair<4>(codes, d2);
+    col[5] = decode_pair<0>(high, d2);
+    col[6] = decode_pair<1>(high, d2);
+    col[7] = decode_pair<2>(high, d2);
 }
 
 struct GemmMaps {
@@ -869,13 +882,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                 const int ab = gs % na;
                 const uint8_t* wb = ring + r * sbytes + wofs;
                 const uint4 codes = *reinterpret_cast<const uint4*>(wb + ct * 16);
-                const __half2 sc = *reinterpret_cast<const __half2*>(wb + 2048 + ct * 4);
+                const uint32_t sc = *reinterpret_cast<const uint32_t*>(wb + 2048 + ct * 4);  // the two blocks' scales
+                const uint32_t d_lo = __byte_perm(sc, 0u, 0x1010), d_hi = __byte_perm(sc, 0u, 0x3232);
                 uint32_t col[16];  // one 32-value block at a time
-                decode_weights16(codes.x, __low2half2(sc), col);
-                decode_weights16(codes.y, __low2half2(sc), col + 8);
+                decode_weights16(codes.x, d_lo, col);
+                decode_weights16(codes.y, d_lo, col + 8);
                 tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols, col);
-                decode_weights16(codes.z, __high2half2(sc), col);
-                decode_weights16(codes.w, __high2half2(sc), col + 8);
+                decode_weights16(codes.z, d_hi, col);
+                decode_weights16(codes.w, d_hi, col + 8);
                 tmem_st_32x32b_x16(tmem + lane_base + (uint32_t)ab * kACols + 16u, col);
                 if (gs % S == S - 1) {
                     // the stage's last slice: test the next stage's barrier while the stores complete (a stage whose
