@@ -857,6 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
         const uint32_t ready0 = kPair ? cluster_addr(&afull[0], leader) : 0u;
         int gs = 0;          // the slice's global index
         bool ready = false;  // the stage's copies are known to have landed (tested while the last stage was stored)
+        bool afree = false;  // pair form: its A buffers are known to be free (tested likewise)
         Item t;
         for (int item = cid; item < n_items && ok; item += NC) {
             if (!load_item<kPair>(tiles, item, mgroups, C, crank, p, t)) continue;
@@ -872,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     if constexpr (kPair) {
                         // the stage's A buffers were last read by stage gst - na / S: released by its MMAs' commit
                         const int pg = gst - na / S;
-                        if (pg >= 0 && !mbar_wait(&sempty[pg % nst], (uint32_t)(pg / nst) & 1u, abort_flag)) {
+                        if (!afree && pg >= 0 && !mbar_wait(&sempty[pg % nst], (uint32_t)(pg / nst) & 1u, abort_flag)) {
                             ok = false;
                             break;
                         }
@@ -895,6 +896,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
                     // the stage's last slice: test the next stage's barrier while the stores complete (a stage whose
                     // weights have landed then costs no wait round trip), then signal the stage
                     ready = mbar_test(smem_u32(&wfull[(gst + 1) % nst]), (uint32_t)((gst + 1) / nst) & 1u);
+                    if constexpr (kPair) {
+                        const int pn = gst + 1 - na / S;  // the next stage's A buffers' previous stage
+                        afree = pn < 0 || mbar_test(smem_u32(&sempty[pn % nst]), (uint32_t)(pn / nst) & 1u);
+                    }
                     tmem_st_wait();
                     tc_fence_before();
                     if constexpr (kPair) {
