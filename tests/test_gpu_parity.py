@@ -476,11 +476,9 @@ def test_products_special_cases(B):
     assert np.all(np.abs(gu1 - want) <= 1e-6 * want)
 
 
-@pytest.mark.parametrize("shape", [(37, 128, 5, 3, 64), (300, 256, 2, 1, 128), (513, 128, 1, 1, 64),
-                                   (64, 384, 9, 4, 192)])
-def test_products_ragged_shapes(B, shape):
+def _products_case(B, inp, shape):
+    """Both products of one synthetic layer against the oracle, every routed row."""
     T, H, E, K, F = shape
-    inp = synth.make_custom(T, H, E, K, F, seed=sum(shape))
     ids, _ = oracle.route(inp["logits"], K)
     g = oracle.group(ids, E)
     xc, xs = oracle.quantize_q8(inp["x"])
@@ -496,6 +494,30 @@ def test_products_ragged_shapes(B, shape):
         if r1 > r0:
             mag = np.abs(Hd[r0:r1]) @ np.abs(deq_w(inp["wd_c"][e], inp["wd_s"][e], F)).T
             check_products(dm[r0:r1], want_d[r0:r1], mag, f"down {shape}")
+
+
+# (96, 256, 6, 2, 192): the down product's weight matrix has an even number of 128-row slices but K = 192 is three
+# 64-wide slices, not whole two-slice stages, so it takes the single-CTA form
+@pytest.mark.parametrize("shape", [(37, 128, 5, 3, 64), (300, 256, 2, 1, 128), (513, 128, 1, 1, 64),
+                                   (64, 384, 9, 4, 192), (96, 256, 6, 2, 192)])
+def test_products_ragged_shapes(B, shape):
+    _products_case(B, synth.make_custom(*shape, seed=sum(shape)), shape)
+
+
+@pytest.mark.parametrize("lo,hi,T", [(0, 48, 160), (48, 64, 160), (64, 192, 320)])
+def test_products_partial_buffer_counts(B, lo, hi, T):
+    """The products keep as many partial buffers in tensor memory as the launch's widest tile allows: four when no
+    tile has more than 48 rows, three up to 64, two above.  A seed whose largest expert falls in (lo, hi] is picked
+    from the oracle's routing, so each count is exercised."""
+    H, E, K, F = 256, 16, 4, 128
+    for seed in range(200):
+        inp = synth.make_custom(T, H, E, K, F, seed=seed)
+        widest = int(oracle.group(oracle.route(inp["logits"], K)[0], E)["counts"].max())
+        if lo < widest <= hi:
+            break
+    else:
+        pytest.fail(f"no seed below 200 gives a largest expert in ({lo}, {hi}]")
+    _products_case(B, inp, (T, H, E, K, F))
 
 
 # ------------------------------------------------------------------------------------------------ SwiGLU + requant
