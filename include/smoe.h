@@ -44,7 +44,9 @@
  *
  * CONVENTIONS
  *   - Every pointer argument is a DEVICE pointer owned by the caller; the library allocates nothing and keeps no
- *     state between calls.  Every buffer must be 16-byte aligned.
+ *     state between calls.  Every buffer must be 16-byte aligned.  The one exception is the block object
+ *     (smoe_block_*, at the end of this header): it owns the device buffers, streams, events and CUDA graphs of a
+ *     whole block and takes HOST pointers for its inputs and output.
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream) and never
  *     synchronises with the host.
  *   - A call returns SMOE_OK or an error found on the host before anything is launched (a bad argument, an
@@ -71,6 +73,8 @@ typedef int smoe_status;
 #define SMOE_ERR_UNSUPPORTED 3  /* a shape the kernels do not cover, or a device other than sm_103 */
 #define SMOE_ERR_RANGE 4        /* (device, tiles header[1]) a routed id outside [0, E) */
 #define SMOE_ERR_TIMEOUT 5      /* (device, tiles header[3]) a kernel's internal wait gave up; outputs undefined */
+#define SMOE_ERR_CUDA 6         /* (smoe_block_*) a CUDA runtime call failed: an allocation, a copy, a stream, event
+                                   or graph operation; smoe_last_error_string() names the CUDA error */
 
 /* Largest supported sizes. */
 #define SMOE_MAX_EXPERTS 1024
@@ -267,6 +271,42 @@ smoe_status smoe_shared_gate(const float* x, const float* wsg, int64_t T, int H,
  *   arguments and rules as smoe_combine. */
 smoe_status smoe_combine_shared(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,
                                 const float* ds, const float* sg, float* y, void* stream);
+
+/* THE BLOCK AS ONE OBJECT (a library service over the calls above; the pages' Prefill::run owns the equivalent
+ * buffers).  A smoe_block holds every device buffer of the eight steps for chunks of T tokens, two device sets of
+ * the chunk's inputs and output, three streams of its own (a copy-in, a copy-out and a compute stream) and a CUDA
+ * graph of the eight calls for each input set.  It is created and used with the same device current; calls on one
+ * block must not run concurrently from several host threads.
+ *
+ * smoe_block_create: T >= 1 tokens a chunk; H, E, K, F as for the calls above (H % 128 == 0, F % 64 == 0,
+ *   1 <= K <= min(E, 32), E <= 1024).  wgu and wd are the routed experts' weights packed by smoe_pack_q2 (DEVICE
+ *   pointers, owned by the caller, read by every chunk: they must outlive the block).  *out receives the block, or
+ *   NULL on an error (SMOE_ERR_ARG for a bad size or pointer, SMOE_ERR_UNSUPPORTED off sm_103, SMOE_ERR_CUDA when an
+ *   allocation fails; nothing is left allocated then).
+ * smoe_block_destroy: waits for the block's queued work, then frees everything it owns (NULL is ignored).
+ * smoe_block_run: one chunk device to device on `stream`: logits fp32 [T][E], x fp32 [T][H] -> y fp32 [T][H] (DEVICE
+ *   pointers, 16-byte aligned), exactly the eight calls in order (the q8 quantisation on a side stream beside the
+ *   routing and grouping); asynchronous like the calls above.
+ * smoe_block_submit_host: one chunk from and into HOST memory, queued behind the chunks submitted before it:
+ *   logits fp32 [T][E] and x fp32 [T][H] are copied to one of the two device input sets while the previous chunk
+ *   computes, the chunk runs as a replay of that set's graph, and y fp32 [T][H] is copied back while the next chunk
+ *   computes.  The call returns at once; the host buffers must stay valid and unchanged (y: unread) until
+ *   smoe_block_sync returns.  Page-locked host memory (cudaHostAlloc, cudaHostRegister) lets the copies run beside
+ *   the compute; pageable memory is correct but serialises them.  The first submit of a block runs the chunk
+ *   eagerly once on zero inputs and captures the two graphs (about a millisecond); do that before timing.  The
+ *   block's work starts after the work queued on `stream` before the call.
+ * smoe_block_sync: `stream` waits for every chunk submitted so far (their outputs are then in host memory) and the
+ *   host waits for them too.  Errors found on the device are in the tiles header (smoe_block_status). */
+typedef struct smoe_block smoe_block;
+smoe_status smoe_block_create(int64_t T, int H, int E, int K, int F, const uint8_t* wgu, const uint8_t* wd,
+                              smoe_block** out);
+void smoe_block_destroy(smoe_block* b);
+smoe_status smoe_block_run(smoe_block* b, const float* logits, const float* x, float* y, void* stream);
+smoe_status smoe_block_submit_host(smoe_block* b, const float* logits, const float* x, float* y, void* stream);
+smoe_status smoe_block_sync(smoe_block* b, void* stream);
+/* The last chunk's device-side status (synchronises): header[1] (grouping: SMOE_OK or SMOE_ERR_RANGE) into *group,
+ * header[3] (the expert products: SMOE_OK or SMOE_ERR_TIMEOUT) into *kernel. */
+smoe_status smoe_block_status(smoe_block* b, int* group, int* kernel);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,7 @@ import torch
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsmoe.so")
 
-SMOE_OK, SMOE_ERR_ARG, SMOE_ERR_LAUNCH, SMOE_ERR_UNSUPPORTED, SMOE_ERR_RANGE, SMOE_ERR_TIMEOUT = range(6)
+SMOE_OK, SMOE_ERR_ARG, SMOE_ERR_LAUNCH, SMOE_ERR_UNSUPPORTED, SMOE_ERR_RANGE, SMOE_ERR_TIMEOUT, SMOE_ERR_CUDA = range(7)
 TILE_ROWS = 192
 
 
@@ -81,6 +81,16 @@ _SIGS = {
     "smoe_combine_shared": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                              ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
                             ctypes.c_int),
+    "smoe_block_create": ([ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                           ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+    "smoe_block_destroy": ([ctypes.c_void_p], None),
+    "smoe_block_run": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+                       ctypes.c_int),
+    "smoe_block_submit_host": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p],
+                               ctypes.c_int),
+    "smoe_block_sync": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_block_status": ([ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
+                          ctypes.c_int),
 }
 
 # every symbol include/smoe.h declares
@@ -111,7 +121,7 @@ def status_string(status: int) -> str:
 def _check(call: str, status: int):
     if status != SMOE_OK:
         text = status_string(status)
-        if status == SMOE_ERR_LAUNCH:
+        if status in (SMOE_ERR_LAUNCH, SMOE_ERR_CUDA):
             text += ": " + load_library().smoe_last_error_string().decode()
         raise SmoeError(call, status, text)
 
@@ -525,6 +535,61 @@ class SmoePipeline:
     def synchronize(self):
         self.drain()
         self.compute.synchronize()
+
+
+class NativeBlock:
+    """The block as the library's own object (smoe_block_*): its device buffers, streams and CUDA graphs live in
+    libsmoe; this class only passes pointers.  run(logits, x, y): one chunk device to device.  submit_host(logits,
+    x, y): one chunk from and into host memory (torch CPU tensors, pinned for overlapped copies), queued; sync(): the
+    host (and `stream`) wait for every submitted chunk.  The expert weights are packed here once and kept alive as
+    long as the block."""
+
+    def __init__(self, T: int, H: int, E: int, K: int, F: int, wgu_c, wgu_s, wd_c, wd_s, device="cuda"):
+        load_library()
+        device_check()
+        self.T, self.H, self.E, self.K, self.F = T, H, E, K, F
+        self.wgu = pack_weights(wgu_c, wgu_s, device)
+        self.wd = pack_weights(wd_c, wd_s, device)
+        torch.cuda.synchronize(self.wgu.device)
+        h = ctypes.c_void_p()
+        lib = load_library()
+        _check("smoe_block_create", lib.smoe_block_create(T, H, E, K, F, self.wgu.data_ptr(), self.wd.data_ptr(),
+                                                          ctypes.byref(h)))
+        self._h = h
+
+    def _stream(self, stream):
+        return _as_stream(stream, self.wgu.device).cuda_stream
+
+    def run(self, logits, x, y, stream=None):
+        _check("smoe_block_run", load_library().smoe_block_run(self._h, logits.data_ptr(), x.data_ptr(), y.data_ptr(),
+                                                               self._stream(stream)))
+        return y
+
+    def submit_host(self, logits, x, y, stream=None):
+        for t in (logits, x, y):
+            assert t.device.type == "cpu" and t.dtype == torch.float32 and t.is_contiguous()
+        assert logits.numel() == self.T * self.E and x.numel() == self.T * self.H and y.numel() == self.T * self.H
+        _check("smoe_block_submit_host", load_library().smoe_block_submit_host(
+            self._h, logits.data_ptr(), x.data_ptr(), y.data_ptr(), self._stream(stream)))
+
+    def sync(self, stream=None):
+        _check("smoe_block_sync", load_library().smoe_block_sync(self._h, self._stream(stream)))
+
+    def device_status(self):
+        g, k = ctypes.c_int(), ctypes.c_int()
+        _check("smoe_block_status", load_library().smoe_block_status(self._h, ctypes.byref(g), ctypes.byref(k)))
+        return g.value, k.value
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            load_library().smoe_block_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def pack_weights(codes, scales, device="cuda", swiglu=False):

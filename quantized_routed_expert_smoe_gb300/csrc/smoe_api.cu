@@ -41,6 +41,15 @@ constexpr int64_t kMaxGridY = 65535;
 
 }  // namespace
 
+namespace smoe {
+smoe_status note_cuda_error(cudaError_t err) {
+    if (err == cudaSuccess) return SMOE_OK;
+    g_last_cuda_error = cudaGetErrorName(err);
+    cudaGetLastError();
+    return SMOE_ERR_CUDA;
+}
+}  // namespace smoe
+
 extern "C" {
 
 const char* smoe_status_string(smoe_status s) {
@@ -51,6 +60,7 @@ const char* smoe_status_string(smoe_status s) {
         case SMOE_ERR_UNSUPPORTED: return "unsupported shape or device (libsmoe runs on sm_103 only)";
         case SMOE_ERR_RANGE: return "a routed expert id is outside [0, E)";
         case SMOE_ERR_TIMEOUT: return "a kernel's internal wait ran out";
+        case SMOE_ERR_CUDA: return "a CUDA runtime call failed (allocation, copy, stream, event or graph)";
         default: return "unknown status";
     }
 }

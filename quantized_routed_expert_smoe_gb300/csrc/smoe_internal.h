@@ -10,6 +10,9 @@
 
 namespace smoe {
 
+// a failed CUDA runtime call: remembered for smoe_last_error_string and cleared; returns SMOE_ERR_CUDA
+smoe_status note_cuda_error(cudaError_t err);
+
 size_t group_work_bytes(int64_t n, int E);
 
 cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int K, int32_t* ids, float* w, cudaStream_t s);

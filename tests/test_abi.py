@@ -103,6 +103,23 @@ def test_host_side_rejections_need_no_gpu(lib):
     assert lib.smoe_group_noalloc(fake, 8, 2, 4, odd, fake, fake, fake, fake, 1 << 20, null) == ARG
     assert lib.smoe_group_noalloc(fake, 8, 2, 4, fake, fake, fake, odd, fake, 1 << 20, null) == ARG
     assert lib.smoe_group_noalloc(fake, 8, 0, 4, fake, fake, fake, fake, fake, 1 << 20, null) == ARG
+    # the block object: bad sizes, null or misaligned weights, a null block -- refused before any device work
+    h = ctypes.c_void_p(123)
+    assert lib.smoe_block_create(0, 256, 16, 2, 128, fake, fake, ctypes.byref(h)) == ARG and h.value is None
+    assert lib.smoe_block_create(64, 200, 16, 2, 128, fake, fake, ctypes.byref(h)) == ARG
+    assert lib.smoe_block_create(64, 256, 16, 17, 128, fake, fake, ctypes.byref(h)) == ARG
+    assert lib.smoe_block_create(64, 256, 16, 2, 96, fake, fake, ctypes.byref(h)) == ARG
+    assert lib.smoe_block_create(64, 256, 16, 2, 128, null, fake, ctypes.byref(h)) == ARG
+    assert lib.smoe_block_create(64, 256, 16, 2, 128, fake, odd, ctypes.byref(h)) == ARG
+    assert lib.smoe_block_create(64, 256, 16, 2, 128, fake, fake, None) == ARG
+    assert lib.smoe_block_run(null, fake, fake, fake, null) == ARG
+    assert lib.smoe_block_submit_host(null, fake, fake, fake, null) == ARG
+    assert lib.smoe_block_sync(null, null) == ARG
+    g, k = ctypes.c_int(), ctypes.c_int()
+    assert lib.smoe_block_status(null, ctypes.byref(g), ctypes.byref(k)) == ARG
+    lib.smoe_block_destroy(null)  # a no-op
+    if not _has_gpu():
+        assert lib.smoe_block_create(64, 256, 16, 2, 128, fake, fake, ctypes.byref(h)) == UNSUP and h.value is None
     # well-formed arguments on a machine without an sm_103 device: a clean error, never a fallback
     st = lib.smoe_route_topk(fake, 4, 16, 2, fake, fake, null)
     if not _has_gpu():

@@ -125,3 +125,39 @@ def test_pipeline_matches_run(B, with_shared, with_router, graphs):
     for s in range(steps):
         assert np.array_equal(h_out[s].numpy(), want[s]), f"step {s}"
     assert blk.device_status() == (0, 0)
+
+
+@pytest.mark.parametrize("name", ["tiny", "t1024"])
+def test_native_block_matches_run(B, name):
+    # the block as libsmoe's own object (smoe_block_*): chunks from and into pinned host memory through its copy
+    # streams and graphs, and device to device, give every chunk's output bit for bit as SmoeBlock.run; more chunks
+    # than device sets, and a second round after a sync
+    cfg = synth.CONFIGS[name]
+    inp = synth.make_layer(cfg)
+    blk = B.SmoeBlock(cfg.T, cfg.H, cfg.E, cfg.K, cfg.F, inp["wgu_c"], inp["wgu_s"], inp["wd_c"], inp["wd_s"])
+    nb = B.NativeBlock(cfg.T, cfg.H, cfg.E, cfg.K, cfg.F, inp["wgu_c"], inp["wgu_s"], inp["wd_c"], inp["wd_s"])
+    steps = 5
+    xs = [synth.make_rows(cfg.T, cfg.H, seed=60 + s) for s in range(steps)]
+    lgs = [synth.make_rows(cfg.T, cfg.E, seed=70 + s, scale=0.5) for s in range(steps)]
+    want = [host(blk.run(dev(lgs[s]), dev(xs[s]))).copy() for s in range(steps)]
+    h_lg = [torch.from_numpy(lgs[s]).pin_memory() for s in range(steps)]
+    h_x = [torch.from_numpy(xs[s]).pin_memory() for s in range(steps)]
+    for rnd in range(2):
+        h_out = [torch.full((cfg.T, cfg.H), float("nan")).pin_memory() for _ in range(steps)]
+        for s in range(steps):
+            nb.submit_host(h_lg[s], h_x[s], h_out[s])
+        nb.sync()
+        for s in range(steps):
+            assert np.array_equal(h_out[s].numpy(), want[s]), f"round {rnd} chunk {s}"
+        assert nb.device_status() == (0, 0)
+    y = torch.empty(cfg.T, cfg.H, dtype=torch.float32, device="cuda")
+    nb.run(dev(lgs[2]), dev(xs[2]), y)
+    assert np.array_equal(host(y), want[2])
+    # pageable host memory is correct too (its copies do not overlap the compute)
+    h_page = torch.empty(cfg.T, cfg.H, dtype=torch.float32)
+    nb.submit_host(torch.from_numpy(lgs[1]), torch.from_numpy(xs[1]), h_page)
+    nb.sync()
+    assert np.array_equal(h_page.numpy(), want[1])
+    nb.close()
+    del blk
+    torch.cuda.empty_cache()
