@@ -169,7 +169,8 @@ smoe_status smoe_gather_q8(const int8_t* codes, const uint16_t* scales, int64_t 
  * output j in [0, 2F):
  *   GU[r][j] = sum_b dX[src r][b] * dW[e][j][b] * sum_{i in block b} (qW - 2) * qX[src r][i]     (fp32 result)
  *   xop      the routed rows in operand form, fp16 [2][n][H] (from smoe_gather_q8).
- *   tiles    from smoe_group (header[3] receives SMOE_ERR_TIMEOUT).   n = T*K (sizes the launch).
+ *   tiles    from smoe_group (header[3] receives SMOE_ERR_TIMEOUT, or SMOE_ERR_ARG when its tile count exceeds
+ *            smoe_max_tiles(n, E): then no tile is read and nothing is written).   n = T*K (sizes the launch).
  *   wgu      gate/up weights [E][2F][H] packed by smoe_pack_q2.
  *   gu       fp32 [n][2F] out, row r = routed row r.
  *   H % 128 == 0, F % 64 == 0. */

@@ -407,6 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
     int32_t* tiles = p.tiles;
     if (tiles[1] != 0) return;  // the grouping failed: nothing to do (the same answer in every CTA)
     const int n_tiles = tiles[0];
+    if (n_tiles < 0 || n_tiles > p.max_tiles) {  // not a tile list of this size: read nothing beyond it
+        if (blockIdx.x == 0 && threadIdx.x == 0) tiles[3] = SMOE_ERR_ARG;
+        return;
+    }
     const int nk = p.K / kBK;  // slices of an item
     // A stage is S consecutive slices (pair form: S = 2, K a multiple of 128; single form: S = 1) with one set of
     // ring barriers: one wait of the MMA thread, one commit, one arrival of each converter warp for S slices' work.
@@ -1004,6 +1008,7 @@ cudaError_t launch_form(const ExpertsGemmArgs& a, int64_t max_tiles, int dev, cu
     ExpertsGemmArgs args = a;
     // the pair form is a cluster of one CTA pair; the single form runs without clusters
     args.cluster = kPair ? 2 : 1;
+    args.max_tiles = (int)max_tiles;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
@@ -1059,8 +1064,8 @@ cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cud
         }
     }
     if (max_tiles <= 0) return cudaSuccess;
-    // the CTA-pair form needs an even number of 128-row weight slices (each pair takes 256 rows)
-    // the pair form: an even number of 128-row weight slices and whole stages of two 64-wide K slices
+    // the CTA-pair form: an even number of 128-row weight slices (each pair takes 256 rows) and whole stages of two
+    // 64-wide K slices
     if ((a.a_rows / kBM) % 2 == 0 && (a.K / kBK) % 2 == 0) return launch_form<true>(a, max_tiles, dev, s);
     return launch_form<false>(a, max_tiles, dev, s);
 }

@@ -50,6 +50,7 @@ struct ExpertsGemmArgs {
     int8_t* hc;           // [b_rows][a_rows / 2] q8 codes of h, or null: fp32 rows to `out`
     uint16_t* hs;         // [b_rows][a_rows / 64] fp16 scales
     uint16_t* hop;        // [2][b_rows][a_rows / 2] h in operand form
+    int max_tiles = 0;    // entries the tile list holds (set by the launcher): a larger header count is an error
 };
 cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s);
 

@@ -474,6 +474,16 @@ def test_products_special_cases(B):
     # every term is positive here, so sum |terms| = the closed form itself
     check_products(gu1, np.full(gu1.shape, want), np.full(gu1.shape, want), "constant row")
     assert np.all(np.abs(gu1 - want) <= 1e-6 * want)
+    # a tile list whose header counts more tiles than smoe_max_tiles(n, E) allows: the product reads none of them,
+    # reports SMOE_ERR_ARG in header[3] and leaves its output untouched
+    tiles = _tiles_dev(B, g, T * K, E)
+    tiles[0] = B.max_tiles(T * K, E) + 5
+    out = torch.full((T * K, 2 * F), float("nan"), dtype=torch.float32, device="cuda")
+    src = g["src"].astype(np.int64)
+    wp = B.pack_weights(inp["wgu_c"], inp["wgu_s"])
+    B.smoe_experts_gateup(dev(to_operand(xc[src], xs[src])), tiles, T * K, E, wp, H, F, out)
+    assert host(tiles)[3] == B.SMOE_ERR_ARG
+    assert torch.isnan(out).all()
 
 
 def _products_case(B, inp, shape):
