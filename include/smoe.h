@@ -297,7 +297,10 @@ smoe_status smoe_combine_shared(const float* dm, const int32_t* slot, const floa
  *   eagerly once on zero inputs and captures the two graphs (about a millisecond); do that before timing.  The
  *   block's work starts after the work queued on `stream` before the call.
  * smoe_block_sync: `stream` waits for every chunk submitted so far (their outputs are then in host memory) and the
- *   host waits for them too.  Errors found on the device are in the tiles header (smoe_block_status). */
+ *   host waits for them too.  Errors found on the device are in the tiles header (smoe_block_status).
+ * smoe_block_run and the submitted chunks share the block's intermediate buffers: call smoe_block_sync before a
+ *   smoe_block_run, and let a smoe_block_run finish (its stream) before the next submit.  After an error status from
+ *   any of these calls, destroy the block. */
 typedef struct smoe_block smoe_block;
 smoe_status smoe_block_create(int64_t T, int H, int E, int K, int F, const uint8_t* wgu, const uint8_t* wd,
                               smoe_block** out);
