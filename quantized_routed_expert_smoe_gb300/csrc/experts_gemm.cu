@@ -30,19 +30,26 @@
 // order; the MMA's N, a multiple of 16) x one 128-row slice of the expert's weight matrix (the MMA's M; swap-AB:
 // weights are the M operand so that a small expert wastes little).
 //
-// Two forms.  The CTA-pair form (any weight matrix with an even number of 128-row slices) runs the MMAs over a pair
-// of CTAs with tcgen05 cta_group::2: M = 256, each CTA decoding and accumulating its own 128 weight rows, and the
-// tile's B rows split between the two CTAs' shared memories (a tile of at most 96 rows: its hi rows in the even CTA
-// and its lo rows in the odd one, one MMA of 2N; a larger tile: N/2 rows of each part in each).  The tensor cores
-// of both SMs read both halves, so each SM takes in half the row bytes per MMA of the single-CTA form, its ring
-// slots are half as large and twice as many slices are in flight.  A cluster is one pair.  The even CTA issues the
-// pair's MMAs: both CTAs' converter warps meet on its `ready` barrier, both CTAs' B copies count their bytes on its
-// slot barrier (the cta_group::2 form of the TMA load) and both CTAs' promoter warps arrive on its `pempty`; its
-// commits release the slots and signal the partials in both CTAs.  The single-CTA form (an odd number of 128-row
-// slices) issues its own MMAs.  No TMA load is multicast.  Five warpgroups, registers rebalanced with setmaxnreg:
-//   warpgroup 0   warps 0 and 2, one lane each: the MMAs of alternate slices -- of alternate slice pairs for
-//                 gate/up (four K16 steps x two parts a slice; one thread's waits overlap the other's MMAs); warp 0
-//                 also allocates the tensor memory;
+// Two forms.  The CTA-pair form (a weight matrix with an even number of 128-row slices and K a multiple of 128) runs
+// the MMAs over a pair of CTAs with tcgen05 cta_group::2: M = 256, each CTA decoding and accumulating its own 128
+// weight rows, and the tile's B rows split between the two CTAs' shared memories (a tile of at most 96 rows: its hi
+// rows in the even CTA and its lo rows in the odd one, one MMA of 2N; a larger tile: N/2 rows of each part in each).
+// The tensor cores of both SMs read both halves, so each SM takes in half the row bytes per MMA of the single-CTA
+// form, its ring slots are half as large and twice as many slices are in flight.  A cluster is one pair.  The even
+// CTA issues the pair's MMAs: both CTAs' converter warps meet on its `ready` barrier, both CTAs' B copies count
+// their bytes on its stage barrier (the cta_group::2 form of the TMA load) and both CTAs' promoter warps arrive on
+// its `pempty`; its commits release the slots and signal the partials in both CTAs.  The single-CTA form (any other
+// shape) issues its own MMAs.  No TMA load is multicast.
+//
+// Stages.  Every barrier hand-over costs a few hundred cycles, so the ring's barriers are per STAGE: S consecutive
+// 64-wide slices (pair form S = 2, 128 values of K; single form S = 1) share one wait of the producer, one arrival
+// of each converter warp, one wait and one commit of the MMA thread.
+//
+// Five warpgroups, registers rebalanced with setmaxnreg (launched at 96; warpgroup 0 and the converters 48, the
+// promoters 128):
+//   warpgroup 0   warps 0 and 2, one lane each: the MMAs of alternate stages -- of alternate groups of 128 values
+//                 of K for gate/up (one thread's waits overlap the other's MMAs; a stage's MMAs go out from one
+//                 asm block with every operand computed before the wait); warp 0 also allocates the tensor memory;
 //                 warp 1: the producer -- per 64-wide K slice, one TMA tile load of the tile's rows of each part
 //                 (128-byte swizzle; pair form: this CTA's half of them) and one bulk copy of the packed weight
 //                 block into a ring slot;
@@ -51,21 +58,23 @@
 //                 and up rows interleaved in the packed weights), h = silu(g) * u requantised to q8, planar and in
 //                 operand form;
 //   warpgroup 4   converters: thread = weight row: decode its 64 weights of the slice into the slice's A buffer in
-//                 tensor memory.
-// Tensor memory (512 columns): 4 A buffers of 32 columns, then 2 partial buffers of 192 columns (a tile's partial
-// takes N of them, or 2N for a tile of at most 96 rows, which stacks its hi and lo rows into one MMA; gate/up
-// promotes a partial every two slices, down one partial per MMA thread at the item's end).  A tile has at most 192
-// rows: a promoter thread then holds its 64 accumulators and two 32-column loads.
+//                 tensor memory (three register instructions a column of two weights).
+// Tensor memory (512 columns): 4 A buffers of 32 columns, then the partial buffers in the other 384 -- as many as
+// the launch's widest partial allows (2 for 97..192 columns, 3 up to 128, 4 up to 96; a tile's partial takes N
+// columns, or 2N for a tile of at most 96 rows, which stacks its hi and lo rows into one MMA).  Gate/up promotes a
+// partial every 128 values of K, down one partial per MMA thread at the item's end.  A tile has at most 192 rows: a
+// promoter thread then holds its 64 accumulators and one 32-column load.
 //
 // Synchronisation: a satisfied mbarrier wait still costs a round trip of a few hundred cycles, and the ring's slots
 // circulate through a chain of latencies (slot released -> copies issued -> landed -> A decoded -> MMAs -> released),
-// so each role waits as little as it can and nothing waits on what it does not need.  A slot's packed weights land
+// so each role waits as little as it can and nothing waits on what it does not need.  A stage's packed weights land
 // on their own barrier, so the converters decode while the B tiles are still in flight; in the single form they
 // wait on nothing else -- its ring has as many slots as A buffers, so a slot's new contents also mean that the MMAs
 // of the slice that last used its A buffer have completed (the pair form's ring is twice as deep, so there they also
-// wait for that slice's release) -- and test the next slot's barrier while a slice's stores complete.  The MMA
-// thread waits once per slice, in one round trip, on "A decoded", "B tiles landed" and, for a slice that starts a
-// partial in a buffer used before, "the promoters have taken that buffer's previous partial".
+// wait for the release of the stage that last used the A buffers) -- and test the next stage's barriers while a
+// stage's stores complete.  The MMA thread waits once per stage, in one round trip, on "A decoded", "B tiles landed"
+// and, for a stage that starts a partial in a buffer used before, "the promoters have taken that buffer's previous
+// partial".
 //
 // K order: within each group of 16 K values, operand position 2m holds value m and position 2m+1 value m+8
 // (m = 0..7) -- the order in which 2-bit codes unpack in pairs -- for A and B alike, so the contraction is unchanged
