@@ -56,66 +56,73 @@ __device__ __forceinline__ void split_pairs(uint4 qp, __half2 d2, uint4& hi, uin
     lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// round-half-away(x / d) for the q8 rule, where the quotient is the IEEE (correctly rounded) fp32 division, from a
-// multiply by the correctly rounded reciprocal inv = RN(1/d): g = RN(x * inv) is within |x/d| 2^-23 of x/d and
+// q8 of the NV values v held by this thread (NV = 8 or 16), its 32-value block being spread over 32 / NV consecutive
+// lanes; writes the NV codes packed little-endian into `out` and returns the block's fp16 scale bits.
+//
+// Each code is round-half-away(x / d) of the IEEE (correctly rounded) fp32 quotient, clamped to [-127, 127], taken
+// from a multiply by the correctly rounded reciprocal inv = RN(1/d): g = RN(x * inv) is within |x/d| 2^-23 of x/d and
 // RN(x/d) within |x/d| 2^-24, so both round to the same integer unless a half-integer lies within |x/d| 2^-22 of g.
-// In the q8 rule |x/d| < 127.1 (d >= amax/127 (1 - 2^-11)), so that margin is below 2^-14: only values whose g lies
-// within 2^-14 of a half-integer (exact .5 ties included) take the IEEE division itself.
-__device__ __forceinline__ float q8_round(float x, float d, float inv) {
-    const float g = x * inv;
-    const float a = fabsf(g);
-    if (fabsf((a - truncf(a)) - 0.5f) <= 6.103515625e-05f) return roundf(__fdiv_rn(x, d));  // 2^-14
-    return roundf(g);
-}
-
-// q8 of the 8 values v held by this thread, its block being spread over 4 consecutive lanes; returns the 8 codes
-// packed little-endian and the block's fp16 scale bits.
-__device__ __forceinline__ uint2 q8_encode8(const float (&v)[8], uint16_t* scale_bits) {
+// Here |x/d| < 192 (d = fp16_rn(amax/127) is at least amax/127 (1 - 2^-11) when normal, and at least 2/3 of it when
+// subnormal), so that margin is below 2^-14: only values whose g lies within 2^-14 of a half-integer (exact .5 ties
+// included) take the IEEE division itself.  Elsewhere g rounds to the same integer under any tie rule, so it is
+// rounded by adding and subtracting 1.5 * 2^23 (round to nearest even, exact for |g| < 2^22), and the clamped
+// integer's low byte is read off the bits of (r + 1.5 * 2^23).  A zero scale gives zero codes.
+template <int NV>
+__device__ __forceinline__ uint16_t q8_encode(const float (&v)[NV], uint32_t (&out)[NV / 4]) {
+    static_assert(NV == 8 || NV == 16, "a block spread over 4 or 2 lanes");
     float amax = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    for (int i = 0; i < NV; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+    for (int off = 1; off < 32 / NV; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     const __half dh = __float2half_rn(__fdiv_rn(amax, 127.0f));
     const float d = __half2float(dh);
-    *scale_bits = __half_as_ushort(dh);
-    const float inv = d != 0.0f ? __frcp_rn(d) : 0.0f;
-    uint32_t lo = 0, hi = 0;
+    if (d == 0.0f) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        int q = 0;
-        if (d != 0.0f) {
-            float r = q8_round(v[i], d, inv);
-            r = fminf(fmaxf(r, -127.0f), 127.0f);
-            q = (int)r;
-        }
-        const uint32_t b = (uint32_t)(q & 0xff);
-        if (i < 4) lo |= b << (8 * i);
-        else hi |= b << (8 * (i - 4));
+        for (int w = 0; w < NV / 4; ++w) out[w] = 0u;
+        return __half_as_ushort(dh);
     }
-    return make_uint2(lo, hi);
+    const float inv = __frcp_rn(d);
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    uint32_t b[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const float g = v[i] * inv;
+        float r = (g + kRound) - kRound;
+        if (fabsf(g - r) >= 0.5f - 6.103515625e-05f) r = roundf(__fdiv_rn(v[i], d));  // within 2^-14 of a tie
+        r = fminf(fmaxf(r, -127.0f), 127.0f);
+        b[i] = __float_as_uint(r + kRound);  // low byte: r mod 256
+    }
+#pragma unroll
+    for (int w = 0; w < NV / 4; ++w)
+        out[w] = __byte_perm(__byte_perm(b[4 * w], b[4 * w + 1], 0x0040),
+                             __byte_perm(b[4 * w + 2], b[4 * w + 3], 0x0040), 0x5410);
+    return __half_as_ushort(dh);
 }
 
-// step 3: x [rows][cols] -> codes, scales; thread i covers elements [8i, 8i + 8) of the flattened rows
-__global__ void __launch_bounds__(256) quantize_q8_kernel(const float4* __restrict__ x, int64_t n8, int cols,
-                                                          uint2* __restrict__ codes, uint16_t* __restrict__ scales) {
-    for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < n8; base += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t i = base + threadIdx.x;
-        // n8 is a multiple of 4 (cols % 32 == 0), so every group of 4 lanes is either all in range or all out;
-        // lanes past the end still take part in the block's shuffles
-        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        const bool in = i < n8;
-        if (in) {
-            const float4 a = __ldcs(x + 2 * i), b = __ldcs(x + 2 * i + 1);
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-            v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        }
-        uint16_t sb;
-        const uint2 q = q8_encode8(v, &sb);
-        if (in) {
-            codes[i] = q;
-            if ((i & 3) == 0) scales[i >> 2] = sb;
-        }
+// step 3: x [rows][cols] -> codes, scales.  Thread i covers elements [16i, 16i + 16) of the flattened rows (four
+// 16-byte loads, all issued before the encode; a 32-value block over two lanes).
+__global__ void __launch_bounds__(256) quantize_q8_kernel(const float4* __restrict__ x, int64_t n16,
+                                                          uint4* __restrict__ codes, uint16_t* __restrict__ scales) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    // n16 is even (cols % 32 == 0), so both lanes of a block are in range or both out; lanes past the end still take
+    // part in the shuffle
+    const bool in = i < n16;
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (in) a = __ldcs(x + 4 * i + u);
+        v[4 * u] = a.x;
+        v[4 * u + 1] = a.y;
+        v[4 * u + 2] = a.z;
+        v[4 * u + 3] = a.w;
+    }
+    uint32_t q[4];
+    const uint16_t sb = q8_encode<16>(v, q);
+    if (in) {
+        codes[i] = make_uint4(q[0], q[1], q[2], q[3]);
+        if ((i & 1) == 0) scales[i >> 1] = sb;
     }
 }
 
@@ -142,8 +149,9 @@ __global__ void __launch_bounds__(256) swiglu_requant_kernel(const float* __rest
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = __fdiv_rn(g[k], 1.0f + expf(-g[k])) * u[k];
         }
-        uint16_t sb;
-        const uint2 q = q8_encode8(v, &sb);
+        uint32_t qw[2];
+        const uint16_t sb = q8_encode<8>(v, qw);
+        const uint2 q = make_uint2(qw[0], qw[1]);
         // the even lane holds values 0..7 of its group of 16, the odd lane 8..15; F % 16 == 0 keeps the pairs aligned
         const bool even = (threadIdx.x & 1) == 0;
         const uint32_t other = __shfl_xor_sync(0xffffffffu, even ? q.y : q.x, 1);
@@ -336,14 +344,14 @@ int grid_for(int64_t threads, int block) {
 
 cudaError_t launch_quantize_q8(const float* x, int64_t rows, int cols, int8_t* codes, uint16_t* scales,
                                cudaStream_t s) {
-    const int64_t n8 = rows * (int64_t)cols / 8;
-    if (n8 == 0) return cudaSuccess;
-    // one group of 8 values a thread and no grid-stride loop: the blocks stream through the SMs as earlier ones
-    // retire, which keeps more loads in flight than a resident grid looping over the rows
-    const int64_t blocks = (n8 + 255) / 256;
+    const int64_t n16 = rows * (int64_t)cols / 16;
+    if (n16 == 0) return cudaSuccess;
+    // one 16-value item a thread and no grid-stride loop: the blocks stream through the SMs as earlier ones retire,
+    // which keeps more loads in flight than a resident grid looping over the rows
+    const int64_t blocks = (n16 + 255) / 256;
     if (blocks > INT32_MAX) return cudaErrorInvalidValue;
-    quantize_q8_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(x), n8, cols,
-                                                        reinterpret_cast<uint2*>(codes), scales);
+    quantize_q8_kernel<<<(unsigned)blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(x), n16,
+                                                        reinterpret_cast<uint4*>(codes), scales);
     return cudaGetLastError();
 }
 

@@ -23,7 +23,7 @@ namespace {
 // the high word maps the fp32 value to an unsigned integer of the same order (-0 taken as +0, so that equal values
 // tie and the lower id wins, as in a float comparison), the low word is 0xFFFF - id.  The largest key is the best
 // expert.  Lane l holds the logits of experts 4l..4l+3 + 128 i (float4 loads) and keeps its own three largest keys in
-// order; each of the K rounds takes the warp's largest head by a butterfly of shuffles and the lane that owned it pops
+// order; each of the K rounds takes the warp's largest head by two warp reductions and the lane that owned it pops
 // it.  Winners leave in descending key order, so a lane that has popped all three rescans its keys below the last one
 // it popped.  Lane k keeps round k's winner; the K weights are exp(l_k - l_1) / sum_j exp(l_j - l_1), summed in k
 // order.
@@ -94,12 +94,12 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     int popped = 0;
     uint64_t mine = 0;
     for (int k = 0; k < K; ++k) {
-        uint64_t best = h0;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const uint64_t o = __shfl_xor_sync(0xffffffffu, best, off);
-            best = o > best ? o : best;
-        }
+        // the warp's largest head as two 32-bit reductions: the largest high word, then the largest low word among
+        // the lanes that hold it (the 64-bit order is lexicographic in the two words)
+        const uint32_t hh = (uint32_t)(h0 >> 32);
+        const uint32_t bh = __reduce_max_sync(0xffffffffu, hh);
+        const uint32_t bl = __reduce_max_sync(0xffffffffu, hh == bh ? (uint32_t)h0 : 0u);
+        const uint64_t best = ((uint64_t)bh << 32) | bl;
         if (lane == k) mine = best;
         if (best == h0) {  // this lane owned the winner (keys are unique): pop it
             h0 = h1;
@@ -179,12 +179,28 @@ __global__ void __launch_bounds__(kGroupThreads) group_scan_kernel(int32_t* __re
     extern __shared__ int32_t hs[];
     __shared__ int warp_sums[32];
     const int total_cells = nchunks * E;
-    for (int i = threadIdx.x; i < total_cells; i += blockDim.x) hs[i] = hist[i];
+    // eight loads in flight a thread (a load-then-store loop would wait out every load's latency in turn)
+    constexpr int kBatch = 8;
+    for (int i0 = 0; i0 < total_cells; i0 += kBatch * kGroupThreads) {
+        int32_t h[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + u * kGroupThreads + threadIdx.x;
+            h[u] = i < total_cells ? hist[i] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int i = i0 + u * kGroupThreads + threadIdx.x;
+            if (i < total_cells) hs[i] = h[u];
+        }
+    }
     __syncthreads();
     const int e = threadIdx.x;
     int c = 0;
-    if (e < E)
+    if (e < E) {
+#pragma unroll 8
         for (int b = 0; b < nchunks; ++b) c += hs[b * E + e];
+    }
     int total;
     const int off = block_exclusive_scan(e < E ? c : 0, warp_sums, &total);
     if (e < E) {
