@@ -19,51 +19,52 @@ namespace smoe {
 namespace {
 
 // ------------------------------------------------------------------------------------------------ route
-// One warp per token.  Every logit becomes a 64-bit key that orders like (value descending, expert id ascending):
-// the high word maps the fp32 value to an unsigned integer of the same order (-0 taken as +0, so that equal values
-// tie and the lower id wins, as in a float comparison), the low word is 0xFFFF - id.  The largest key is the best
-// expert.  Lane l holds the logits of experts 4l..4l+3 + 128 i (float4 loads) and keeps its own three largest keys in
-// order; each of the K rounds takes the warp's largest head by two warp reductions and the lane that owned it pops
-// it.  Winners leave in descending key order, so a lane that has popped all three rescans its keys below the last one
-// it popped.  Lane k keeps round k's winner; the K weights are exp(l_k - l_1) / sum_j exp(l_j - l_1), summed in k
+// One warp per token.  Every logit has a key that orders like (value descending, expert id ascending), as two 32-bit
+// words: the high word maps the fp32 value to an unsigned integer of the same order (-0 taken as +0, so that equal
+// values tie and the lower id wins, as in a float comparison), the low word is 0xFFFF - id.  The largest key is the
+// best expert.  Lane l holds the logits of experts 128 i + 4 l + j (float4 loads; position 4 i + j of the lane), so a
+// lane meets its experts in increasing id order and needs only the high words to order its own keys: with strict
+// comparisons, of two equal values the earlier (lower id, larger key) stays ahead.  It keeps its three largest keys
+// in order; each of the K rounds takes the warp's largest head by two warp reductions (the largest high word, then
+// the largest low word among the lanes holding it) and the lane that owned it pops it.  Winners leave in descending
+// key order, so a lane that has popped all three rescans its keys below the last one it popped.  Lane k keeps round
+// k's winner; the K weights are exp(l_k - l_1) / sum_j exp(l_j - l_1), summed in k order.  A high word of 0 marks an
+// empty place (an expert id >= E); the only value it also stands for is one NaN bit pattern, and NaN logits have no
 // order.
-__device__ __forceinline__ uint64_t route_key(float v, int e) {
+__device__ __forceinline__ uint32_t key_hi(float v) {
     if (v == 0.0f) v = 0.0f;  // -0 -> +0
     const uint32_t b = __float_as_uint(v);
-    const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    return ((uint64_t)o << 32) | (uint32_t)(0xFFFF - e);
+    return b ^ ((uint32_t)((int32_t)b >> 31) | 0x80000000u);  // negative: ~b; else b | sign bit
 }
-__device__ __forceinline__ float key_value(uint64_t k) {
-    const uint32_t o = (uint32_t)(k >> 32);
+__device__ __forceinline__ float key_value(uint32_t o) {
     return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
-__device__ __forceinline__ int key_id(uint64_t k) { return 0xFFFF - (int)(k & 0xFFFFu); }
 
-// the lane's three largest keys below `bound` among kv (0 = empty), in order
-template <int NV>
-__device__ __forceinline__ void top3(const uint64_t (&kv)[NV], uint64_t bound, uint64_t& a, uint64_t& b,
-                                     uint64_t& c) {
-    a = b = c = 0;
+// The lane's three largest keys (a >= b >= c as high word h and low word l; h = 0: none), among its places after
+// (below) the key (bh, bl) when kBounded, else among all.  Place p holds high word kh[p] and low word lo0 - off(p).
+template <int VPL, bool kBounded>
+__device__ __forceinline__ void lane_top3(const uint32_t (&kh)[VPL], uint32_t lo0, uint32_t bh, uint32_t bl,
+                                          uint32_t& ah, uint32_t& al, uint32_t& bh2, uint32_t& bl2, uint32_t& ch,
+                                          uint32_t& cl) {
+    ah = bh2 = ch = 0u;
+    al = bl2 = cl = 0u;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-        const uint64_t k = kv[i] < bound ? kv[i] : 0ull;
-        if (k > c) {
-            if (k > b) {
-                c = b;
-                if (k > a) {
-                    b = a;
-                    a = k;
-                } else {
-                    b = k;
-                }
-            } else {
-                c = k;
-            }
-        }
+    for (int p = 0; p < VPL; ++p) {
+        const uint32_t lo = lo0 - (uint32_t)(128 * (p >> 2) + (p & 3));
+        uint32_t h = kh[p];
+        // below the bound: a smaller high word, or the same one at a later place (a higher id)
+        if (kBounded && !(h < bh || (h == bh && lo < bl))) h = 0u;
+        const bool ga = h > ah, gb = h > bh2, gc = h > ch;
+        ch = gb ? bh2 : (gc ? h : ch);
+        cl = gb ? bl2 : (gc ? lo : cl);
+        bh2 = ga ? ah : (gb ? h : bh2);
+        bl2 = ga ? al : (gb ? lo : bl2);
+        ah = ga ? h : ah;
+        al = ga ? lo : al;
     }
 }
 
-template <int VPL>
+template <int VPL, bool kFull>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int K,
                                                          int32_t* __restrict__ ids, float* __restrict__ w) {
     constexpr int NQ = VPL / 4;  // float4 loads a lane
@@ -71,50 +72,53 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     const float* lt = logits + t * E;
-    uint64_t kv[VPL];
-    const bool vec = (E & 3) == 0;  // rows 16-byte aligned: E % 4 == 0 (the pointer itself is 16-byte aligned)
+    uint32_t kh[VPL];
+    const bool vec = kFull || (E & 3) == 0;  // rows 16-byte aligned: E % 4 == 0 (the pointer itself is 16-byte aligned)
 #pragma unroll
     for (int i = 0; i < NQ; ++i) {
         const int e0 = 128 * i + 4 * lane;
         float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (vec && e0 + 3 < E) f = __ldg(reinterpret_cast<const float4*>(lt + e0));
+        if (kFull || (vec && e0 + 3 < E)) f = __ldg(reinterpret_cast<const float4*>(lt + e0));
         else if (e0 < E) {
             f.x = __ldg(lt + e0);
             if (e0 + 1 < E) f.y = __ldg(lt + e0 + 1);
             if (e0 + 2 < E) f.z = __ldg(lt + e0 + 2);
             if (e0 + 3 < E) f.w = __ldg(lt + e0 + 3);
         }
-        kv[4 * i + 0] = e0 + 0 < E ? route_key(f.x, e0 + 0) : 0ull;
-        kv[4 * i + 1] = e0 + 1 < E ? route_key(f.y, e0 + 1) : 0ull;
-        kv[4 * i + 2] = e0 + 2 < E ? route_key(f.z, e0 + 2) : 0ull;
-        kv[4 * i + 3] = e0 + 3 < E ? route_key(f.w, e0 + 3) : 0ull;
+        kh[4 * i + 0] = (kFull || e0 + 0 < E) ? key_hi(f.x) : 0u;
+        kh[4 * i + 1] = (kFull || e0 + 1 < E) ? key_hi(f.y) : 0u;
+        kh[4 * i + 2] = (kFull || e0 + 2 < E) ? key_hi(f.z) : 0u;
+        kh[4 * i + 3] = (kFull || e0 + 3 < E) ? key_hi(f.w) : 0u;
     }
-    uint64_t h0, h1, h2;
-    top3(kv, ~0ull, h0, h1, h2);
+    const uint32_t lo0 = 0xFFFFu - 4u * (uint32_t)lane;
+    uint32_t ah, al, bh, bl, ch, cl;
+    lane_top3<VPL, false>(kh, lo0, 0u, 0u, ah, al, bh, bl, ch, cl);
     int popped = 0;
-    uint64_t mine = 0;
+    uint32_t mine_h = 0u, mine_l = 0u;
     for (int k = 0; k < K; ++k) {
-        // the warp's largest head as two 32-bit reductions: the largest high word, then the largest low word among
-        // the lanes that hold it (the 64-bit order is lexicographic in the two words)
-        const uint32_t hh = (uint32_t)(h0 >> 32);
-        const uint32_t bh = __reduce_max_sync(0xffffffffu, hh);
-        const uint32_t bl = __reduce_max_sync(0xffffffffu, hh == bh ? (uint32_t)h0 : 0u);
-        const uint64_t best = ((uint64_t)bh << 32) | bl;
-        if (lane == k) mine = best;
-        if (best == h0) {  // this lane owned the winner (keys are unique): pop it
-            h0 = h1;
-            h1 = h2;
-            h2 = 0;
-            if (++popped % 3 == 0) top3(kv, best, h0, h1, h2);
+        const uint32_t wh = __reduce_max_sync(0xffffffffu, ah);
+        const uint32_t wl = __reduce_max_sync(0xffffffffu, ah == wh ? al : 0u);
+        if (lane == k) {
+            mine_h = wh;
+            mine_l = wl;
+        }
+        if (ah == wh && al == wl) {  // this lane owned the winner (keys are unique): pop it
+            ah = bh;
+            al = bl;
+            bh = ch;
+            bl = cl;
+            ch = 0u;
+            cl = 0u;
+            if (++popped % 3 == 0) lane_top3<VPL, true>(kh, lo0, wh, wl, ah, al, bh, bl, ch, cl);
         }
     }
-    const float lmax = key_value(__shfl_sync(0xffffffffu, mine, 0));
-    const float mv = key_value(mine);
+    const float lmax = key_value(__shfl_sync(0xffffffffu, mine_h, 0));
+    const float mv = key_value(mine_h);
     const float ex = lane < K ? expf(mv - lmax) : 0.0f;
     float sum = 0.0f;
     for (int k = 0; k < K; ++k) sum += __shfl_sync(0xffffffffu, ex, k);
     if (lane < K) {
-        ids[t * K + lane] = key_id(mine);
+        ids[t * K + lane] = 0xFFFF - (int)mine_l;
         w[t * K + lane] = __fdiv_rn(ex, sum);
     }
 }
@@ -318,10 +322,15 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int K, int3
                               cudaStream_t s) {
     const int warps = 8;
     const dim3 grid((unsigned)((T + warps - 1) / warps)), block(32 * warps);
-    if (E <= 128) route_topk_kernel<4><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
-    else if (E <= 256) route_topk_kernel<8><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
-    else if (E <= 512) route_topk_kernel<16><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
-    else route_topk_kernel<32><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
+    // E a whole number of 128-expert rows: every place of every lane holds an expert (no range checks)
+    if (E == 128) route_topk_kernel<4, true><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
+    else if (E == 256) route_topk_kernel<8, true><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
+    else if (E == 512) route_topk_kernel<16, true><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
+    else if (E == 1024) route_topk_kernel<32, true><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
+    else if (E <= 128) route_topk_kernel<4, false><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
+    else if (E <= 256) route_topk_kernel<8, false><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
+    else if (E <= 512) route_topk_kernel<16, false><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
+    else route_topk_kernel<32, false><<<grid, block, 0, s>>>(logits, T, E, K, ids, w);
     return cudaGetLastError();
 }
 

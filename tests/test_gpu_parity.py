@@ -92,9 +92,12 @@ def test_route_edge_cases(B):
         assert np.array_equal(ids, ids_o)
         assert np.all(np.abs(w - w_o) <= 2e-6 * w_o)
     rng = np.random.default_rng(7)
-    for E, K in ((1000, 10), (33, 32), (512, 1), (2, 2), (1024, 8)):
+    # every kernel form: E = 128, 256, 512, 1024 fill every lane's places; the others leave some empty
+    for E, K in ((1000, 10), (33, 32), (512, 1), (2, 2), (1024, 8), (128, 10), (256, 8), (200, 10), (1024, 32)):
         lg = (rng.standard_normal((67, E)) * 0.3).astype(np.float32)
         lg[5, :] = np.round(lg[5, :] * 4) / 4     # many exact ties
+        lg[6, :] = 0.5                            # all tied: ids 0..K-1, several of them in one lane
+        lg[7, ::2] = -0.0                         # -0 and +0 tie
         ids, w = gpu_route(B, lg, K)
         ids_o, w_o = oracle.route(lg, K)
         assert np.array_equal(ids, ids_o), (E, K)
