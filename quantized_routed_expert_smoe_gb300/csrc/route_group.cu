@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     const uint32_t lo0 = 0xFFFFu - 4u * (uint32_t)lane;
     uint32_t ah, al, bh, bl, ch, cl;
     lane_top3<VPL, false>(kh, lo0, 0u, 0u, ah, al, bh, bl, ch, cl);
-    int popped = 0;
+    int left = 3;  // heads the lane holds before it must rescan
     uint32_t mine_h = 0u, mine_l = 0u;
     for (int k = 0; k < K; ++k) {
         const uint32_t wh = __reduce_max_sync(0xffffffffu, ah);
@@ -109,7 +109,10 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
             bl = cl;
             ch = 0u;
             cl = 0u;
-            if (++popped % 3 == 0) lane_top3<VPL, true>(kh, lo0, wh, wl, ah, al, bh, bl, ch, cl);
+            if (--left == 0) {
+                lane_top3<VPL, true>(kh, lo0, wh, wl, ah, al, bh, bl, ch, cl);
+                left = 3;
+            }
         }
     }
     const float lmax = key_value(__shfl_sync(0xffffffffu, mine_h, 0));
@@ -246,16 +249,20 @@ __global__ void __launch_bounds__(kGroupThreads) group_scatter_kernel(const int3
     int32_t* run = sm;                                            // [E]
     uint16_t* wcnt = reinterpret_cast<uint16_t*>(sm + E);         // [32][E]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t p0 = (int64_t)blockIdx.x * chunk, p1 = min(n, p0 + chunk);
+    // the first round's ids are loaded before the tables are set up, each later round's during the round before
+    int32_t e_next = p0 + threadIdx.x < p1 ? ids[p0 + threadIdx.x] : -1;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         run[e] = hist[(int64_t)blockIdx.x * E + e];
         for (int w2 = 0; w2 < 32; ++w2) wcnt[w2 * E + e] = 0;
     }
     __syncthreads();
-    const int64_t p0 = (int64_t)blockIdx.x * chunk, p1 = min(n, p0 + chunk);
     const uint32_t lt_mask = (1u << lane) - 1u;
     for (int64_t base = p0; base < p1; base += blockDim.x) {
         const int64_t p = base + threadIdx.x;
-        int32_t e = p < p1 ? ids[p] : -1;
+        int32_t e = e_next;
+        const int64_t pn = p + blockDim.x;
+        e_next = pn < p1 ? ids[pn] : -1;
         if (e >= E) e = -1;
         if (e < -1) e = -1;
         const uint32_t peers = __match_any_sync(0xffffffffu, e);
