@@ -244,6 +244,19 @@ smoe_status smoe_experts_down(const uint16_t* hop, int32_t* tiles, int64_t n, in
 smoe_status smoe_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H, float* y,
                          void* stream);
 
+/* Steps 6 and 7 with a narrow Dm (not the pages' form, which keeps the down rows in fp32; an option for layers whose
+ * down outputs fit fp16): the down product stores each row as fp16, rounded to nearest from the same fp32 value that
+ * smoe_experts_down writes (a value beyond the fp16 range becomes +-inf), and the combine reads fp16 rows.  This
+ * halves the bytes of Dm that the down product writes and the combine reads again (839 MB each way at T=8192,
+ * H=2560, K=10); each term of a token's sum then carries one more fp16 rounding (relative 2^-11 at most).
+ *   smoe_experts_down_h: arguments as smoe_experts_down; dm_h fp16 bits [n][H] out.
+ *   smoe_combine_h: arguments as smoe_combine, with dm_h fp16 bits [n][H]; the sum is fp32 in k order of the values
+ *   widened from fp16.  H % 8 == 0. */
+smoe_status smoe_experts_down_h(const uint16_t* hop, int32_t* tiles, int64_t n, int E, const uint8_t* wd, int H,
+                                int F, uint16_t* dm_h, void* stream);
+smoe_status smoe_combine_h(const uint16_t* dm_h, const int32_t* slot, const float* w, int64_t T, int K, int H,
+                           float* y, void* stream);
+
 /* Step 1 with the router projection fused in (the logits are never written).  Page "src/prefill/prefill.cpp",
  * Prefill::run, MoE half: the router is a BF16 projection of the hidden state, with the low part of its BF16 copy,
  * followed by route().  Here

@@ -73,6 +73,10 @@ _SIGS = {
                            ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_combine": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                       ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_experts_down_h": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p,
+                             ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "smoe_combine_h": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                        ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_router_topk": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "smoe_router_work_bytes": ([ctypes.c_int64, ctypes.c_int], ctypes.c_size_t),
@@ -302,6 +306,22 @@ def smoe_combine(dm, slot, w, y, stream=None):
         _dev(y, torch.float32, "y"), _stream(stream)))
 
 
+def smoe_experts_down_h(hop, tiles, n, E, wd, H, F, dm_h, stream=None):
+    """smoe_experts_down with the rows stored as fp16 (dm_h torch.float16 [n][H])."""
+    _check("smoe_experts_down_h", load_library().smoe_experts_down_h(
+        _dev(hop, torch.float16, "hop"), _dev(tiles, torch.int32, "tiles"), n, E, _dev(wd, torch.uint8, "wd"), H, F,
+        _dev(dm_h, torch.float16, "dm_h"), _stream(stream)))
+
+
+def smoe_combine_h(dm_h, slot, w, y, stream=None):
+    """smoe_combine from fp16 down rows (dm_h torch.float16 [n][H])."""
+    T, K = w.shape
+    H = y.shape[1]
+    _check("smoe_combine_h", load_library().smoe_combine_h(
+        _dev(dm_h, torch.float16, "dm_h"), _dev(slot, torch.int32, "slot"), _dev(w, torch.float32, "w"), T, K, H,
+        _dev(y, torch.float32, "y"), _stream(stream)))
+
+
 def router_work_bytes(T: int, H: int) -> int:
     return int(load_library().smoe_router_work_bytes(T, H))
 
@@ -346,11 +366,16 @@ class SmoeBlock:
     itself (smoe_router_topk) and run() ignores its logits argument.
 
     fused: run gate/up, SwiGLU and the requantisation as one product (smoe_experts_gateup_swiglu, the gate/up weights
-    packed interleaved); GU is then never written."""
+    packed interleaved); GU is then never written.
+
+    narrow_dm: keep the down rows Dm in fp16 (smoe_experts_down_h / smoe_combine_h) instead of fp32, the pages' form;
+    not with a shared expert."""
 
     def __init__(self, T: int, H: int, E: int, K: int, F: int, wgu_c, wgu_s, wd_c, wd_s, device="cuda",
-                 shared=None, router=None, fused=False):
+                 shared=None, router=None, fused=False, narrow_dm=False):
         load_library()
+        if narrow_dm and shared is not None:
+            raise ValueError("narrow_dm: the shared-expert combine reads fp32 down rows")
         device_check()
         self.T, self.H, self.E, self.K, self.F = T, H, E, K, F
         dev = torch.device(device)
@@ -377,7 +402,8 @@ class SmoeBlock:
         self.hc = e(n, F, dt=torch.int8)
         self.hs = e(n, F // 32, dt=torch.int16)
         self.hop = e(2, max(n, 1), F, dt=torch.float16)
-        self.dm = e(n, H, dt=torch.float32)
+        self.narrow_dm = bool(narrow_dm)
+        self.dm = e(n, H, dt=torch.float16 if self.narrow_dm else torch.float32)
         self.y = e(T, H, dt=torch.float32)
         self.router = None
         if router is not None:
@@ -438,6 +464,10 @@ class SmoeBlock:
         else:
             smoe_experts_gateup(self.xop, self.tiles, self.n, self.E, self.wgu, self.H, self.F, self.gu, stream)
             smoe_swiglu_requant(self.gu, self.hc, self.hs, self.hop, stream)
+        if self.narrow_dm:
+            smoe_experts_down_h(self.hop, self.tiles, self.n, self.E, self.wd, self.H, self.F, self.dm, stream)
+            smoe_combine_h(self.dm, self.slot, self.w, y, stream)
+            return y
         smoe_experts_down(self.hop, self.tiles, self.n, self.E, self.wd, self.H, self.F, self.dm, stream)
         if not self.shared:
             smoe_combine(self.dm, self.slot, self.w, y, stream)

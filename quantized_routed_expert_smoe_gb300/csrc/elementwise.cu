@@ -202,6 +202,33 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
     reinterpret_cast<float4*>(y + t * H)[o4] = acc;
 }
 
+// Step 7 from fp16 down rows (the narrow form of Dm): Y[t][o] = sum_k w[t][k] * float(dm[slot[t*K+k]][o]), fp32 fmaf
+// in k order.  Block (t, y): 128 threads, 8 outputs each (one 16-byte load of 8 fp16 values a row).
+__global__ void __launch_bounds__(128) combine_h_kernel(const uint4* __restrict__ dm, const int32_t* __restrict__ slot,
+                                                        const float* __restrict__ w, int K, int H, int64_t n,
+                                                        float* __restrict__ y) {
+    const int64_t t = blockIdx.x;
+    const int o8 = blockIdx.y * blockDim.x + threadIdx.x;
+    if (8 * o8 >= H) return;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k = 0; k < K; ++k) {
+        const int32_t r = __ldg(slot + t * K + k);
+        const float wk = __ldg(w + t * K + k);
+        if (r < 0 || r >= n) continue;
+        const uint4 d = __ldcs(dm + (int64_t)r * (H / 8) + o8);
+        const uint32_t v[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v[i]));
+            acc[2 * i] = fmaf(wk, f.x, acc[2 * i]);
+            acc[2 * i + 1] = fmaf(wk, f.y, acc[2 * i + 1]);
+        }
+    }
+    float4* yo = reinterpret_cast<float4*>(y + t * H) + 2 * o8;
+    yo[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    yo[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
 // The shared expert's scalar gate (page "src/prefill/prefill.cpp", Prefill::run, MoE half: "the shared expert and
 // its scalar gate", a projection of the token onto one row): sg[t] = 1 / (1 + exp(-(x[t] . w_sg))), the dot product
 // in fp32 (lane l sums the float4s l, l + 32, ... of the row, then a butterfly).  One warp per token.
@@ -385,6 +412,14 @@ cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w,
     if (T == 0) return cudaSuccess;
     const dim3 grid((unsigned)T, (unsigned)((H / 4 + 127) / 128));
     combine_kernel<<<grid, 128, 0, s>>>(dm, slot, w, K, H, T * (int64_t)K, ds, sg, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine_h(const uint16_t* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,
+                             float* y, cudaStream_t s) {
+    if (T == 0) return cudaSuccess;
+    const dim3 grid((unsigned)T, (unsigned)((H / 8 + 127) / 128));
+    combine_h_kernel<<<grid, 128, 0, s>>>(reinterpret_cast<const uint4*>(dm), slot, w, K, H, T * (int64_t)K, y);
     return cudaGetLastError();
 }
 

@@ -788,7 +788,21 @@ __global__ void __launch_bounds__(kThreads, 1) experts_gemm_kernel(const Experts
             auto owned = [&](int i, int k) {
                 return stacked ? (2 * i + (k >> 4)) < kMaxStackN / 48 : (i < mine || (half && i == mine && k < 16));
             };
-            if (p.hc == nullptr) {
+            if (p.hc == nullptr && p.out_h != nullptr) {
+                if (!ok) break;
+                // ------------------------------------------------------------ epilogue: fp16 rows out (round to
+                // nearest; a value beyond the fp16 range becomes +-inf)
+                uint16_t* outcol = p.out_h + (t.m0 + mrow);
+#pragma unroll
+                for (int i = 0; i < kChunks; ++i) {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int col = column(i, k);
+                        if (owned(i, k) && col < t.rows)
+                            outcol[(int64_t)(t.row0 + col) * p.a_rows] = __half_as_ushort(__float2half_rn(acc[i][k]));
+                    }
+                }
+            } else if (p.hc == nullptr) {
                 if (!ok) break;
                 // ------------------------------------------------------------ epilogue: fp32 rows out
                 float* outcol = p.out + (t.m0 + mrow);

@@ -198,6 +198,18 @@ smoe_status smoe_experts_down(const uint16_t* hop, int32_t* tiles, int64_t n, in
     return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
 }
 
+smoe_status smoe_experts_down_h(const uint16_t* hop, int32_t* tiles, int64_t n, int E, const uint8_t* wd, int H,
+                                int F, uint16_t* dm_h, void* stream) {
+    const smoe_status st = check_gemm_shape(n, E, H, F);
+    if (st != SMOE_OK) return st;
+    if (n == 0) return SMOE_OK;
+    if (!aligned16(hop) || !aligned16(tiles) || !aligned16(wd) || !aligned16(dm_h)) return SMOE_ERR_ARG;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    smoe::ExpertsGemmArgs a{hop, tiles, wd, H, F, nullptr, n, E, false, 1, nullptr, nullptr, nullptr};
+    a.out_h = dm_h;
+    return launch_status(smoe::launch_experts_gemm(a, smoe_max_tiles(n, E), (cudaStream_t)stream));
+}
+
 size_t smoe_experts_q8_work_bytes(int64_t n, int E, int H, int F) {
     if (n < 0 || E < 1 || H < 1 || F < 1) return 0;
     // the routed rows in operand form (fp16 [2][n][K]), then the packed weights; the larger of the two products
@@ -261,6 +273,16 @@ smoe_status smoe_combine(const float* dm, const int32_t* slot, const float* w, i
     if ((H / 4 + 127) / 128 > kMaxGridY) return SMOE_ERR_UNSUPPORTED;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
     return launch_status(smoe::launch_combine(dm, slot, w, T, K, H, nullptr, nullptr, y, (cudaStream_t)stream));
+}
+
+smoe_status smoe_combine_h(const uint16_t* dm_h, const int32_t* slot, const float* w, int64_t T, int K, int H,
+                           float* y, void* stream) {
+    if (T < 0 || T > INT32_MAX || K < 1 || K > SMOE_MAX_TOPK || H < 8 || H % 8 != 0) return SMOE_ERR_ARG;
+    if (T == 0) return SMOE_OK;
+    if (!aligned16(dm_h) || !aligned16(slot) || !aligned16(w) || !aligned16(y)) return SMOE_ERR_ARG;
+    if ((H / 8 + 127) / 128 > kMaxGridY) return SMOE_ERR_UNSUPPORTED;
+    if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
+    return launch_status(smoe::launch_combine_h(dm_h, slot, w, T, K, H, y, (cudaStream_t)stream));
 }
 
 smoe_status smoe_router_topk(const float* x, const uint16_t* wr, int64_t T, int H, int E, int K, uint16_t* work,

@@ -28,6 +28,8 @@ cudaError_t launch_gather_q8(const int8_t* codes, const uint16_t* scales, int64_
                              const int32_t* src, int64_t n, uint16_t* out, cudaStream_t s);
 cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,
                            const float* ds, const float* sg, float* y, cudaStream_t s);
+cudaError_t launch_combine_h(const uint16_t* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,
+                             float* y, cudaStream_t s);
 cudaError_t launch_router_topk(const float* x, const uint16_t* wr, int64_t T, int H, int E, int K, uint16_t* work,
                                int32_t* ids, float* w, cudaStream_t s);
 cudaError_t launch_shared_gate(const float* x, const float* wsg, int64_t T, int H, float* sg, cudaStream_t s);
@@ -51,6 +53,7 @@ struct ExpertsGemmArgs {
     uint16_t* hs;         // [b_rows][a_rows / 64] fp16 scales
     uint16_t* hop;        // [2][b_rows][a_rows / 2] h in operand form
     int max_tiles = 0;    // entries the tile list holds (set by the launcher): a larger header count is an error
+    uint16_t* out_h = nullptr;  // fp16 rows [b_rows][a_rows] in place of `out` (the down product's narrow form)
 };
 cudaError_t launch_experts_gemm(const ExpertsGemmArgs& a, int64_t max_tiles, cudaStream_t s);
 

@@ -84,6 +84,13 @@ def test_host_side_rejections_need_no_gpu(lib):
     assert lib.smoe_shared_gate(fake, fake, 0, 32, fake, null) == 0  # empty chunk: nothing to do
     assert lib.smoe_combine_shared(fake, fake, fake, 4, 2, 32, odd, fake, fake, null) == ARG
     assert lib.smoe_combine_shared(fake, fake, fake, 4, 2, 32, fake, null, fake, null) == ARG
+    # the narrow Dm: fp16 rows need H % 8 for the combine; misaligned rows; the down product's shape rules
+    assert lib.smoe_combine_h(fake, fake, fake, 4, 2, 36, fake, null) == ARG
+    assert lib.smoe_combine_h(odd, fake, fake, 4, 2, 32, fake, null) == ARG
+    assert lib.smoe_combine_h(fake, fake, fake, 4, 0, 32, fake, null) == ARG
+    assert lib.smoe_combine_h(fake, fake, fake, 0, 2, 32, fake, null) == 0  # empty chunk: nothing to do
+    assert lib.smoe_experts_down_h(fake, fake, 10, 4, fake, 256, 64, odd, null) == ARG
+    assert lib.smoe_experts_down_h(fake, fake, 10, 4, fake, 256, 48, fake, null) == UNSUP
     # router: H % 64, E out of range or not a multiple of 16 (of 32 above 256), K > 16
     assert lib.smoe_router_topk(fake, fake, 4, 96, 64, 2, fake, fake, fake, null) == ARG
     assert lib.smoe_router_topk(fake, fake, 4, 128, 8, 2, fake, fake, fake, null) == ARG

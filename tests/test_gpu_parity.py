@@ -565,6 +565,23 @@ def test_combine_parity(B):
     assert np.all(np.abs(got - want) <= 1e-6 * mag + 1e-30)
 
 
+@pytest.mark.parametrize("T,K,H", [(777, 10, 2560), (5, 3, 8), (33, 7, 1064)])
+def test_combine_h_parity(B, T, K, H):
+    # the combine from fp16 rows: the oracle's sum over the same fp16 values, widened (H = 1064: a partial last block)
+    rng = np.random.default_rng(H + K)
+    n = T * K
+    dm = synth.make_dm(n, H, seed=6).astype(np.float16)
+    slot = rng.permutation(n).astype(np.int32)
+    w = rng.random((T, K)).astype(np.float32)
+    y = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    B.smoe_combine_h(dev(dm), dev(slot), dev(w), y)
+    got = host(y)
+    d = dm.astype(np.float64)
+    want = oracle.combine(d, slot, w.astype(np.float64), T, K, H)
+    mag = np.einsum("tk,tkh->th", np.abs(w.astype(np.float64)), np.abs(d[slot.reshape(T, K)]))
+    assert np.all(np.abs(got - want) <= 1e-6 * mag + 1e-30)
+
+
 # ------------------------------------------------------------------------------------------------ the whole block
 @pytest.mark.parametrize("name", ALL)
 def test_block_parity(B, name):
@@ -604,6 +621,52 @@ def test_block_parity(B, name):
     assert np.all(err <= 2e-3), f"worst err/rms {float(err.max()):.3e} at token {worst}"
     assert np.isfinite(y).all()
     del blk
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["tiny", "t1024", "t8192"])
+def test_block_narrow_dm(B, name):
+    """The block with fp16 down rows: Dm is exactly the fp32 block's Dm rounded to nearest fp16, the fp16 combine is
+    the combine of those values, and (tiny, t1024: every row against the oracle) the output stays within the bar."""
+    cfg = synth.CONFIGS[name]
+    inp = layer_inputs(name)
+    args = (cfg.T, cfg.H, cfg.E, cfg.K, cfg.F, inp["wgu_c"], inp["wgu_s"], inp["wd_c"], inp["wd_s"])
+    b32 = B.SmoeBlock(*args)
+    b16 = B.SmoeBlock(*args, narrow_dm=True)
+    lg, x = dev(inp["logits"]), dev(inp["x"])
+    y32 = host(b32.run(lg, x)).copy()
+    y16 = host(b16.run(lg, x)).astype(np.float64)
+    assert b16.device_status() == (0, 0) and b32.device_status() == (0, 0)
+    dm32 = host(b32.dm)
+    dm16 = host(b16.dm)
+    assert dm16.dtype == np.float16
+    assert np.array_equal(dm16.view(np.uint16), dm32.astype(np.float16).view(np.uint16))
+    T, K, H = cfg.T, cfg.K, cfg.H
+    slot, w = host(b16.slot)[:cfg.n], host(b16.w)
+    d = dm16.astype(np.float64)
+    want = oracle.combine(d, slot, w.astype(np.float64), T, K, H)
+    mag = np.einsum("tk,tkh->th", np.abs(w.astype(np.float64)), np.abs(d[slot.reshape(T, K)]))
+    assert np.all(np.abs(y16 - want) <= 1e-6 * mag + 1e-30)
+    # the narrowing's own effect on the output: each term moves by at most 2^-11 of itself, or 2^-25 absolute below
+    # the fp16 normal range (6.1e-5)
+    d32 = dm32.astype(np.float64)[slot.reshape(T, K)]
+    aw = np.abs(w.astype(np.float64))
+    step = np.einsum("tk,tkh->th", aw, np.maximum(2.0 ** -11 * np.abs(d32), 2.0 ** -25))
+    mag32 = np.einsum("tk,tkh->th", aw, np.abs(d32))
+    assert np.all(np.abs(y16 - y32) <= step * (1 + 1e-6) + 1e-6 * (mag + mag32) + 1e-30)
+    if name != "t8192":
+        y_o, ids_t, w_t, h_o, hc_o, hs_o = oracle.layer_tokens_h(inp, np.arange(T))
+        rows = slot.reshape(T, K)
+        hc_g = host(b16.hc)[rows]
+        hs_g = host(b16.hs).view(np.uint16)[rows]
+        check_h_decisions(hc_g, hs_g, h_o, hc_o, hs_o)
+        ids_o, _ = oracle.route(inp["logits"], K)
+        corr = tie_correction(hc_g, hs_g, hc_o, hs_o, ids_o, w_t, inp["wd_c"], inp["wd_s"])
+        rms = np.sqrt((y_o ** 2).mean(axis=1))
+        err = np.abs(y16 - y_o - corr).max(axis=1) / rms
+        print(f"block {name} with fp16 Dm: every row within {float(err.max()):.3e} * RMS of the oracle")
+        assert np.all(err <= 2e-3), f"worst err/rms {float(err.max()):.3e}"
+    del b16, b32
     torch.cuda.empty_cache()
 
 
