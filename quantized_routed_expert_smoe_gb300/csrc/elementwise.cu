@@ -203,25 +203,39 @@ __global__ void __launch_bounds__(128) combine_kernel(const float* __restrict__ 
 }
 
 // Step 7 from fp16 down rows (the narrow form of Dm): Y[t][o] = sum_k w[t][k] * float(dm[slot[t*K+k]][o]), fp32 fmaf
-// in k order.  Block (t, y): 128 threads, 8 outputs each (one 16-byte load of 8 fp16 values a row).
-__global__ void __launch_bounds__(128) combine_h_kernel(const uint4* __restrict__ dm, const int32_t* __restrict__ slot,
-                                                        const float* __restrict__ w, int K, int H, int64_t n,
-                                                        float* __restrict__ y) {
+// in k order.  Block (t, y): 64 threads, 8 outputs each (one 16-byte load of 8 fp16 values a row); the rows of four
+// k at a time are loaded before they are added, so that each thread keeps four loads in flight.
+constexpr int kCombineHThreads = 64;
+__global__ void __launch_bounds__(kCombineHThreads) combine_h_kernel(const uint4* __restrict__ dm,
+                                                                     const int32_t* __restrict__ slot,
+                                                                     const float* __restrict__ w, int K, int H,
+                                                                     int64_t n, float* __restrict__ y) {
     const int64_t t = blockIdx.x;
     const int o8 = blockIdx.y * blockDim.x + threadIdx.x;
     if (8 * o8 >= H) return;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int k = 0; k < K; ++k) {
-        const int32_t r = __ldg(slot + t * K + k);
-        const float wk = __ldg(w + t * K + k);
-        if (r < 0 || r >= n) continue;
-        const uint4 d = __ldcs(dm + (int64_t)r * (H / 8) + o8);
-        const uint32_t v[4] = {d.x, d.y, d.z, d.w};
+    for (int k0 = 0; k0 < K; k0 += 4) {
+        uint4 d[4];
+        float wk[4];
+        bool ok[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v[i]));
-            acc[2 * i] = fmaf(wk, f.x, acc[2 * i]);
-            acc[2 * i + 1] = fmaf(wk, f.y, acc[2 * i + 1]);
+        for (int j = 0; j < 4; ++j) {
+            const int k = k0 + j;
+            const int32_t r = k < K ? __ldg(slot + t * K + k) : -1;
+            ok[j] = r >= 0 && r < n;  // a pair dropped for an out-of-range id (or past K) contributes nothing
+            wk[j] = ok[j] ? __ldg(w + t * K + k) : 0.0f;
+            d[j] = ok[j] ? __ldcs(dm + (int64_t)r * (H / 8) + o8) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (!ok[j]) continue;
+            const uint32_t v[4] = {d[j].x, d[j].y, d[j].z, d[j].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&v[i]));
+                acc[2 * i] = fmaf(wk[j], f.x, acc[2 * i]);
+                acc[2 * i + 1] = fmaf(wk[j], f.y, acc[2 * i + 1]);
+            }
         }
     }
     float4* yo = reinterpret_cast<float4*>(y + t * H) + 2 * o8;
@@ -418,8 +432,9 @@ cudaError_t launch_combine(const float* dm, const int32_t* slot, const float* w,
 cudaError_t launch_combine_h(const uint16_t* dm, const int32_t* slot, const float* w, int64_t T, int K, int H,
                              float* y, cudaStream_t s) {
     if (T == 0) return cudaSuccess;
-    const dim3 grid((unsigned)T, (unsigned)((H / 8 + 127) / 128));
-    combine_h_kernel<<<grid, 128, 0, s>>>(reinterpret_cast<const uint4*>(dm), slot, w, K, H, T * (int64_t)K, y);
+    const dim3 grid((unsigned)T, (unsigned)((H / 8 + kCombineHThreads - 1) / kCombineHThreads));
+    combine_h_kernel<<<grid, kCombineHThreads, 0, s>>>(reinterpret_cast<const uint4*>(dm), slot, w, K, H,
+                                                       T * (int64_t)K, y);
     return cudaGetLastError();
 }
 

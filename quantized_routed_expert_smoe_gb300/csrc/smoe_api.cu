@@ -280,7 +280,7 @@ smoe_status smoe_combine_h(const uint16_t* dm_h, const int32_t* slot, const floa
     if (T < 0 || T > INT32_MAX || K < 1 || K > SMOE_MAX_TOPK || H < 8 || H % 8 != 0) return SMOE_ERR_ARG;
     if (T == 0) return SMOE_OK;
     if (!aligned16(dm_h) || !aligned16(slot) || !aligned16(w) || !aligned16(y)) return SMOE_ERR_ARG;
-    if ((H / 8 + 127) / 128 > kMaxGridY) return SMOE_ERR_UNSUPPORTED;
+    if ((H / 8 + 63) / 64 > kMaxGridY) return SMOE_ERR_UNSUPPORTED;
     if (!device_is_sm103()) return SMOE_ERR_UNSUPPORTED;
     return launch_status(smoe::launch_combine_h(dm_h, slot, w, T, K, H, y, (cudaStream_t)stream));
 }
