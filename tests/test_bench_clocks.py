@@ -12,6 +12,9 @@ def _line(sm, power_cap=False, thermal=False):
 class _Done:
     stdout = []
 
+    def poll(self):
+        return None
+
     def terminate(self):
         pass
 
