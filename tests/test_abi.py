@@ -155,3 +155,17 @@ def test_binding_fails_loudly_without_library(tmp_path):
 
 def test_build_targets_sm103a_only():
     assert smoe_build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_header_is_plain_c(tmp_path):
+    # the boundary is a C ABI: the header compiles as C99 (no C++ types or overloads leak into it)
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "smoe.h"\nint main(void) { return smoe_max_tiles(0, 1) == 0 ? 0 : 1; }\n')
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I" + os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
