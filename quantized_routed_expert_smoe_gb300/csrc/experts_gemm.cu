@@ -54,9 +54,9 @@
 //                 (128-byte swizzle; pair form: this CTA's half of them) and one bulk copy of the packed weight
 //                 block into a ring slot;
 //   warpgroups 1-3  promoters: add each finished partial into fp32 registers (a TMEM lane a thread, every third
-//                 32-column chunk a warpgroup), then write the fp32 rows -- or, for the fused SwiGLU product (gate
-//                 and up rows interleaved in the packed weights), h = silu(g) * u requantised to q8, planar and in
-//                 operand form;
+//                 32-column chunk a warpgroup), then write the fp32 rows (or, for the down product's narrow form,
+//                 the same values rounded to fp16) -- or, for the fused SwiGLU product (gate and up rows interleaved
+//                 in the packed weights), h = silu(g) * u requantised to q8, planar and in operand form;
 //   warpgroup 4   converters: thread = weight row: decode its 64 weights of the slice into the slice's A buffer in
 //                 tensor memory (three register instructions a column of two weights).
 // Tensor memory (512 columns): 4 A buffers of 32 columns, then the partial buffers in the other 384 -- as many as
